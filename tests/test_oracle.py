@@ -1,0 +1,315 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+None of these tests needs a GPU.  Each pin is chosen so that a plausible slip
+in the oracle (a dropped rule, a wrong sign or offset, a transposed operand, a
+wrong default) fails at least one of them; ``test_planted_mistakes_are_caught``
+checks that claim by planting such slips in the oracle.
+"""
+import glob
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.hstu_oracle as orc
+from oracle.hstu_oracle import (HstuParams, SeqMaskParams, allowed_pair_count, dense_mask,
+                                executed_tile_count, group_of_batch, hstu_attention_forward,
+                                hstu_attention_forward_rows, phy_seqlen_kv, phy_seqlen_q, silu)
+from recommender_attention_gb300 import workloads as W
+from tests.helpers import as_f64, oracle_forward, oracle_params, read_mask_fixture
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def seq(c, u, t, causal, w, f, cross=False, u_kv=None):
+    L_q = c + u + t
+    L_kv = (c + u_kv) if cross else L_q
+    return SeqMaskParams(L_q=L_q, L_kv=L_kv, context=c, targets=t, causal=bool(causal),
+                         local=w, minfull=f, cross=cross)
+
+
+# ---------------------------------------------------------------- lengths, groups
+def test_phy_seqlen_formulas():
+    # README "Masking": phy_seqlen_q = uih + targets + context; the tiny config
+    # (uih 64, 4 targets, context 2) is 70 long.
+    assert phy_seqlen_q(64, 4, 2) == 70
+    assert phy_seqlen_kv(64, 4, 2, cross=False) == 70
+    # cross-attention: phy_seqlen_kv = uih_seqlen_kv + context_len (no targets)
+    assert phy_seqlen_kv(4096, 7, 16, cross=True) == 4112
+    assert W.tiny_batched().lengths_q().tolist() == [70, 70]
+
+
+def test_group_mapping_matches_readme_example():
+    lines = dict(l.split(None, 1) for l in open(os.path.join(GOLDEN, "group_example.txt"))
+                 if l.strip() and not l.startswith("#"))
+    batch, groups = int(lines["batch"]), int(lines["groups"])
+    seqlens = [int(x) for x in lines["seqlens"].split(",")]
+    expect = [int(x) for x in lines["g_max_seqlens"].split(",")]
+    seqlens = seqlens + [seqlens[-1]] * (batch - len(seqlens))
+    got = [0] * groups
+    for b in range(batch):
+        g = group_of_batch(b, batch, groups)
+        got[g] = max(got[g], seqlens[b])
+    assert got == expect
+    # the other plausible mapping (b % G) is not consistent with the example
+    alt = [max(seqlens[b] for b in range(batch) if b % groups == g) for g in range(groups)]
+    assert alt != expect
+    with pytest.raises(ValueError):
+        group_of_batch(0, 10, 3)
+
+
+# ---------------------------------------------------------------- the mask
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(GOLDEN, "mask_*.txt"))))
+def test_mask_hand_fixtures(path):
+    p, expect = read_mask_fixture(path)
+    sp = seq(p["context"], p["uih"], p["targets"], p["causal"], p["local"], p["minfull"],
+             cross=bool(p["cross"]), u_kv=p.get("uih_kv"))
+    got = dense_mask(sp)
+    assert got.shape == expect.shape
+    assert np.array_equal(got, expect), "\n" + "\n".join(
+        "".join("X" if x else "." for x in r) for r in got)
+
+
+def _grid():
+    for c, u, t, causal, w, f in itertools.product([0, 1, 3], [0, 1, 4, 9], [0, 1, 3], [0, 1],
+                                                  [0, 1, 2, 5], [0, 1, 3]):
+        yield seq(c, u, t, causal, w, f)
+        for u_kv in (0, 2, 7, 12):
+            yield seq(c, u, t, causal, w, f, cross=True, u_kv=u_kv)
+
+
+def test_mask_rule_invariants_bruteforce():
+    """Each stated rule, checked as its own property on every tiny case."""
+    n = 0
+    for sp in _grid():
+        m = dense_mask(sp)
+        c, u, t, u_kv = sp.context, sp.uih_q, sp.targets, sp.uih_kv
+        L_q, L_kv = sp.L_q, sp.L_kv
+        assert m.shape == (L_q, L_kv)
+        # contextual keys: visible to every query
+        assert m[:, :c].all()
+        # target keys (self-attention): visible to their own row and no other
+        for j in range(c + u_kv, L_kv):
+            assert m[j, j] and m[:, j].sum() == 1
+        # contextual rows: ctx + every UIH key, never a target
+        assert m[:c, :c + u_kv].all() and not m[:c, c + u_kv:].any()
+        for i in range(c, L_q):
+            x_i = (i - c) + (u_kv - u) if i < c + u else u_kv
+            uih_ok = [x for x in range(u_kv) if m[i, c + x]]
+            if sp.causal:
+                # no UIH or target row sees a later UIH position
+                assert all(x <= x_i for x in uih_ok)
+            full = sp.minfull > 0 and x_i >= u_kv - sp.minfull
+            if sp.local > 0 and not full:
+                # "the N most recent keys": at most W+1 UIH keys when causal
+                # (self + W before it), and they are the most recent ones
+                if sp.causal:
+                    assert len(uih_ok) <= sp.local + 1
+                if uih_ok:
+                    assert uih_ok == list(range(uih_ok[0], uih_ok[-1] + 1))
+                    assert all(abs(x_i - x) <= sp.local for x in uih_ok)
+            else:
+                # min-full rows / no local window: the full (causal) UIH history
+                want = [x for x in range(u_kv) if (x <= x_i or not sp.causal)]
+                assert uih_ok == want
+            # UIH rows never see target keys other than themselves
+            assert not any(m[i, j] for j in range(c + u_kv, L_kv) if j != i)
+        n += 1
+    assert n > 1000
+
+
+@pytest.mark.parametrize("c,u,t", [(0, 1, 0), (2, 64, 4), (6, 400, 16), (3, 17, 5), (0, 50, 0)])
+def test_mask_closed_form_count_full_causal(c, u, t):
+    # W = 0, F = 0, causal, self: ctx rows see c+u keys, UIH row x sees c + x+1,
+    # a target row sees c + u + 1 (itself)
+    closed = c * (c + u) + c * u + u * (u + 1) // 2 + t * (c + u + 1)
+    assert dense_mask(seq(c, u, t, True, 0, 0)).sum() == closed
+    # no mask component at all: every non-target key for every row + target diagonal
+    m = dense_mask(seq(0, u, 0, False, 0, 0))
+    assert m.all()
+
+
+def test_config_pair_counts():
+    # useful (i, j) pairs of the three small configs under these readings
+    for fn, expect in ((W.tiny_batched, 4492), (W.jagged_readme, 932088),
+                       (W.batched_default, 771936)):
+        w = fn()
+        got = allowed_pair_count(w.seq_offsets_q(), w.seq_offsets_kv(), w.num_targets(),
+                                 oracle_params(w), w.nhead)
+        assert got == expect, w.name
+
+
+def test_executed_tiles_full_causal():
+    # causal, no other component, L = 128 n: n(n+1)/2 tiles per (b, h)
+    for n in (1, 2, 5):
+        p = HstuParams(causal=True)
+        off = np.array([0, 128 * n, 128 * n + 128 * n], dtype=np.int32)
+        assert executed_tile_count(off, None, None, p, nhead=3) == 2 * 3 * n * (n + 1) // 2
+    # a window of 5 touches only the diagonal tile and its left neighbour
+    p = HstuParams(causal=True, local_len=[5])
+    off = np.array([0, 128 * 4], dtype=np.int32)
+    assert executed_tile_count(off, None, None, p, nhead=1) == 1 + 2 * 3
+
+
+# ---------------------------------------------------------------- arithmetic
+def test_silu_pin_from_article():
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "silu_mass.txt")):
+        if line.strip() and not line.startswith("#"):
+            parts = line.split()
+            vals[(parts[0], parts[1])] = parts[-1]
+    assert round(1.0 / (1.0 + math.exp(-2.0)), 4) == float(vals[("sigma2", "0.8808")])
+    # s = alpha * q.k = 2 on every key: q = k = 4 e_0, alpha = 1/8 (hdim 64).
+    for k_keys in (3, 20):
+        L = 25
+        q = np.zeros((L, 1, 64)); q[:, 0, 0] = 4.0
+        k = q.copy()
+        v = np.ones((L, 1, 64))
+        p = HstuParams(alpha=1.0 / 8, attn_scale=[1.0], causal=True)
+        o, _ = hstu_attention_forward(q, k, v, [0, L], None, None, p)
+        # causal, no other component: row k-1 sees exactly k keys
+        mass = o[k_keys - 1, 0, 0]
+        assert f"{mass:.2f}" == vals[("k", str(k_keys))]
+
+
+def test_silu_all_components_off_equals_dense_torch():
+    rng = np.random.default_rng(3)
+    L, H, D = 37, 2, 16
+    q, k, v = (rng.standard_normal((L, H, D)) for _ in range(3))
+    p = HstuParams(alpha=0.3, attn_scale=[0.05], causal=False)
+    o, lse = hstu_attention_forward(q, k, v, [0, L], None, None, p)
+    assert lse is None
+    tq, tk, tv = (torch.from_numpy(x).double().transpose(0, 1) for x in (q, k, v))
+    ref = 0.05 * torch.nn.functional.silu(0.3 * tq @ tk.transpose(1, 2)) @ tv
+    np.testing.assert_allclose(o, ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_softmax_causal_only_equals_sdpa():
+    rng = np.random.default_rng(5)
+    L, H, D = 41, 3, 32
+    q, k, v = (rng.standard_normal((L, H, D)) for _ in range(3))
+    p = HstuParams(alpha=0.2, attn_scale=[0.5], causal=True, softmax=True)
+    o, lse = hstu_attention_forward(q, k, v, [0, L], None, None, p)
+    tq, tk, tv = (torch.from_numpy(x).double().transpose(0, 1) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True,
+                                                           scale=0.2)
+    np.testing.assert_allclose(o, 0.5 * ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
+    scores = 0.2 * tq @ tk.transpose(1, 2)
+    scores = scores.masked_fill(~torch.ones(L, L, dtype=torch.bool).tril(), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(scores, dim=-1).numpy(), rtol=1e-12)
+
+
+def test_defaults_alpha_and_attn_scale():
+    # alpha 0 -> 1/sqrt(hdim_qk); attn_scale 0 -> 1/max UIH of the group
+    rng = np.random.default_rng(9)
+    w = W.random_small(4, cross=False).with_(num_groups=1, batch=3, uih_q=[5, 9, 7],
+                                             targets=[1, 0, 2], context_len=[2],
+                                             local_len=[0], minfull_len=[0], max_uih_len=[0],
+                                             attn_scale=[0.0], alpha=0.0, causal=False)
+    q, k, v = (rng.standard_normal((w.total_q, 1, 16)) for _ in range(3))
+    o_def, _ = hstu_attention_forward(q, k, v, w.seq_offsets_q(), None, w.num_targets(),
+                                      oracle_params(w))
+    explicit = oracle_params(w)
+    explicit.alpha = 0.25
+    explicit.attn_scale = [1.0 / 9]
+    o_exp, _ = hstu_attention_forward(q, k, v, w.seq_offsets_q(), None, w.num_targets(),
+                                      explicit)
+    np.testing.assert_allclose(o_def, o_exp, rtol=1e-13)
+    # the max_uih override replaces the data maximum
+    ovr = oracle_params(w)
+    ovr.max_uih_len = [20]
+    o_ovr, _ = hstu_attention_forward(q, k, v, w.seq_offsets_q(), None, w.num_targets(), ovr)
+    np.testing.assert_allclose(o_ovr * 20, o_def * 9, rtol=1e-12)
+
+
+def test_empty_rows_give_zero_and_minus_inf():
+    # cross-attention with fewer key UIH than query UIH and no context: the
+    # earliest query UIH rows sit before the first key and see nothing
+    sp = seq(0, 6, 0, True, 0, 0, cross=True, u_kv=3)
+    m = dense_mask(sp)
+    assert not m[:3].any() and m[3:].any()
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((6, 1, 8)); k = rng.standard_normal((3, 1, 8)); v = rng.standard_normal((3, 1, 8))
+    for sm in (False, True):
+        p = HstuParams(causal=True, softmax=sm, attn_scale=[1.0])
+        o, lse = hstu_attention_forward(q, k, v, [0, 6], [0, 3], None, p)
+        assert np.all(o[:3] == 0)
+        assert np.all(np.abs(o[3:]).sum(-1) > 0)
+        if sm:
+            assert np.all(np.isneginf(lse[0, :3])) and np.all(np.isfinite(lse[0, 3:]))
+
+
+def test_rows_function_matches_full_forward():
+    for sm in (False, True):
+        w = W.random_small(11, softmax=sm, cross=True, max_uih=40)
+        q, k, v = w.tensors()
+        o, lse = oracle_forward(w, q, k, v)
+        off = w.seq_offsets_q()
+        for b in range(w.batch):
+            L = off[b + 1] - off[b]
+            rows = np.arange(0, L, 3)
+            for h in range(w.nhead):
+                ob, lb = hstu_attention_forward_rows(as_f64(q), as_f64(k), as_f64(v), off,
+                                                     w.seq_offsets_kv(), w.num_targets(),
+                                                     oracle_params(w), b, h, rows)
+                np.testing.assert_array_equal(ob, o[off[b] + rows, h])
+                if sm:
+                    np.testing.assert_array_equal(lb, lse[h, off[b] + rows])
+
+
+def test_input_validation():
+    p = HstuParams(context_len=[5])
+    q = np.zeros((4, 1, 8))
+    with pytest.raises(ValueError):
+        hstu_attention_forward(q, q, q, [0, 4], None, [0], p)
+
+
+# ---------------------------------------------------------------- planted slips
+def _pins_pass():
+    try:
+        for path in sorted(glob.glob(os.path.join(GOLDEN, "mask_*.txt"))):
+            test_mask_hand_fixtures(path)
+        test_mask_rule_invariants_bruteforce()
+        test_config_pair_counts()
+        test_silu_pin_from_article()
+        test_silu_all_components_off_equals_dense_torch()
+        test_softmax_causal_only_equals_sdpa()
+        test_empty_rows_give_zero_and_minus_inf()
+    except AssertionError:
+        return False
+    return True
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    assert _pins_pass()
+    # 1. window off by one
+    monkeypatch.setattr(orc, "WINDOW_KEEPS_DISTANCE_EQUAL_W", False)
+    assert not _pins_pass()
+    monkeypatch.undo()
+    # 2. SiLU with the wrong sign inside the sigmoid
+    monkeypatch.setattr(orc, "silu", lambda s: s / (1.0 + np.exp(s)))
+    assert not _pins_pass()
+    monkeypatch.undo()
+    # 3. a mask without the target-key rule (targets visible like UIH keys)
+    real_mask_rows = orc.mask_rows
+
+    def no_target_rule(p, rows):
+        m = real_mask_rows(p, rows)
+        if not p.cross:
+            tgt = np.arange(p.L_kv) >= p.context + p.uih_kv
+            m[:, tgt] = np.asarray(rows)[:, None] >= np.arange(p.L_kv)[None, tgt]
+        return m
+
+    monkeypatch.setattr(orc, "mask_rows", no_target_rule)
+    assert not _pins_pass()
+    monkeypatch.undo()
+    # 4. K transposed against Q in the head product (Q K instead of Q K^T)
+    real_head = orc._head_forward
+    monkeypatch.setattr(orc, "_head_forward",
+                        lambda q, k, v, a, al, sc, sm: real_head(q, k[::-1].copy(), v, a, al, sc, sm))
+    assert not _pins_pass()
+    monkeypatch.undo()
+    assert _pins_pass()
