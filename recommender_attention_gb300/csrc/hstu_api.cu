@@ -1,0 +1,356 @@
+// C ABI of the HSTU forward: argument validation, workspace planning, TMA
+// tensor-map encoding and the launches (scheduler -> forward -> combine).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "hstu_attn.h"
+#include "hstu_common.cuh"
+#include "hstu_launch.h"
+
+using namespace hstu;
+
+namespace {
+
+static_assert(HSTU_MAX_GROUPS == kMaxGroups, "group slots");
+static_assert(HSTU_MAX_SPLITS == kMaxSplits, "split slots");
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int sm_count_current() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+int64_t packed_or(int64_t stride, int64_t packed) { return stride == 0 ? packed : stride; }
+
+hstu_status validate(const hstu_fwd_args* a) {
+  if (!a) return HSTU_ERR_INVALID_ARG;
+  if (a->dtype != HSTU_DTYPE_FP16 && a->dtype != HSTU_DTYPE_BF16) return HSTU_ERR_UNSUPPORTED;
+  if (a->batch < 1 || a->nhead < 1 || a->total_q < 1 || a->total_kv < 1) return HSTU_ERR_INVALID_ARG;
+  if (a->hdim_qk != 64 && a->hdim_qk != 128 && a->hdim_qk != 256) return HSTU_ERR_UNSUPPORTED;
+  if (a->hdim_v != a->hdim_qk) return HSTU_ERR_UNSUPPORTED;
+  if (a->num_groups < 1 || a->batch % a->num_groups != 0) return HSTU_ERR_INVALID_ARG;
+  if (a->num_groups > kMaxGroups) return HSTU_ERR_UNSUPPORTED;
+  if (a->num_splits < 0) return HSTU_ERR_INVALID_ARG;
+  if (a->num_splits > kMaxSplits) return HSTU_ERR_UNSUPPORTED;
+  if (a->max_seqlen_q < 0 || a->max_seqlen_kv < 0) return HSTU_ERR_INVALID_ARG;
+  if (a->causal != 0 && a->causal != 1) return HSTU_ERR_INVALID_ARG;
+  if (a->softmax != 0 && a->softmax != 1) return HSTU_ERR_INVALID_ARG;
+  if (!std::isfinite(a->alpha) || a->alpha < 0.f) return HSTU_ERR_INVALID_ARG;
+  if (a->seq_offsets_kv == nullptr && a->total_kv != a->total_q) return HSTU_ERR_INVALID_ARG;
+  const int64_t wq = static_cast<int64_t>(a->nhead) * a->hdim_qk;
+  const int64_t wv = static_cast<int64_t>(a->nhead) * a->hdim_v;
+  const int64_t qs = packed_or(a->q_row_stride, wq), ks = packed_or(a->k_row_stride, wq);
+  const int64_t vs = packed_or(a->v_row_stride, wv), os = packed_or(a->o_row_stride, wv);
+  if (qs < wq || ks < wq || vs < wv || os < wv) return HSTU_ERR_INVALID_ARG;
+  if ((qs * 2) % 16 || (ks * 2) % 16 || (vs * 2) % 16 || (os * 2) % 16) return HSTU_ERR_INVALID_ARG;
+  for (int g = 0; g < a->num_groups; ++g) {
+    if (a->local_len && a->local_len[g] < 0) return HSTU_ERR_INVALID_ARG;
+    if (a->context_len && a->context_len[g] < 0) return HSTU_ERR_INVALID_ARG;
+    if (a->minfull_len && a->minfull_len[g] < 0) return HSTU_ERR_INVALID_ARG;
+    if (a->max_uih_len && a->max_uih_len[g] < 0) return HSTU_ERR_INVALID_ARG;
+    if (a->attn_scale && !std::isfinite(a->attn_scale[g])) return HSTU_ERR_INVALID_ARG;
+  }
+  return HSTU_OK;
+}
+
+hstu_status validate_pointers(const hstu_fwd_args* a) {
+  if (!a->q || !a->k || !a->v || !a->o || !a->seq_offsets_q) return HSTU_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(a->q) | reinterpret_cast<uintptr_t>(a->k) |
+                        reinterpret_cast<uintptr_t>(a->v) | reinterpret_cast<uintptr_t>(a->o);
+  if (mis & 15) return HSTU_ERR_INVALID_ARG;
+  if (a->workspace == nullptr || (reinterpret_cast<uintptr_t>(a->workspace) & 255))
+    return HSTU_ERR_WORKSPACE;
+  return HSTU_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Plan {
+  int splits;
+  int max_seq_q, max_seq_kv;
+  int max_units;
+  size_t off_scale, off_scratch, off_units, off_opart, off_mlpart, total;
+};
+
+int choose_splits(const hstu_fwd_args* a, int max_seq_q, int max_seq_kv, int sms) {
+  if (a->num_splits > 0) return a->num_splits;
+  const long long q_tiles = (max_seq_q + kBlockM - 1) / kBlockM;
+  const long long units = static_cast<long long>(a->batch) * q_tiles * a->nhead;
+  const int kv_tiles = (max_seq_kv + kBlockN - 1) / kBlockN;
+  const long long target = 4LL * (sms > 0 ? sms : 148);
+  if (units >= target || kv_tiles < 8) return 1;
+  long long s = (target + units - 1) / units;
+  if (s > kv_tiles / 4) s = kv_tiles / 4;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+Plan make_plan(const hstu_fwd_args* a, int sms) {
+  Plan pl{};
+  pl.max_seq_q = a->max_seqlen_q > 0 ? a->max_seqlen_q : a->total_q;
+  pl.max_seq_kv = a->max_seqlen_kv > 0 ? a->max_seqlen_kv : a->total_kv;
+  pl.splits = choose_splits(a, pl.max_seq_q, pl.max_seq_kv, sms);
+  const long long tiles_a = static_cast<long long>(a->batch) * ((pl.max_seq_q + kBlockM - 1) / kBlockM);
+  const long long tiles_b = (static_cast<long long>(a->total_q) + kBlockM - 1) / kBlockM + a->batch;
+  const long long q_tiles = tiles_a < tiles_b ? tiles_a : tiles_b;
+  long long units = q_tiles * a->nhead * pl.splits;
+  if (units > (1LL << 30)) units = 1LL << 30;
+  pl.max_units = static_cast<int>(units);
+  size_t off = align256(kWsHeaderInts * sizeof(int));
+  pl.off_scale = off;
+  off = align256(off + kMaxGroups * sizeof(float));
+  pl.off_scratch = off;
+  off = align256(off + 4ull * a->batch * sizeof(int));
+  pl.off_units = off;
+  off = align256(off + static_cast<size_t>(pl.max_units) * sizeof(int4));
+  pl.off_opart = pl.off_mlpart = 0;
+  if (pl.splits > 1) {
+    pl.off_opart = off;
+    off = align256(off + static_cast<size_t>(pl.splits) * a->total_q * a->nhead * a->hdim_v * sizeof(float));
+    pl.off_mlpart = off;
+    off = align256(off + static_cast<size_t>(pl.splits) * a->nhead * a->total_q * 2 * sizeof(float));
+  }
+  pl.total = off;
+  return pl;
+}
+
+bool encode_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_t rows,
+                int64_t row_stride_elems) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_elems * 2)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockN)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+void fill_group_params(const hstu_fwd_args* a, int* ctx, int* loc, int* mf) {
+  for (int g = 0; g < kMaxGroups; ++g) {
+    const bool in = g < a->num_groups;
+    ctx[g] = (in && a->context_len) ? a->context_len[g] : 0;
+    loc[g] = (in && a->local_len) ? a->local_len[g] : 0;
+    mf[g] = (in && a->minfull_len) ? a->minfull_len[g] : 0;
+  }
+}
+
+PrepParams make_prep(const hstu_fwd_args* a, const Plan& pl) {
+  PrepParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  pp.off_q = a->seq_offsets_q;
+  pp.off_kv = a->seq_offsets_kv ? a->seq_offsets_kv : a->seq_offsets_q;
+  pp.targets = a->num_targets;
+  pp.units = reinterpret_cast<int4*>(ws + pl.off_units);
+  pp.ws_header = reinterpret_cast<int*>(ws);
+  pp.group_scale = reinterpret_cast<float*>(ws + pl.off_scale);
+  pp.batch_scratch = reinterpret_cast<int*>(ws + pl.off_scratch);
+  pp.batch = a->batch;
+  pp.nhead = a->nhead;
+  pp.num_groups = a->num_groups;
+  pp.batch_per_group = a->batch / a->num_groups;
+  pp.splits = pl.splits;
+  pp.total_q = a->total_q;
+  pp.total_kv = a->total_kv;
+  pp.max_seqlen_q = pl.max_seq_q;
+  pp.max_seqlen_kv = pl.max_seq_kv;
+  pp.max_units = pl.max_units;
+  pp.causal = a->causal;
+  pp.self_attn = a->seq_offsets_kv == nullptr;
+  fill_group_params(a, pp.ctx, pp.loc, pp.mf);
+  for (int g = 0; g < kMaxGroups; ++g) {
+    const bool in = g < a->num_groups;
+    pp.max_uih[g] = (in && a->max_uih_len) ? a->max_uih_len[g] : 0;
+    pp.attn_scale[g] = (in && a->attn_scale) ? a->attn_scale[g] : 0.f;
+  }
+  return pp;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hstu_abi_version(void) { return HSTU_ABI_VERSION; }
+
+const char* hstu_status_string(hstu_status s) {
+  switch (s) {
+    case HSTU_OK: return "ok";
+    case HSTU_ERR_INVALID_ARG: return "invalid argument";
+    case HSTU_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HSTU_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case HSTU_ERR_CUDA: return "CUDA error";
+    case HSTU_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+int32_t hstu_device_sm_count(void) { return sm_count_current(); }
+
+size_t hstu_fwd_args_size(void) { return sizeof(hstu_fwd_args); }
+
+hstu_status hstu_selftest_wait_timeout(int32_t* result_dev, uint64_t timeout_ns, void* stream_ptr,
+                                       int32_t* timed_out) {
+  if (!result_dev || !timed_out) return HSTU_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (launch_wait_selftest(result_dev, timeout_ns, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (cudaMemcpy(timed_out, result_dev, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  return HSTU_OK;
+}
+
+hstu_status hstu_attn_fwd_workspace_size(const hstu_fwd_args* a, size_t* bytes) {
+  if (!bytes) return HSTU_ERR_INVALID_ARG;
+  const hstu_status st = validate(a);
+  if (st != HSTU_OK) return st;
+  *bytes = make_plan(a, sm_count_current()).total;
+  return HSTU_OK;
+}
+
+hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
+  hstu_status st = validate(a);
+  if (st != HSTU_OK) return st;
+  st = validate_pointers(a);
+  if (st != HSTU_OK) return st;
+  const int sms = sm_count_current();
+  if (sms <= 0) return HSTU_ERR_CUDA;
+  const Plan pl = make_plan(a, sms);
+  if (a->workspace_bytes < pl.total) return HSTU_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const bool bf16 = a->dtype == HSTU_DTYPE_BF16;
+  const int D = a->hdim_qk;
+  const int64_t wq = static_cast<int64_t>(a->nhead) * D;
+  CUtensorMap tq, tk, tv;
+  if (!encode_map(&tq, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq)) ||
+      !encode_map(&tk, a->k, bf16, wq, a->total_kv, packed_or(a->k_row_stride, wq)) ||
+      !encode_map(&tv, a->v, bf16, wq, a->total_kv, packed_or(a->v_row_stride, wq)))
+    return HSTU_ERR_CUDA;
+
+  const PrepParams pp = make_prep(a, pl);
+  if (launch_prep(pp, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+  FwdParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.o = a->o;
+  fp.lse = a->softmax ? a->lse : nullptr;
+  fp.o_part = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.off_opart) : nullptr;
+  fp.ml_part = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.off_mlpart) : nullptr;
+  fp.off_q = a->seq_offsets_q;
+  fp.off_kv = a->seq_offsets_kv ? a->seq_offsets_kv : a->seq_offsets_q;
+  fp.targets = a->num_targets;
+  fp.units = pp.units;
+  fp.ws_header = pp.ws_header;
+  fp.group_scale = pp.group_scale;
+  fp.o_stride = packed_or(a->o_row_stride, wq);
+  fp.total_q = a->total_q;
+  fp.batch = a->batch;
+  fp.nhead = a->nhead;
+  fp.num_groups = a->num_groups;
+  fp.batch_per_group = a->batch / a->num_groups;
+  fp.causal = a->causal;
+  fp.self_attn = a->seq_offsets_kv == nullptr;
+  fp.splits = pl.splits;
+  fp.alpha = a->alpha != 0.f ? a->alpha : 1.f / std::sqrt(static_cast<float>(a->hdim_qk));
+  fill_group_params(a, fp.ctx, fp.loc, fp.mf);
+  const int grid = pl.max_units < sms ? (pl.max_units > 0 ? pl.max_units : 1) : sms;
+  cudaError_t e;
+  if (D == 64) e = launch_fwd_d64(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
+  else if (D == 128) e = launch_fwd_d128(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
+  else e = launch_fwd_d256(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
+  if (e != cudaSuccess) return HSTU_ERR_CUDA;
+
+  if (pl.splits > 1) {
+    CombineParams cp;
+    std::memset(&cp, 0, sizeof(cp));
+    cp.o = a->o;
+    cp.lse = fp.lse;
+    cp.o_part = fp.o_part;
+    cp.ml_part = fp.ml_part;
+    cp.off_q = a->seq_offsets_q;
+    cp.group_scale = pp.group_scale;
+    cp.ws_header = pp.ws_header;
+    cp.o_stride = fp.o_stride;
+    cp.total_q = a->total_q;
+    cp.nhead = a->nhead;
+    cp.batch = a->batch;
+    cp.batch_per_group = fp.batch_per_group;
+    cp.splits = pl.splits;
+    cp.softmax = a->softmax;
+    if (launch_combine(cp, D, bf16, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  }
+  return HSTU_OK;
+}
+
+hstu_status hstu_attn_fwd_check(const void* workspace, void* stream_ptr, int32_t* device_error) {
+  if (!workspace) return HSTU_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  int32_t err = 0;
+  if (cudaMemcpy(&err, static_cast<const int*>(workspace) + kWsError, sizeof(int32_t),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  if (device_error) *device_error = err;
+  return err ? HSTU_ERR_DEVICE : HSTU_OK;
+}
+
+hstu_status hstu_attn_fwd_stats(const hstu_fwd_args* a, void* stream_ptr, hstu_fwd_stats* out) {
+  if (!out) return HSTU_ERR_INVALID_ARG;
+  hstu_status st = validate(a);
+  if (st != HSTU_OK) return st;
+  if (!a->seq_offsets_q) return HSTU_ERR_INVALID_ARG;
+  if (a->workspace == nullptr || (reinterpret_cast<uintptr_t>(a->workspace) & 255)) return HSTU_ERR_WORKSPACE;
+  const int sms = sm_count_current();
+  if (sms <= 0) return HSTU_ERR_CUDA;
+  const Plan pl = make_plan(a, sms);
+  if (a->workspace_bytes < pl.total) return HSTU_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const PrepParams pp = make_prep(a, pl);
+  if (launch_prep(pp, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (cudaMemsetAsync(pp.ws_header + kWsPairsLo, 0, 2 * sizeof(int), stream) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  if (launch_pairs(pp, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  int hdr[kWsHeaderInts];
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (cudaMemcpy(hdr, pp.ws_header, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return HSTU_ERR_CUDA;
+  long long tiles, pairs;
+  std::memcpy(&tiles, hdr + kWsTilesLo, sizeof(tiles));
+  std::memcpy(&pairs, hdr + kWsPairsLo, sizeof(pairs));
+  out->executed_tiles = tiles;
+  out->allowed_pairs = pairs;
+  out->work_units = hdr[kWsUnits];
+  out->num_splits = pl.splits;
+  out->device_error = hdr[kWsError];
+  out->reserved = 0;
+  return hdr[kWsError] ? HSTU_ERR_DEVICE : HSTU_OK;
+}
+
+}  // extern "C"

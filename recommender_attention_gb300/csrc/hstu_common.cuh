@@ -1,0 +1,289 @@
+// Shared definitions of the HSTU forward kernels: launch parameters, the
+// per-sequence geometry and the functional mask in interval form.
+//
+// Mask (composable_kernel 18_hstu_attention README, "Masking" table and the
+// phy_seqlen formulas).  A sequence is laid out [context c | UIH u | targets t]
+// on the query side and [context c | UIH u_kv | targets t] (self-attention) or
+// [context c | UIH u_kv] (cross-attention) on the key side.  For a query row i
+// the allowed keys are exactly
+//     [0, c)                    context keys, visible to every query
+//   U [lo_i, hi_i)              the row's UIH keys (one interval, see below)
+//   U {i} if i is a target row  (self-attention: a target key is seen only by itself)
+// where, with UIH coordinates x_i = (i - c) + (u_kv - u) for a UIH row
+// (bottom-right aligned for cross-attention), x_i = u_kv for a target row and
+// x_j = j - c for a key:
+//   context rows: every UIH key;
+//   other rows:   x_j <= x_i when causal; when a local window W > 0 applies and
+//                 the row is not in the min-full tail (F > 0 and x_i >= u_kv - F),
+//                 |x_i - x_j| <= W.
+// Because consecutive rows' intervals overlap or nest, the union over any run
+// of rows is again one interval; tile skipping relies on that.
+#pragma once
+#include <cstdint>
+#include <climits>
+
+#ifdef __CUDACC__
+#define HSTU_HD __host__ __device__ __forceinline__
+#else
+#define HSTU_HD inline
+#endif
+
+namespace hstu {
+
+constexpr int kBlockM = 128;      // query rows per tile
+constexpr int kBlockN = 128;      // keys per tile
+constexpr int kMaxGroups = 256;   // per-group parameter slots in the launch parameters
+constexpr int kMaxSplits = 16;
+
+// Device error word bits (also returned by hstu_attn_fwd_check).
+enum : int {
+  kErrOffsets = 1,       // offsets not monotone or beyond the token totals
+  kErrQLayout = 2,       // query length < context + targets
+  kErrKvLayout = 4,      // key length < context (cross) / != query length (self)
+  kErrMaxSeqlen = 8,     // a length exceeds the max_seqlen hint the workspace was sized for
+  kErrTimeout = 16,      // a pipeline wait gave up (the kernel returned early)
+};
+
+// Workspace header (int32 slots).
+enum : int {
+  kWsUnits = 0,      // number of work units written by the scheduler
+  kWsError = 1,      // device error word
+  kWsCounter = 2,    // dynamic work counter of the persistent kernel
+  kWsTilesLo = 4,    // executed (b, h, q-tile, kv-tile) blocks, int64 in slots 4-5
+  kWsPairsLo = 6,    // allowed (b, h, i, j) pairs, int64 in slots 6-7 (stats only)
+  kWsHeaderInts = 64,
+};
+
+struct SeqGeom {
+  int q0, kv0;     // first token of the sequence in the flattened Q / KV tensors
+  int Lq, Lkv;     // physical lengths
+  int c, u, ukv;   // context, query UIH, key UIH lengths
+  int W, F;        // local window, min-full tail
+  int causal, self_attn;
+};
+
+// UIH coordinate of query row i (meaningful for i >= c).
+HSTU_HD int uih_coord(const SeqGeom& s, int i) {
+  return i < s.c + s.u ? (i - s.c) + (s.ukv - s.u) : s.ukv;
+}
+
+// Allowed UIH keys of query row i as the key interval [lo, hi); hi == lo when none.
+HSTU_HD void row_uih_keys(const SeqGeom& s, int i, int& lo, int& hi) {
+  if (i < s.c) {
+    lo = s.c;
+    hi = s.c + s.ukv;
+    return;
+  }
+  const int x = uih_coord(s, i);
+  int xlo = 0, xhi = s.ukv - 1;
+  if (s.causal) xhi = xhi < x ? xhi : x;
+  const bool full = s.F > 0 && x >= s.ukv - s.F;
+  if (s.W > 0 && !full) {
+    xlo = xlo > x - s.W ? xlo : x - s.W;
+    if (!s.causal) xhi = xhi < x + s.W ? xhi : x + s.W;
+  }
+  lo = s.c + xlo;
+  hi = s.c + xhi + 1;
+  if (hi < lo) hi = lo;
+}
+
+// The single target key row i may see (itself), or -1.
+HSTU_HD int row_diag_key(const SeqGeom& s, int i) {
+  return (s.self_attn && i >= s.c + s.u && i < s.Lq) ? i : -1;
+}
+
+// Number of allowed keys of row i (0 <= i < Lq).
+HSTU_HD int row_pair_count(const SeqGeom& s, int i) {
+  int lo, hi;
+  row_uih_keys(s, i, lo, hi);
+  return s.c + (hi - lo) + (row_diag_key(s, i) >= 0 ? 1 : 0);
+}
+
+// Over the valid rows of [i0, i1): the hull [LO, HI) of their UIH-key intervals
+// (LO >= HI: no row has one), the largest lo and the smallest hi.  The interval
+// ends are monotone on each of the pieces context / UIH before the min-full
+// tail / min-full tail / targets, so evaluating the rows at piece boundaries
+// gives the exact extremes.
+struct TileBounds {
+  int LO, HI, maxLO, minHI;
+};
+HSTU_HD TileBounds tile_uih_bounds(const SeqGeom& s, int i0, int i1) {
+  if (i1 > s.Lq) i1 = s.Lq;
+  TileBounds t{INT_MAX, INT_MIN, INT_MIN, INT_MAX};
+  const int ff = s.c + (s.u - s.F > 0 ? s.u - s.F : 0);
+  int shift = s.u - s.ukv;
+  if (!s.causal && s.W > 0) shift -= s.W;
+  const int fne = s.c + (shift > 0 ? shift : 0);
+  const int cand[10] = {i0, i1 - 1, s.c - 1, s.c, s.c + s.u - 1, s.c + s.u, ff - 1, ff, fne - 1, fne};
+#pragma unroll
+  for (int k = 0; k < 10; ++k) {
+    int r = cand[k];
+    r = r < i0 ? i0 : r;
+    r = r > i1 - 1 ? i1 - 1 : r;
+    int lo, hi;
+    row_uih_keys(s, r, lo, hi);
+    t.maxLO = t.maxLO > lo ? t.maxLO : lo;
+    t.minHI = t.minHI < hi ? t.minHI : hi;
+    if (hi > lo) {
+      t.LO = t.LO < lo ? t.LO : lo;
+      t.HI = t.HI > hi ? t.HI : hi;
+    }
+  }
+  return t;
+}
+
+// Key tiles (of kBlockN keys) a query tile touches, as up to three sorted,
+// disjoint tile-index ranges: the context keys, the UIH hull, the target
+// diagonal.
+struct TileSet {
+  int lo[3], hi[3];
+  int nr;      // number of ranges
+  int count;   // number of tiles
+};
+
+HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, int m) {
+  const int i0 = m * kBlockM;
+  const int i1 = (i0 + kBlockM < s.Lq) ? i0 + kBlockM : s.Lq;
+  int rlo[3], rhi[3], n = 0;
+  if (s.c > 0 && i1 > i0) {
+    rlo[n] = 0;
+    rhi[n] = (s.c + kBlockN - 1) / kBlockN;
+    ++n;
+  }
+  const TileBounds b = tile_uih_bounds(s, i0, i1);
+  if (b.HI > b.LO) {
+    rlo[n] = b.LO / kBlockN;
+    rhi[n] = (b.HI + kBlockN - 1) / kBlockN;
+    ++n;
+  }
+  if (s.self_attn) {
+    const int d0 = i0 > s.c + s.u ? i0 : s.c + s.u;
+    if (i1 > d0) {
+      rlo[n] = d0 / kBlockN;
+      rhi[n] = (i1 + kBlockN - 1) / kBlockN;
+      ++n;
+    }
+  }
+  // sort the (at most three) ranges by start, then merge overlapping/adjacent ones
+  for (int a = 0; a < n; ++a)
+    for (int c = a + 1; c < n; ++c)
+      if (rlo[c] < rlo[a]) {
+        int t0 = rlo[a], t1 = rhi[a];
+        rlo[a] = rlo[c]; rhi[a] = rhi[c];
+        rlo[c] = t0; rhi[c] = t1;
+      }
+  TileSet ts;
+  ts.nr = 0;
+  ts.count = 0;
+  for (int a = 0; a < n; ++a) {
+    if (ts.nr > 0 && rlo[a] <= ts.hi[ts.nr - 1]) {
+      if (rhi[a] > ts.hi[ts.nr - 1]) ts.hi[ts.nr - 1] = rhi[a];
+    } else {
+      ts.lo[ts.nr] = rlo[a];
+      ts.hi[ts.nr] = rhi[a];
+      ++ts.nr;
+    }
+  }
+  for (int a = 0; a < ts.nr; ++a) ts.count += ts.hi[a] - ts.lo[a];
+  for (int a = ts.nr; a < 3; ++a) ts.lo[a] = ts.hi[a] = 0;
+  return ts;
+}
+
+// The k-th tile (0-based) of a tile set.
+HSTU_HD int tileset_at(const TileSet& ts, int k) {
+  if (k < ts.hi[0] - ts.lo[0]) return ts.lo[0] + k;
+  k -= ts.hi[0] - ts.lo[0];
+  if (k < ts.hi[1] - ts.lo[1]) return ts.lo[1] + k;
+  k -= ts.hi[1] - ts.lo[1];
+  return ts.lo[2] + k;
+}
+
+// Tiles [k0, k1) of the set belong to split `sp` of `splits`.
+HSTU_HD void split_range(int count, int sp, int splits, int& k0, int& k1) {
+  k0 = static_cast<int>((static_cast<long long>(count) * sp) / splits);
+  k1 = static_cast<int>((static_cast<long long>(count) * (sp + 1)) / splits);
+}
+
+// True when every valid row of query tile m sees every key of key tile n, so
+// the per-element predicate can be skipped.  Conservative: may say false for a
+// tile that happens to be fully allowed, never true for one that is not.
+HSTU_HD bool tile_fully_allowed(const SeqGeom& s, int m, int n) {
+  const int i0 = m * kBlockM;
+  const int j0 = n * kBlockN, j1 = j0 + kBlockN;
+  if (j1 > s.Lkv) return false;
+  if (j1 <= s.c) return true;
+  if (j1 > s.c + s.ukv) return false;   // holds target keys
+  const TileBounds b = tile_uih_bounds(s, i0, i0 + kBlockM);
+  const int jlo = j0 > s.c ? j0 : s.c;
+  return b.maxLO <= jlo && b.minHI >= j1;
+}
+
+// Launch parameters of the persistent forward kernel.
+struct FwdParams {
+  void* o;                 // [total_q, o_stride] outputs (fp16/bf16)
+  float* lse;              // [nhead, total_q] or null
+  float* o_part;           // split partials [splits, total_q, nhead, hdim_v] fp32
+  float* ml_part;          // split row stats [splits, nhead, total_q, 2] fp32
+  const int* off_q;
+  const int* off_kv;       // == off_q for self-attention
+  const int* targets;      // null = no targets
+  const int4* units;       // work units {b, m, h, split}
+  int* ws_header;          // workspace header (kWs*)
+  const float* group_scale;  // resolved attn_scale per group
+  long long o_stride;      // elements between consecutive output tokens
+  int total_q;
+  int batch, nhead, num_groups, batch_per_group;
+  int causal, self_attn, splits;
+  float alpha;             // resolved QK scale
+  int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
+};
+
+// Launch parameters of the scheduler (prep) kernel.
+struct PrepParams {
+  const int* off_q;
+  const int* off_kv;
+  const int* targets;
+  int4* units;
+  int* ws_header;
+  float* group_scale;
+  int* batch_scratch;      // [4 * batch] ints
+  int batch, nhead, num_groups, batch_per_group, splits;
+  int total_q, total_kv, max_seqlen_q, max_seqlen_kv, max_units;
+  int causal, self_attn;
+  int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups], max_uih[kMaxGroups];
+  float attn_scale[kMaxGroups];
+};
+
+// Combine kernel parameters (split-KV).
+struct CombineParams {
+  void* o;
+  float* lse;
+  const float* o_part;
+  const float* ml_part;
+  const int* off_q;
+  const float* group_scale;
+  const int* ws_header;
+  long long o_stride;
+  int total_q, nhead, batch, batch_per_group, splits, softmax;
+};
+
+// Fills the geometry of sequence b from the device/host offset arrays.
+HSTU_HD SeqGeom make_geom(const int* off_q, const int* off_kv, const int* targets, int b,
+                          int c, int W, int F, int causal, int self_attn) {
+  SeqGeom s;
+  s.q0 = off_q[b];
+  s.Lq = off_q[b + 1] - s.q0;
+  s.kv0 = self_attn ? s.q0 : off_kv[b];
+  s.Lkv = self_attn ? s.Lq : off_kv[b + 1] - s.kv0;
+  const int t = targets ? targets[b] : 0;
+  s.c = c;
+  s.u = s.Lq - c - t;
+  s.ukv = self_attn ? s.u : s.Lkv - c;
+  s.W = W;
+  s.F = F;
+  s.causal = causal;
+  s.self_attn = self_attn;
+  return s;
+}
+
+}  // namespace hstu

@@ -1,0 +1,35 @@
+// Instantiations of the persistent HSTU forward for head dimension 64.
+#include "hstu_fwd_kernel.cuh"
+#include "hstu_launch.h"
+
+namespace hstu {
+
+namespace {
+template <bool BF16, bool SOFTMAX>
+cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const FwdParams& p, int grid, cudaStream_t stream) {
+  constexpr int smem = FwdCfg<64>::SMEM_BYTES;
+  auto kern = hstu_fwd_kernel<64, BF16, SOFTMAX>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_done[64] = {};
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  kern<<<grid, kFwdThreads, smem, stream>>>(q, k, v, p);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_fwd_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream) {
+  if (bf16) return softmax ? launch_one<true, true>(q, k, v, p, grid, stream)
+                           : launch_one<true, false>(q, k, v, p, grid, stream);
+  return softmax ? launch_one<false, true>(q, k, v, p, grid, stream)
+                 : launch_one<false, false>(q, k, v, p, grid, stream);
+}
+
+}  // namespace hstu

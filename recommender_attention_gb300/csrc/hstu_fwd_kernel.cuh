@@ -1,0 +1,503 @@
+// Persistent, warp-specialised HSTU attention forward for sm_103a.
+//
+// Per work unit (batch b, query tile m of 128 rows, head h, KV split sp) the
+// kernel computes, for the key tiles the functional mask does not fully
+// exclude (composable_kernel 18_hstu_attention README, "Forward computation"):
+//     S = Q K^T                       tcgen05.mma, A = Q and B = K from shared memory, D in TMEM
+//     P = SiLU(alpha S) on allowed entries, 0 elsewhere        (SiLU mode)
+//       = exp(alpha S - m) with a running max m                 (softmax mode, online)
+//     O += P V                        tcgen05.mma, A = P from TMEM (aliasing S), B = V (MN-major)
+// and writes O * attn_scale (softmax: / rowsum, plus LSE) or, with split-KV,
+// fp32 partials for the combine kernel.
+//
+// Roles (192 threads, one CTA per SM, all waits time-bounded):
+//   warp 0       scheduler + TMA producer: fetches units from a global counter,
+//                loads Q once per unit and K/V tiles into STAGES-deep rings
+//   warp 1       TMEM owner + MMA issuer (one thread)
+//   warps 2..5   elementwise group: TMEM S -> registers, mask + SiLU/softmax,
+//                P -> TMEM; then the epilogue O -> registers -> global
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores with the
+// 16-bit P of a tile packed into the first 64 columns of its own S buffer;
+// O [256, 256 + D).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "hstu_common.cuh"
+#include "ptx.cuh"
+
+namespace hstu {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int KCH = D / 64;                  // 128-byte column chunks per row
+  static constexpr int TILE_BYTES = kBlockN * D * 2;  // one Q, K or V tile
+  static constexpr int CHUNK_BYTES = kBlockN * 128;   // one 128-row x 128-byte TMA box
+  static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);
+  static constexpr int SMEM_BYTES = (1 + 2 * STAGES) * TILE_BYTES + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t O_COL = 256;
+};
+
+constexpr int kFwdThreads = 192;
+constexpr int kSchedDepth = 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
+
+struct FwdSmemCtl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t o_full, o_empty;
+  uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
+  int sched_unit[kSchedDepth];
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct UnitView {
+  SeqGeom s;
+  TileSet ts;
+  int m, h, g, sp, k0, k1;
+};
+
+__device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
+  const int4 w = p.units[unit];
+  UnitView u;
+  const int b = w.x;
+  u.m = w.y;
+  u.h = w.z;
+  u.sp = w.w;
+  u.g = b / p.batch_per_group;
+  u.s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[u.g], p.loc[u.g], p.mf[u.g], p.causal,
+                  p.self_attn);
+  u.ts = query_tile_kv_tiles(u.s, u.m);
+  split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);
+  return u;
+}
+
+// Bounded wait; on timeout flags the error word and asks every role to stop.
+__device__ __forceinline__ bool wait_or_abort(FwdSmemCtl& ctl, const FwdParams& p, uint64_t* bar,
+                                              uint32_t parity) {
+  if (ptx::mbar_wait(bar, parity, kWaitLimitNs)) return true;
+  ctl.abort_flag = 1;
+  atomicOr(&p.ws_header[kWsError], kErrTimeout);
+  return false;
+}
+
+// Warp-uniform bounded wait for the elementwise group: every lane waits, then
+// the warp agrees (and reconverges) before the next .sync.aligned tcgen05 op.
+__device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdParams& p, uint64_t* bar,
+                                                   uint32_t parity) {
+  const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, kWaitLimitNs));
+  if (!ok) {
+    ctl.abort_flag = 1;
+    atomicOr(&p.ws_header[kWsError], kErrTimeout);
+  }
+  return ok;
+}
+
+template <int D, bool BF16, bool SOFTMAX>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+  using Cfg = FwdCfg<D>;
+  constexpr int KCH = Cfg::KCH;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ FwdSmemCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + Cfg::TILE_BYTES;
+  uint8_t* sV = sK + STAGES * Cfg::TILE_BYTES;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+    ptx::mbar_init(&ctl.q_full, 1);
+    ptx::mbar_init(&ctl.q_empty, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&ctl.k_full[s], 1);
+      ptx::mbar_init(&ctl.k_empty[s], 1);
+      ptx::mbar_init(&ctl.v_full[s], 1);
+      ptx::mbar_init(&ctl.v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&ctl.s_full[s], 1);
+      ptx::mbar_init(&ctl.p_full[s], 128);
+      ptx::mbar_init(&ctl.pv_done[s], 1);
+    }
+    ptx::mbar_init(&ctl.o_full, 1);
+    ptx::mbar_init(&ctl.o_empty, 128);
+    for (int s = 0; s < kSchedDepth; ++s) {
+      ptx::mbar_init(&ctl.sched_full[s], 1);
+      ptx::mbar_init(&ctl.sched_empty[s], 5);
+    }
+    ctl.abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tm_q);
+    ptx::prefetch_tensormap(&tm_k);
+    ptx::prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl.tmem_base, Cfg::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  const int n_units = p.ws_header[kWsUnits];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int q_it = 0, kv_it = 0, sched_it = 0;
+      while (!ctl.abort_flag) {
+        int unit = atomicAdd(&p.ws_header[kWsCounter], 1);
+        if (unit >= n_units) unit = -1;
+        const int slot = sched_it % kSchedDepth;
+        if (!wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((sched_it / kSchedDepth) & 1) ^ 1)) break;
+        ctl.sched_unit[slot] = unit;
+        ptx::mbar_arrive(&ctl.sched_full[slot]);
+        ++sched_it;
+        if (unit < 0) break;
+        const UnitView u = decode_unit(p, unit);
+        if (u.k1 <= u.k0) continue;
+        if (!wait_or_abort(ctl, p, &ctl.q_empty, (q_it & 1) ^ 1)) break;
+        ptx::mbar_arrive_expect_tx(&ctl.q_full, Cfg::TILE_BYTES);
+        const int qrow = u.s.q0 + u.m * kBlockM;
+#pragma unroll
+        for (int kc = 0; kc < KCH; ++kc)
+          ptx::tma_load_2d(sQ + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full, u.h * D + kc * 64, qrow);
+        ++q_it;
+        bool ok = true;
+        for (int k = u.k0; k < u.k1 && ok; ++k) {
+          const int n = tileset_at(u.ts, k);
+          const int st = kv_it % STAGES;
+          const uint32_t ph = ((kv_it / STAGES) & 1) ^ 1;
+          const int krow = u.s.kv0 + n * kBlockN;
+          if (!wait_or_abort(ctl, p, &ctl.k_empty[st], ph)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.k_full[st], Cfg::TILE_BYTES);
+#pragma unroll
+          for (int kc = 0; kc < KCH; ++kc)
+            ptx::tma_load_2d(sK + st * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_k, &ctl.k_full[st],
+                             u.h * D + kc * 64, krow);
+          if (!wait_or_abort(ctl, p, &ctl.v_empty[st], ph)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.v_full[st], Cfg::TILE_BYTES);
+#pragma unroll
+          for (int kc = 0; kc < KCH; ++kc)
+            ptx::tma_load_2d(sV + st * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[st],
+                             u.h * D + kc * 64, krow);
+          ++kv_it;
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
+      constexpr uint32_t idesc_pv = ptx::idesc_f16_f32acc(BF16, true, kBlockM, D);
+      const uint32_t q_base = ptx::smem_u32(sQ);
+      const uint32_t k_base = ptx::smem_u32(sK);
+      const uint32_t v_base = ptx::smem_u32(sV);
+      int q_it = 0, kv_it = 0, s_it = 0, sched_it = 0;
+      bool ok = true;
+      // S = Q K^T for the tile held in K stage (kvi % STAGES), into S buffer (si & 1).
+      auto issue_qk = [&](int kvi, int si) -> bool {
+        const int st = kvi % STAGES;
+        if (!wait_or_abort(ctl, p, &ctl.k_full[st], (kvi / STAGES) & 1)) return false;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + (si & 1) * 128;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * Cfg::CHUNK_BYTES + (ks & 3) * 32;
+          const uint64_t ad = ptx::sdesc_sw128(q_base + off, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(k_base + st * Cfg::TILE_BYTES + off, 16, 1024);
+          ptx::umma_ss(d_tmem, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        ptx::umma_commit(&ctl.k_empty[st]);
+        ptx::umma_commit(&ctl.s_full[si & 1]);
+        return true;
+      };
+      while (ok && !ctl.abort_flag) {
+        const int slot = sched_it % kSchedDepth;
+        if (!wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
+        const int unit = ctl.sched_unit[slot];
+        ptx::mbar_arrive(&ctl.sched_empty[slot]);
+        ++sched_it;
+        if (unit < 0) break;
+        const UnitView u = decode_unit(p, unit);
+        const int nt = u.k1 - u.k0;
+        if (nt <= 0) continue;
+        if (!wait_or_abort(ctl, p, &ctl.q_full, q_it & 1)) break;
+        ptx::tc_fence_after();
+        if (!issue_qk(kv_it, s_it)) break;
+        for (int idx = 0; idx < nt; ++idx) {
+          if (idx + 1 < nt) {
+            if (!issue_qk(kv_it + idx + 1, s_it + idx + 1)) { ok = false; break; }
+          } else {
+            ptx::umma_commit(&ctl.q_empty);   // every QK of this unit is issued
+          }
+          const int si = s_it + idx;
+          if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (idx == 0) {
+            if (!wait_or_abort(ctl, p, &ctl.o_empty, (q_it & 1) ^ 1)) { ok = false; break; }
+            ptx::tc_fence_after();
+          }
+          const int kvi = kv_it + idx;
+          const int st = kvi % STAGES;
+          if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / STAGES) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t p_tmem = tmem + (si & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            const uint64_t bd = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES + kk * 2048,
+                                                 Cfg::CHUNK_BYTES, 1024);
+            ptx::umma_ts(tmem + Cfg::O_COL, p_tmem + kk * 8, bd, idesc_pv,
+                         (idx > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::umma_commit(&ctl.v_empty[st]);
+          if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
+        }
+        if (!ok) break;
+        ptx::umma_commit(&ctl.o_full);
+        kv_it += nt;
+        s_it += nt;
+        ++q_it;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int quarter = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const float half_alpha = 0.5f * p.alpha;
+    const float scale_log2 = p.alpha * 1.4426950408889634f;
+    int s_it = 0, q_it = 0, sched_it = 0;
+    while (!ctl.abort_flag) {
+      const int slot = sched_it % kSchedDepth;
+      if (!warp_wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
+      const int unit = ctl.sched_unit[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ctl.sched_empty[slot]);
+      ++sched_it;
+      if (unit < 0) break;
+      const UnitView u = decode_unit(p, unit);
+      const int nt = u.k1 - u.k0;
+      const int row = u.m * kBlockM + quarter * 32 + lane;
+      const bool valid = row < u.s.Lq;
+      int r_lo, r_hi;
+      row_uih_keys(u.s, valid ? row : 0, r_lo, r_hi);
+      int r_diag = row_diag_key(u.s, row);
+      int r_ctx = u.s.c;
+      if (!valid) { r_lo = r_hi = 0; r_diag = -1; r_ctx = 0; }
+      const uint32_t r_span = static_cast<uint32_t>(r_hi - r_lo);
+      const float attn_scale = p.group_scale[u.g];
+      const long long grow = static_cast<long long>(u.s.q0) + row;   // global token row
+
+      float m_run = -INFINITY, l_run = 0.f;   // softmax row state (log2 domain)
+      bool ok = true;
+      for (int idx = 0; idx < nt; ++idx) {
+        const int n = tileset_at(u.ts, u.k0 + idx);
+        const bool full = tile_fully_allowed(u.s, u.m, n);
+        const int j0 = n * kBlockN;
+        const int si = s_it + idx;
+        if (!warp_wait_or_abort(ctl, p, &ctl.s_full[si & 1], (si >> 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t s_tmem = tmem + lane_base + (si & 1) * 128;
+        if constexpr (!SOFTMAX) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld32(s_tmem + c * 32, r);
+            ptx::tmem_ld_wait(r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              float pv[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float hh = __uint_as_float(r[k + e]) * half_alpha;
+                float v = fmaf(hh, tanh_approx(hh), hh);   // SiLU(2hh) = hh * (1 + tanh(hh))
+                if (!full) {
+                  const int j = j0 + c * 32 + k + e;
+                  const bool al = (j < r_ctx) | (static_cast<uint32_t>(j - r_lo) < r_span) | (j == r_diag);
+                  v = al ? v : 0.f;
+                }
+                pv[e] = v;
+              }
+              pk[k >> 1] = pack2<BF16>(pv[0], pv[1]);
+            }
+            ptx::tmem_st16(s_tmem + c * 16, pk);
+          }
+        } else {
+          uint32_t r[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_tmem + c * 32, r[c]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(r[c]);
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              float v = __uint_as_float(r[c][k]) * scale_log2;
+              if (!full) {
+                const int j = j0 + c * 32 + k;
+                const bool al = (j < r_ctx) | (static_cast<uint32_t>(j - r_lo) < r_span) | (j == r_diag);
+                v = al ? v : -INFINITY;
+              }
+              r[c][k] = __float_as_uint(v);
+              mx = fmaxf(mx, v);
+            }
+          // PV of the tile before last must be complete before this tile; keeps the
+          // parity tracking of pv_done unambiguous.
+          if (si >= 2) {
+            if (!warp_wait_or_abort(ctl, p, &ctl.pv_done[si & 1], ((si - 2) >> 1) & 1)) { ok = false; break; }
+          }
+          if (mx > m_run + 8.0f) {
+            // New running max; rescale what O already holds (only after a previous
+            // tile of this unit, whose PV must have completed).
+            if (idx > 0 && m_run != -INFINITY) {
+              const int sp = si - 1;
+              if (!warp_wait_or_abort(ctl, p, &ctl.pv_done[sp & 1], (sp >> 1) & 1)) { ok = false; break; }
+              ptx::tc_fence_after();
+              const float corr = ex2_approx(m_run - mx);
+              const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL;
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                ptx::tmem_ld32(o_tmem + c * 32, o);
+                ptx::tmem_ld_wait(o);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+                ptx::tmem_st32(o_tmem + c * 32, o);
+              }
+              l_run *= corr;
+            }
+            m_run = mx;
+          }
+          const float mref = m_run == -INFINITY ? 0.f : m_run;
+          float lsum = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float e0 = ex2_approx(__uint_as_float(r[c][k]) - mref);
+              const float e1 = ex2_approx(__uint_as_float(r[c][k + 1]) - mref);
+              pk[k >> 1] = pack2<BF16>(e0, e1);
+              lsum += e0 + e1;
+            }
+            ptx::tmem_st16(s_tmem + c * 16, pk);
+          }
+          l_run += lsum;
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ctl.p_full[si & 1]);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      if (nt > 0) {
+        if (!warp_wait_or_abort(ctl, p, &ctl.o_full, q_it & 1)) break;
+        ptx::tc_fence_after();
+      }
+      const bool write_part = p.splits > 1;
+      float mul = attn_scale;
+      if constexpr (SOFTMAX) mul = l_run > 0.f ? attn_scale / l_run : 0.f;
+      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (nt > 0) {
+          ptx::tmem_ld32(o_tmem + c * 32, o);
+          ptx::tmem_ld_wait(o);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = 0u;
+        }
+        if (!valid) continue;
+        if (write_part) {
+          float* dst = p.o_part +
+                       ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * D + c * 32;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2)
+            pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * D + c * 32;
+#pragma unroll
+          for (int k = 0; k < 16; k += 4)
+            *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
+        }
+      }
+      if (nt > 0) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ctl.o_empty);
+        ++q_it;
+      }
+      if (valid) {
+        if (write_part) {
+          if constexpr (SOFTMAX) {
+            float* ml = p.ml_part + ((static_cast<long long>(u.sp) * p.nhead + u.h) * p.total_q + grow) * 2;
+            ml[0] = m_run;
+            ml[1] = l_run;
+          }
+        } else if (SOFTMAX && p.lse != nullptr) {
+          p.lse[static_cast<long long>(u.h) * p.total_q + grow] =
+              l_run > 0.f ? m_run * 0.6931471805599453f + logf(l_run) : -INFINITY;
+        }
+      }
+      s_it += nt;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  if (ctl.abort_flag && tid == 0) {
+    // let copies / MMAs already in flight land before the CTA releases its memory
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace hstu

@@ -1,0 +1,302 @@
+// Scheduler (prep), pair-count and split-KV combine kernels of the HSTU forward.
+//
+// The scheduler runs as one CTA before the forward kernel, on the same stream:
+// it validates the jagged offsets, counts for every query tile the key tiles
+// the functional mask does not fully exclude, orders the sequences longest
+// first (most executed tiles first, so the persistent kernel's dynamic queue
+// is a longest-processing-time schedule and a sequence's heads and query tiles
+// run close together in time for L2 reuse of its K/V) and writes one work unit
+// per (sequence, head, query tile, KV split).  It also resolves the per-group
+// attn_scale default (composable_kernel 18_hstu_attention README, "Command-line
+// arguments": attn_scale 0 means 1/max_seqlen, the maximum UIH length).
+//
+// The combine kernel merges split-KV partials ("Split-KV" section of the same
+// README): SiLU partials add; softmax partials are merged with their running
+// maxima and row sums, and the LSE is written.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "hstu_common.cuh"
+#include "hstu_launch.h"
+#include "ptx.cuh"
+
+namespace hstu {
+
+namespace {
+
+constexpr int kPrepThreads = 1024;
+constexpr int kSortMaxBatch = 2048;   // above this the sequences keep their input order
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_constant__ PrepParams p) {
+  __shared__ int s_gmax[kMaxGroups];
+  __shared__ int s_err;
+  __shared__ unsigned long long s_tiles;
+  __shared__ int s_wsum[32];
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
+  for (int g = tid; g < kMaxGroups; g += nth) s_gmax[g] = 0;
+  if (tid == 0) {
+    s_err = 0;
+    s_tiles = 0ull;
+  }
+  __syncthreads();
+
+  int* cost = p.batch_scratch;               // executed key tiles of sequence b (one head)
+  int* nq = p.batch_scratch + p.batch;       // query tiles of sequence b
+  int* order = p.batch_scratch + 2 * p.batch;
+
+  // 1. validate every sequence and count its tiles
+  for (int b = tid; b < p.batch; b += nth) {
+    const int g = b / p.batch_per_group;
+    const int c = p.ctx[g];
+    int err = 0;
+    const int q0 = p.off_q[b], q1 = p.off_q[b + 1];
+    if (q0 < 0 || q1 < q0 || q1 > p.total_q) err |= kErrOffsets;
+    const int t = p.targets ? p.targets[b] : 0;
+    if (t < 0 || q1 - q0 < c + t) err |= kErrQLayout;
+    int Lkv = q1 - q0;
+    if (!p.self_attn) {
+      const int k0 = p.off_kv[b], k1 = p.off_kv[b + 1];
+      if (k0 < 0 || k1 < k0 || k1 > p.total_kv) err |= kErrOffsets;
+      Lkv = k1 - k0;
+      if (Lkv < c) err |= kErrKvLayout;
+    }
+    if (q1 - q0 > p.max_seqlen_q || Lkv > p.max_seqlen_kv) err |= kErrMaxSeqlen;
+    int cst = 0, n = 0;
+    if (err == 0) {
+      const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, c, p.loc[g], p.mf[g], p.causal,
+                                  p.self_attn);
+      n = (s.Lq + kBlockM - 1) / kBlockM;
+      for (int m = 0; m < n; ++m) cst += query_tile_kv_tiles(s, m).count;
+      atomicMax(&s_gmax[g], s.u);
+    } else {
+      atomicOr(&s_err, err);
+    }
+    cost[b] = cst;
+    nq[b] = n;
+  }
+  __syncthreads();
+  if (s_err != 0) {
+    if (tid == 0) {
+      p.ws_header[kWsError] = s_err;
+      p.ws_header[kWsUnits] = 0;
+      p.ws_header[kWsCounter] = 0;
+      reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
+    }
+    return;
+  }
+
+  // 2. longest sequence first (stable rank sort on the executed-tile count)
+  const bool sort = p.batch <= kSortMaxBatch;
+  for (int b = tid; b < p.batch; b += nth) {
+    int r = b;
+    if (sort) {
+      const int cb = cost[b];
+      r = 0;
+      for (int b2 = 0; b2 < p.batch; ++b2) {
+        const int c2 = cost[b2];
+        r += (c2 > cb) | ((c2 == cb) & (b2 < b));
+      }
+    }
+    order[r] = b;
+  }
+  __syncthreads();
+
+  // 3. unit offsets of each sorted position: block-wide exclusive scan
+  const int per = (p.batch + nth - 1) / nth;
+  const int pbeg = min(tid * per, p.batch), pend = min(pbeg + per, p.batch);
+  int local = 0;
+  for (int pos = pbeg; pos < pend; ++pos) local += nq[order[pos]] * p.nhead * p.splits;
+  const int incl = warp_incl_scan(local);
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < nwarps ? s_wsum[lane] : 0;
+    v = warp_incl_scan(v);
+    s_wsum[lane] = v;
+  }
+  __syncthreads();
+  const int total = s_wsum[nwarps - 1];
+  if (total > p.max_units) {
+    if (tid == 0) {
+      p.ws_header[kWsError] = kErrMaxSeqlen;
+      p.ws_header[kWsUnits] = 0;
+      p.ws_header[kWsCounter] = 0;
+      reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
+    }
+    return;
+  }
+  int u = incl - local + (warp > 0 ? s_wsum[warp - 1] : 0);
+
+  // 4. units: per sequence, heads outer, query tiles from the last (most key
+  //    tiles under a causal mask) down, splits innermost
+  unsigned long long tiles = 0ull;
+  for (int pos = pbeg; pos < pend; ++pos) {
+    const int b = order[pos];
+    const int n = nq[b];
+    for (int h = 0; h < p.nhead; ++h)
+      for (int m = n - 1; m >= 0; --m)
+        for (int sp = 0; sp < p.splits; ++sp) p.units[u++] = make_int4(b, m, h, sp);
+    tiles += static_cast<unsigned long long>(cost[b]) * p.nhead;
+  }
+  if (tiles) atomicAdd(&s_tiles, tiles);
+
+  // 5. attn_scale per group: 0 means 1 / (max UIH length of the group)
+  for (int g = tid; g < p.num_groups; g += nth) {
+    float sc = p.attn_scale[g];
+    if (sc == 0.f) {
+      const int mu = p.max_uih[g] > 0 ? p.max_uih[g] : s_gmax[g];
+      sc = mu > 0 ? 1.f / static_cast<float>(mu) : 1.f;
+    }
+    p.group_scale[g] = sc;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    p.ws_header[kWsError] = 0;
+    p.ws_header[kWsUnits] = total;
+    p.ws_header[kWsCounter] = 0;
+    reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = static_cast<long long>(s_tiles);
+  }
+}
+
+// Allowed (b, h, i, j) pairs: one CTA per sequence.
+__global__ void __launch_bounds__(256) hstu_pairs_kernel(const __grid_constant__ PrepParams p) {
+  const int b = blockIdx.x;
+  const int g = b / p.batch_per_group;
+  const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[g], p.loc[g], p.mf[g], p.causal,
+                              p.self_attn);
+  long long sum = 0;
+  for (int i = threadIdx.x; i < s.Lq; i += blockDim.x) sum += row_pair_count(s, i);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_down_sync(0xffffffffu, sum, o);
+  if ((threadIdx.x & 31) == 0 && sum)
+    atomicAdd(reinterpret_cast<unsigned long long*>(p.ws_header + kWsPairsLo),
+              static_cast<unsigned long long>(sum) * p.nhead);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2c(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// One warp per (token row, head); each lane owns D/32 consecutive columns.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) hstu_combine_kernel(const __grid_constant__ CombineParams p) {
+  constexpr int E = D / 32;
+  const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long row = wid / p.nhead;
+  const int h = static_cast<int>(wid % p.nhead);
+  if (row >= p.total_q || p.ws_header[kWsUnits] == 0) return;
+  if (row >= p.off_q[p.batch]) return;
+  int lo = 0, hi = p.batch;   // off_q[lo] <= row < off_q[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.off_q[mid] <= row) lo = mid; else hi = mid;
+  }
+  const float scale = p.group_scale[lo / p.batch_per_group];
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float M = -INFINITY, L = 0.f;
+  if (p.softmax) {
+    for (int sp = 0; sp < p.splits; ++sp)
+      M = fmaxf(M, p.ml_part[((static_cast<long long>(sp) * p.nhead + h) * p.total_q + row) * 2]);
+  }
+  for (int sp = 0; sp < p.splits; ++sp) {
+    float w = 1.f;
+    if (p.softmax) {
+      const float* ml = p.ml_part + ((static_cast<long long>(sp) * p.nhead + h) * p.total_q + row) * 2;
+      w = ml[0] == -INFINITY ? 0.f : exp2f(ml[0] - M);
+      L += w * ml[1];
+    }
+    const float* src = p.o_part + ((static_cast<long long>(sp) * p.total_q + row) * p.nhead + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(src + e);
+      acc[e] += w * v.x;
+      acc[e + 1] += w * v.y;
+    }
+  }
+  float mul = scale;
+  if (p.softmax) mul = L > 0.f ? scale / L : 0.f;
+  uint32_t pk[E / 2];
+#pragma unroll
+  for (int e = 0; e < E; e += 2) pk[e / 2] = pack2c<BF16>(acc[e] * mul, acc[e + 1] * mul);
+  uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + row * p.o_stride + h * D + lane * E;
+  if constexpr (E == 2) {
+    *reinterpret_cast<uint32_t*>(dst) = pk[0];
+  } else if constexpr (E == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+  if (p.softmax && p.lse != nullptr && lane == 0)
+    p.lse[static_cast<long long>(h) * p.total_q + row] =
+        L > 0.f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+}
+
+// One thread waits on a barrier that nothing arrives on; the bounded wait must
+// give up after timeout_ns and let the kernel finish.
+__global__ void hstu_wait_selftest_kernel(int* result, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *result = ptx::mbar_wait(&bar, 0, timeout_ns) ? 0 : 1;
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* result, unsigned long long timeout_ns, cudaStream_t stream) {
+  hstu_wait_selftest_kernel<<<1, 32, 0, stream>>>(result, timeout_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
+  hstu_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pairs(const PrepParams& p, cudaStream_t stream) {
+  hstu_pairs_kernel<<<p.batch, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams& p, int hdim, bool bf16, cudaStream_t stream) {
+  const long long warps = static_cast<long long>(p.total_q) * p.nhead;
+  const unsigned grid = static_cast<unsigned>((warps + 7) / 8);
+  if (grid == 0) return cudaSuccess;
+#define HSTU_COMBINE(DD)                                                            \
+  if (hdim == DD) {                                                                 \
+    if (bf16) hstu_combine_kernel<DD, true><<<grid, 256, 0, stream>>>(p);           \
+    else hstu_combine_kernel<DD, false><<<grid, 256, 0, stream>>>(p);               \
+    return cudaGetLastError();                                                      \
+  }
+  HSTU_COMBINE(64)
+  HSTU_COMBINE(128)
+  HSTU_COMBINE(256)
+#undef HSTU_COMBINE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hstu

@@ -1,0 +1,104 @@
+"""The C-ABI library: it loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a GPU.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from recommender_attention_gb300 import build as B
+from recommender_attention_gb300 import hstu
+
+HEADER = os.path.join(B.INCLUDE, "hstu_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return hstu.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hstu_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "hstu_attn_fwd" in names and len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(hstu.EXPORTS)
+
+
+def test_version_strings_and_struct_layout(lib):
+    assert lib.hstu_abi_version() == 1
+    for s in range(6):
+        assert lib.hstu_status_string(s)
+    assert lib.hstu_status_string(99) == b"unknown status"
+    assert lib.hstu_fwd_args_size() == ctypes.sizeof(hstu.FwdArgs)
+
+
+def _args(**kw):
+    a = hstu.FwdArgs()
+    a.dtype, a.batch, a.nhead, a.hdim_qk, a.hdim_v = 1, 4, 2, 128, 128
+    a.total_q = a.total_kv = 1000
+    a.max_seqlen_q = a.max_seqlen_kv = 300
+    a.causal, a.num_groups = 1, 1
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def _ws(lib, a):
+    n = ctypes.c_size_t(0)
+    st = lib.hstu_attn_fwd_workspace_size(ctypes.byref(a), ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("hdim_qk", 96, 2), ("hdim_v", 64, 2), ("dtype", 7, 2), ("batch", 0, 1), ("nhead", 0, 1),
+    ("num_groups", 3, 1), ("num_groups", 0, 1), ("num_splits", 17, 2), ("num_splits", -1, 1),
+    ("q_row_stride", 100, 1), ("q_row_stride", 3, 1), ("total_kv", 999, 1), ("alpha", -1.0, 1),
+    ("causal", 2, 1), ("max_seqlen_q", -5, 1)])
+def test_host_validation(lib, field, value, status):
+    st, _ = _ws(lib, _args(**{field: value}))
+    assert st == status
+
+
+def test_group_array_validation(lib):
+    g = (ctypes.c_int32 * 2)(5, -1)
+    a = _args(num_groups=2, local_len=ctypes.cast(g, ctypes.c_void_p))
+    assert _ws(lib, a)[0] == 1
+    big = _args(batch=512, num_groups=512)
+    assert _ws(lib, big)[0] == 2
+
+
+def test_workspace_grows_with_splits(lib):
+    st1, n1 = _ws(lib, _args(num_splits=1))
+    st4, n4 = _ws(lib, _args(num_splits=4))
+    assert st1 == st4 == 0
+    # fp32 partials: 4 splits x 1000 rows x 2 heads x 128 + row stats
+    assert n4 - n1 >= 4 * 1000 * 2 * 128 * 4
+
+
+def test_forward_rejects_before_launch(lib):
+    a = _args()
+    # missing pointers / workspace are host-side errors: nothing is launched
+    assert lib.hstu_attn_fwd(ctypes.byref(a), None) == 1
+    a.q = a.k = a.v = a.o = a.seq_offsets_q = 4096
+    assert lib.hstu_attn_fwd(ctypes.byref(a), None) == 3
+    a.workspace = 4096 + 8
+    assert lib.hstu_attn_fwd(ctypes.byref(a), None) == 3
+    a.q = 4096 + 2
+    a.workspace = 8192
+    assert lib.hstu_attn_fwd(ctypes.byref(a), None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(hstu, "_LIB", None)
+    monkeypatch.setattr(hstu, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        hstu.load_library()
