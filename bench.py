@@ -1,0 +1,446 @@
+"""Benchmark of the HSTU attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+
+One step = one forward (scheduler + persistent tcgen05 kernel [+ combine]) over
+the large jagged workload: B=64 sequences, nhead 4, bf16, UIH lengths
+U_int[1024, 4096], targets U_int[1, 32], context 6, full causal, hdim 128
+(repeated at hdim 256 in the same run), synthetic N(0,1) inputs, seed 7.
+Prints one JSON line (rank 0).  Metric: useful TFLOP/s = 2 (hdim_qk + hdim_v)
+x allowed (i, j) pairs / step time.
+
+Multi-GPU (torchrun): every rank runs its own batch of the same shape (seed
+7 + rank); no collective touches the data path ("scaling": "weak").  The time
+is the max over ranks; value = all ranks' useful FLOPs / that time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from recommender_attention_gb300 import workloads as W  # noqa: E402
+
+METRIC = "HSTU fwd useful TFLOP/s (unmasked pairs) at 1 GB300 and % of bf16 dense peak"
+UNIT = "TFLOP/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "hstu_fwd_large_jagged_d128_dram.txt")
+KERNEL_SOURCES = ["hstu_fwd_kernel.cuh", "hstu_common.cuh", "ptx.cuh", "hstu_fwd_d128.cu"]
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def rank_workload(rank: int, hdim: int = 128) -> W.Workload:
+    """Rank r's shard: the large jagged shape with its own seed (weak scaling)."""
+    return W.large_jagged(hdim=hdim, seed=7 + rank)
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- peaks, clocks, traffic
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) >= 9:
+                    rows.append([x.strip() for x in r])
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if smax and s > 0.3 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if _isnum(r[3])), default=None)}
+
+
+def _isnum(x):
+    try:
+        float(x)
+        return True
+    except ValueError:
+        return False
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "recommender_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the forward kernel from the committed ncu summary,
+    when it was taken on the current kernel sources; else None."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- CUDA arm
+def device_call(w, q, k, v, device):
+    from recommender_attention_gb300.hstu import HstuCall
+    off_q = torch.from_numpy(w.seq_offsets_q()).to(device)
+    tg = torch.from_numpy(w.num_targets()).to(device)
+    dq, dk, dv = q.to(device), k.to(device), v.to(device)
+    call = HstuCall(dq, dk, dv, off_q, None, tg, alpha=w.alpha, attn_scale=list(w.attn_scale),
+                    causal=w.causal, local_len=list(w.local_len), context_len=list(w.context_len),
+                    minfull_len=list(w.minfull_len), max_uih_len=list(w.max_uih_len),
+                    num_groups=w.num_groups, softmax=w.softmax,
+                    max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()))
+    return call, (dq, dk, dv, off_q, tg)
+
+
+def time_device_steps(call, steps, warmup, world, stream):
+    for _ in range(warmup):
+        call.launch(stream)
+    call.check(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:   # materialise the event handles
+        a.record(stream)
+        b.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        call.launch(stream, events=ev[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = start.elapsed_time(end) / steps
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    call.check(stream)
+    return step_ms, fwd_ms
+
+
+def time_e2e_steps(call, host, dev, steps, warmup, world, stream):
+    """Public-API round trip per step: pinned host q/k/v/offsets/targets -> device,
+    forward, device o -> pinned host."""
+    hq, hk, hv, hoff, htg = host
+    dq, dk, dv, doff, dtg = dev
+    ho = torch.empty(call.o.shape, dtype=call.o.dtype, pin_memory=True)
+
+    def one():
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            doff.copy_(hoff, non_blocking=True)
+            dtg.copy_(htg, non_blocking=True)
+            call.launch(stream)
+            ho.copy_(call.o, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hoff, htg))
+    d2h = ho.numel() * ho.element_size()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def run_cuda(args):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from recommender_attention_gb300 import build as B
+    from recommender_attention_gb300 import hstu
+    if rank == 0 or not os.path.exists(B.LIB_PATH):
+        B.build()
+    barrier(world)
+    hstu.load_library()
+    stream = torch.cuda.Stream(device)
+
+    w = rank_workload(rank, args.hdim)
+    q, k, v = w.tensors()
+    call, dev = device_call(w, q, k, v, device)
+    st = call.stats(stream)
+    flops_step = 2.0 * (w.hdim_qk + w.hdim_v) * st["allowed_pairs"]
+    exec_flops = 2.0 * 128 * 128 * (w.hdim_qk + w.hdim_v) * st["executed_tiles"]
+
+    with ClockSampler(local) as clk:
+        step_ms, fwd_ms = time_device_steps(call, args.steps, args.warmup, world, stream)
+    clocks = clk.summary()
+    host = tuple(t.pin_memory() for t in (q, k, v, torch.from_numpy(w.seq_offsets_q()),
+                                          torch.from_numpy(w.num_targets())))
+    e2e_ms, h2d, d2h = time_e2e_steps(call, host, dev, args.steps, args.warmup, world, stream)
+
+    # the same workload at hdim 256 (one forward kernel per step, same timing rules)
+    extra = {}
+    if args.hdim == 128 and not args.no_d256:
+        del call, dev
+        torch.cuda.empty_cache()
+        w2 = rank_workload(rank, 256)
+        q2, k2, v2 = w2.tensors()
+        call2, dev2 = device_call(w2, q2, k2, v2, device)
+        st2 = call2.stats(stream)
+        f2 = 2.0 * (w2.hdim_qk + w2.hdim_v) * st2["allowed_pairs"]
+        s2, fw2 = time_device_steps(call2, args.steps, args.warmup, world, stream)
+        s2 = reduce_max(s2, world, device)
+        tot2 = reduce_sum(f2, world, device)
+        extra = {"hdim256": {"value": tot2 / (s2 * 1e-3) / 1e12, "ms_per_step": s2,
+                             "fwd_kernel_ms": fw2,
+                             "fwd_kernel_tflops": f2 / (fw2 * 1e-3) / 1e12}}
+        del call2, dev2
+
+    step_ms_max = reduce_max(step_ms, world, device)
+    e2e_ms_max = reduce_max(e2e_ms, world, device)
+    total_flops = reduce_sum(flops_step, world, device)
+    value = total_flops / (step_ms_max * 1e-3) / 1e12
+    e2e_value = total_flops / (e2e_ms_max * 1e-3) / 1e12
+
+    if rank == 0:
+        peaks, src = load_peaks()
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        achieved = flops_step / (fwd_ms * 1e-3) / 1e12
+        traffic = recorded_traffic()
+        cpu = None if args.no_cpu_baseline else cpu_baseline(w, q, k, v, budget_s=args.cpu_seconds)
+        launches_per_step = 2 + (1 if st["num_splits"] > 1 else 0)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic N(0,1) bf16, seed 7 (+rank)",
+            "config": {"workload": f"large jagged SiLU HSTU self-attention, hdim {w.hdim_qk}",
+                       "batch": w.batch, "nhead": w.nhead, "hdim_qk": w.hdim_qk,
+                       "hdim_v": w.hdim_v, "uih": "U_int[1024,4096]", "targets": "U_int[1,32]",
+                       "context_len": 6, "local_len": 0, "minfull_len": 0, "causal": 1,
+                       "total_tokens": w.total_q, "allowed_pairs": st["allowed_pairs"],
+                       "executed_tiles": st["executed_tiles"], "num_splits": st["num_splits"],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (q+k+v+o %.0f MB > 129 MB)" %
+                             ((q.numel() + k.numel() + v.numel() + q.numel()) * 2 / 1e6)},
+            "pct_of_bf16_peak": 100.0 * value / world / peak,
+            "executed_tile_tflops": reduce_sum(exec_flops, 1) / (step_ms_max * 1e-3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{src} bf16 dense (burst)",
+                         "kernel": "hstu_fwd_kernel<128,bf16,SiLU>", "kernel_ms": fwd_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- oracle arm
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def cpu_baseline(w, q, k, v, budget_s: float = 12.0):
+    """The fp64 oracle as it stands on a bounded sample: whole (sequence, head)
+    problems of the workload, longest sequence first, until the budget is spent."""
+    from oracle.hstu_oracle import HstuParams, SeqMaskParams, dense_mask, hstu_attention_forward_rows
+    p = HstuParams(num_groups=w.num_groups, context_len=w.context_len, local_len=w.local_len,
+                   minfull_len=w.minfull_len, max_uih_len=w.max_uih_len,
+                   attn_scale=w.attn_scale, alpha=w.alpha, causal=w.causal, softmax=w.softmax)
+    off = w.seq_offsets_q()
+    tg = w.num_targets()
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    qd, kd, vd = f64(q), f64(k), f64(v)
+    order = list(np.argsort(-w.lengths_q()))
+    flops, done = 0.0, 0
+    t0 = time.perf_counter()
+    for b in order:
+        L = int(off[b + 1] - off[b])
+        rows = np.arange(L)
+        for h in range(w.nhead):
+            hstu_attention_forward_rows(qd, kd, vd, off, None, tg, p, int(b), h, rows)
+            sp = SeqMaskParams(L_q=L, L_kv=L, context=int(w.context_len[0]), targets=int(tg[b]),
+                               causal=w.causal, local=int(w.local_len[0]),
+                               minfull=int(w.minfull_len[0]), cross=False)
+            flops += 2.0 * (w.hdim_qk + w.hdim_v) * float(dense_mask(sp).sum())
+            done += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} whole (sequence, head) problems of the {w.batch}x{w.nhead}, "
+                      f"longest first, fp64 numpy, {el:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = rank_workload(0, args.hdim)
+    q, k, v = w.tensors()
+    # each step: a bounded sample of the workload through the oracle
+    per_step = max(1.0, min(20.0, args.ref_seconds / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, q, k, v, budget_s=per_step)
+    vals = [cpu_baseline(w, q, k, v, budget_s=per_step) for _ in range(args.steps)]
+    value = statistics.mean(x["value"] for x in vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic N(0,1) bf16 rounded, seed 7",
+        "config": {"workload": f"large jagged SiLU HSTU self-attention, hdim {w.hdim_qk}",
+                   "batch": w.batch, "nhead": w.nhead},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                         "cores": vals[0]["cores"], "sample": vals[0]["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--hdim", type=int, default=128, choices=[64, 128, 256])
+    ap.add_argument("--no-d256", action="store_true", help="skip the hdim-256 repeat")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    if args.impl == "cuda":
+        args.warmup = max(3, args.warmup)   # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -104,6 +104,11 @@ typedef struct hstu_fwd_args {
   const float* attn_scale;        /* [host] [G] post-nonlinearity scale; 0 / NULL = 1/max_uih_len */
   void* workspace;                /* [dev] caller-owned scratch, 256-byte aligned */
   size_t workspace_bytes;         /* its size, >= hstu_attn_fwd_workspace_size() */
+  /* Optional cudaEvent_t handles (NULL = none), recorded on `stream` right
+   * before and right after the forward kernel's launch, so a caller can time
+   * that kernel alone (the scheduler and combine kernels fall outside). */
+  void* event_fwd_begin;
+  void* event_fwd_end;
 } hstu_fwd_args;
 
 /* Counters of one call's schedule (hstu_attn_fwd_stats). */

@@ -124,7 +124,7 @@ Plan make_plan(const hstu_fwd_args* a, int sms) {
   pl.off_scale = off;
   off = align256(off + kMaxGroups * sizeof(float));
   pl.off_scratch = off;
-  off = align256(off + 4ull * a->batch * sizeof(int));
+  off = align256(off + (4ull * a->batch + 2) * sizeof(int));
   pl.off_units = off;
   off = align256(off + static_cast<size_t>(pl.max_units) * sizeof(int4));
   pl.off_opart = pl.off_mlpart = 0;
@@ -282,11 +282,17 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   fp.alpha = a->alpha != 0.f ? a->alpha : 1.f / std::sqrt(static_cast<float>(a->hdim_qk));
   fill_group_params(a, fp.ctx, fp.loc, fp.mf);
   const int grid = pl.max_units < sms ? (pl.max_units > 0 ? pl.max_units : 1) : sms;
+  if (a->event_fwd_begin &&
+      cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_begin), stream) != cudaSuccess)
+    return HSTU_ERR_CUDA;
   cudaError_t e;
   if (D == 64) e = launch_fwd_d64(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
   else if (D == 128) e = launch_fwd_d128(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
   else e = launch_fwd_d256(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
   if (e != cudaSuccess) return HSTU_ERR_CUDA;
+  if (a->event_fwd_end &&
+      cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_end), stream) != cudaSuccess)
+    return HSTU_ERR_CUDA;
 
   if (pl.splits > 1) {
     CombineParams cp;

@@ -207,15 +207,17 @@ HSTU_HD void split_range(int count, int sp, int splits, int& k0, int& k1) {
 // True when every valid row of query tile m sees every key of key tile n, so
 // the per-element predicate can be skipped.  Conservative: may say false for a
 // tile that happens to be fully allowed, never true for one that is not.
-HSTU_HD bool tile_fully_allowed(const SeqGeom& s, int m, int n) {
-  const int i0 = m * kBlockM;
+// `b` is tile_uih_bounds of the query tile.
+HSTU_HD bool tile_fully_allowed(const SeqGeom& s, const TileBounds& b, int n) {
   const int j0 = n * kBlockN, j1 = j0 + kBlockN;
   if (j1 > s.Lkv) return false;
   if (j1 <= s.c) return true;
   if (j1 > s.c + s.ukv) return false;   // holds target keys
-  const TileBounds b = tile_uih_bounds(s, i0, i0 + kBlockM);
   const int jlo = j0 > s.c ? j0 : s.c;
   return b.maxLO <= jlo && b.minHI >= j1;
+}
+HSTU_HD bool tile_fully_allowed(const SeqGeom& s, int m, int n) {
+  return tile_fully_allowed(s, tile_uih_bounds(s, m * kBlockM, m * kBlockM + kBlockM), n);
 }
 
 // Launch parameters of the persistent forward kernel.
@@ -246,7 +248,7 @@ struct PrepParams {
   int4* units;
   int* ws_header;
   float* group_scale;
-  int* batch_scratch;      // [4 * batch] ints
+  int* batch_scratch;      // [4 * batch + 2] ints (used when batch is large)
   int batch, nhead, num_groups, batch_per_group, splits;
   int total_q, total_kv, max_seqlen_q, max_seqlen_kv, max_units;
   int causal, self_attn;

@@ -4,6 +4,10 @@
 
 namespace hstu {
 
+// dynamic (tiles + alignment slack) plus static (barriers, exchange buffers) shared memory
+// must fit the 227 KB a CTA may use on sm_103a.
+static_assert(FwdCfg<64>::SMEM_BYTES + sizeof(FwdSmemCtl) <= 232448, "shared memory over the per-CTA limit");
+
 namespace {
 template <bool BF16, bool SOFTMAX>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,

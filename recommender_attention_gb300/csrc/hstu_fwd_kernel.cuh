@@ -10,16 +10,24 @@
 // and writes O * attn_scale (softmax: / rowsum, plus LSE) or, with split-KV,
 // fp32 partials for the combine kernel.
 //
-// Roles (192 threads, one CTA per SM, all waits time-bounded):
+// Roles (320 threads, one CTA per SM, all waits time-bounded):
 //   warp 0       scheduler + TMA producer: fetches units from a global counter,
-//                loads Q once per unit and K/V tiles into STAGES-deep rings
+//                loads Q once per unit and K and V tiles into separate rings
 //   warp 1       TMEM owner + MMA issuer (one thread)
-//   warps 2..5   elementwise group: TMEM S -> registers, mask + SiLU/softmax,
-//                P -> TMEM; then the epilogue O -> registers -> global
+//   warps 2..9   elementwise groups: warpgroup g (warps 2+4g .. 5+4g) owns key
+//                columns [64g, 64g+64) of every score row, one row per thread:
+//                TMEM S -> registers, mask + SiLU/softmax, P -> TMEM; then the
+//                epilogue writes its half of the O columns
 //
-// TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores with the
-// 16-bit P of a tile packed into the first 64 columns of its own S buffer;
-// O [256, 256 + D).
+// TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores; the
+// 16-bit P of key columns [64g, 64g+64) is packed into S columns
+// [64g, 64g+32) of the same buffer;
+// O [256, 256 + D) and, for D <= 128, a second O buffer right after it so the
+// epilogue of one unit overlaps the next unit's P V products.
+//
+// SiLU is evaluated as SiLU(s) = h + h tanh(h), h = s/2, in packed 16-bit
+// arithmetic of the storage type (one tanh.approx per two elements); P is
+// rounded to that type for the second product in any case.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -34,13 +42,16 @@ struct FwdCfg {
   static constexpr int KCH = D / 64;                  // 128-byte column chunks per row
   static constexpr int TILE_BYTES = kBlockN * D * 2;  // one Q, K or V tile
   static constexpr int CHUNK_BYTES = kBlockN * 128;   // one 128-row x 128-byte TMA box
-  static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);
-  static constexpr int SMEM_BYTES = (1 + 2 * STAGES) * TILE_BYTES + 1024;
+  static constexpr int KSTAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);   // K ring depth
+  static constexpr int VSTAGES = D == 64 ? 4 : (D == 128 ? 2 : 1);   // V ring depth
+  static constexpr int SMEM_BYTES = (1 + KSTAGES + VSTAGES) * TILE_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
+  static constexpr int O_BUFS = D <= 128 ? 2 : 1;
 };
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 320;
+constexpr int kEwThreads = 256;   // two elementwise warpgroups
 constexpr int kSchedDepth = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
 
@@ -48,8 +59,12 @@ struct FwdSmemCtl {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t o_full, o_empty;
+  uint64_t o_full[2], o_empty[2];
   uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
+  uint64_t xch[2];            // softmax row-max exchange between the warpgroups, per tile parity
+  uint64_t lxch;              // softmax row-sum exchange, per unit
+  float xmax[2][2][128];      // [tile parity][warpgroup][row]
+  float xl[2][128];           // [warpgroup][row]
   int sched_unit[kSchedDepth];
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -66,20 +81,54 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-__device__ __forceinline__ float tanh_approx(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// SiLU of two raw scores a, b (fp32 bit patterns), scaled by alpha, as a packed
+// 16-bit pair (a in the low half).  ha2 = (alpha/2, alpha/2).
+template <bool BF16>
+__device__ __forceinline__ uint32_t silu_pair(uint32_t a, uint32_t b, uint64_t ha2) {
+  uint64_t s2, h2;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(s2) : "r"(a), "r"(b));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(h2) : "l"(s2), "l"(ha2));
+  float h0, h1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(h0), "=f"(h1) : "l"(h2));
+  uint32_t hp, tp, pp;
+  if constexpr (BF16) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hp) : "f"(h1), "f"(h0));
+    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(tp) : "r"(hp));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(pp) : "r"(hp), "r"(tp), "r"(hp));
+  } else {
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hp) : "f"(h1), "f"(h0));
+    asm("tanh.approx.f16x2 %0, %1;" : "=r"(tp) : "r"(hp));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(pp) : "r"(hp), "r"(tp), "r"(hp));
+  }
+  return pp;
+}
+
+// Per-row mask in tile-local column terms: key column c (0..127) of the tile
+// is allowed iff c < ctx || (unsigned)(c - lo) < span || c == diag.
+struct RowMask {
+  int ctx, lo, diag;
+  uint32_t span;
+  __device__ __forceinline__ bool allowed(int c) const {
+    return (c < ctx) | (static_cast<uint32_t>(c - lo) < span) | (c == diag);
+  }
+};
+
 struct UnitView {
   SeqGeom s;
   TileSet ts;
+  TileBounds tb;
   int m, h, g, sp, k0, k1;
 };
 
@@ -94,6 +143,7 @@ __device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
   u.s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[u.g], p.loc[u.g], p.mf[u.g], p.causal,
                   p.self_attn);
   u.ts = query_tile_kv_tiles(u.s, u.m);
+  u.tb = tile_uih_bounds(u.s, u.m * kBlockM, u.m * kBlockM + kBlockM);
   split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);
   return u;
 }
@@ -119,20 +169,41 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
   return ok;
 }
 
+// SiLU of the 64 scores of key columns [c0, c0+64) of one row (fp32 bit
+// patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.
+template <bool BF16, bool MASKED>
+__device__ __forceinline__ void silu_half(uint32_t (&r)[64], uint32_t p_tmem, uint64_t ha2,
+                                          const RowMask& rm, int c0) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    uint32_t v = silu_pair<BF16>(r[2 * k], r[2 * k + 1], ha2);
+    if constexpr (MASKED) {
+      const uint32_t m = (rm.allowed(c0 + 2 * k) ? 0x0000FFFFu : 0u) |
+                         (rm.allowed(c0 + 2 * k + 1) ? 0xFFFF0000u : 0u);
+      v &= m;
+    }
+    pk[k] = v;
+  }
+  ptx::tmem_st32(p_tmem, pk);
+}
+
 template <int D, bool BF16, bool SOFTMAX>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
   using Cfg = FwdCfg<D>;
   constexpr int KCH = Cfg::KCH;
-  constexpr int STAGES = Cfg::STAGES;
+  constexpr int KST = Cfg::KSTAGES;
+  constexpr int VST = Cfg::VSTAGES;
+  constexpr int OB = Cfg::O_BUFS;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + Cfg::TILE_BYTES;
-  uint8_t* sV = sK + STAGES * Cfg::TILE_BYTES;
+  uint8_t* sV = sK + KST * Cfg::TILE_BYTES;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -141,22 +212,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (tid == 0) {
     ptx::mbar_init(&ctl.q_full, 1);
     ptx::mbar_init(&ctl.q_empty, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < KST; ++s) {
       ptx::mbar_init(&ctl.k_full[s], 1);
       ptx::mbar_init(&ctl.k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       ptx::mbar_init(&ctl.v_full[s], 1);
       ptx::mbar_init(&ctl.v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&ctl.s_full[s], 1);
-      ptx::mbar_init(&ctl.p_full[s], 128);
+      ptx::mbar_init(&ctl.p_full[s], kEwThreads);
       ptx::mbar_init(&ctl.pv_done[s], 1);
+      ptx::mbar_init(&ctl.o_full[s], 1);
+      ptx::mbar_init(&ctl.o_empty[s], kEwThreads);
+      ptx::mbar_init(&ctl.xch[s], kEwThreads);
     }
-    ptx::mbar_init(&ctl.o_full, 1);
-    ptx::mbar_init(&ctl.o_empty, 128);
+    ptx::mbar_init(&ctl.lxch, kEwThreads);
     for (int s = 0; s < kSchedDepth; ++s) {
       ptx::mbar_init(&ctl.sched_full[s], 1);
-      ptx::mbar_init(&ctl.sched_empty[s], 5);
+      ptx::mbar_init(&ctl.sched_empty[s], 1 + kEwThreads / 32);
     }
     ctl.abort_flag = 0;
     ptx::fence_barrier_init();
@@ -199,20 +274,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         bool ok = true;
         for (int k = u.k0; k < u.k1 && ok; ++k) {
           const int n = tileset_at(u.ts, k);
-          const int st = kv_it % STAGES;
-          const uint32_t ph = ((kv_it / STAGES) & 1) ^ 1;
           const int krow = u.s.kv0 + n * kBlockN;
-          if (!wait_or_abort(ctl, p, &ctl.k_empty[st], ph)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&ctl.k_full[st], Cfg::TILE_BYTES);
+          const int ks = kv_it % KST, vs = kv_it % VST;
+          if (!wait_or_abort(ctl, p, &ctl.k_empty[ks], ((kv_it / KST) & 1) ^ 1)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.k_full[ks], Cfg::TILE_BYTES);
 #pragma unroll
           for (int kc = 0; kc < KCH; ++kc)
-            ptx::tma_load_2d(sK + st * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_k, &ctl.k_full[st],
+            ptx::tma_load_2d(sK + ks * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_k, &ctl.k_full[ks],
                              u.h * D + kc * 64, krow);
-          if (!wait_or_abort(ctl, p, &ctl.v_empty[st], ph)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&ctl.v_full[st], Cfg::TILE_BYTES);
+          if (!wait_or_abort(ctl, p, &ctl.v_empty[vs], ((kv_it / VST) & 1) ^ 1)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::TILE_BYTES);
 #pragma unroll
           for (int kc = 0; kc < KCH; ++kc)
-            ptx::tma_load_2d(sV + st * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[st],
+            ptx::tma_load_2d(sV + vs * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[vs],
                              u.h * D + kc * 64, krow);
           ++kv_it;
         }
@@ -229,10 +303,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t v_base = ptx::smem_u32(sV);
       int q_it = 0, kv_it = 0, s_it = 0, sched_it = 0;
       bool ok = true;
-      // S = Q K^T for the tile held in K stage (kvi % STAGES), into S buffer (si & 1).
+      // S = Q K^T for the tile held in K stage (kvi % KST), into S buffer (si & 1).
       auto issue_qk = [&](int kvi, int si) -> bool {
-        const int st = kvi % STAGES;
-        if (!wait_or_abort(ctl, p, &ctl.k_full[st], (kvi / STAGES) & 1)) return false;
+        const int st = kvi % KST;
+        if (!wait_or_abort(ctl, p, &ctl.k_full[st], (kvi / KST) & 1)) return false;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + (si & 1) * 128;
 #pragma unroll
@@ -256,6 +330,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const UnitView u = decode_unit(p, unit);
         const int nt = u.k1 - u.k0;
         if (nt <= 0) continue;
+        const int ob = q_it % OB;
+        const uint32_t o_tmem = tmem + Cfg::O_COL + ob * D;
         if (!wait_or_abort(ctl, p, &ctl.q_full, q_it & 1)) break;
         ptx::tc_fence_after();
         if (!issue_qk(kv_it, s_it)) break;
@@ -269,26 +345,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
           if (idx == 0) {
-            if (!wait_or_abort(ctl, p, &ctl.o_empty, (q_it & 1) ^ 1)) { ok = false; break; }
+            if (!wait_or_abort(ctl, p, &ctl.o_empty[ob], ((q_it / OB) & 1) ^ 1)) { ok = false; break; }
             ptx::tc_fence_after();
           }
           const int kvi = kv_it + idx;
-          const int st = kvi % STAGES;
-          if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / STAGES) & 1)) { ok = false; break; }
+          const int st = kvi % VST;
+          if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t p_tmem = tmem + (si & 1) * 128;
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk) {
             const uint64_t bd = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES + kk * 2048,
                                                  Cfg::CHUNK_BYTES, 1024);
-            ptx::umma_ts(tmem + Cfg::O_COL, p_tmem + kk * 8, bd, idesc_pv,
+            ptx::umma_ts(o_tmem, p_tmem + (kk >> 2) * 64 + (kk & 3) * 8, bd, idesc_pv,
                          (idx > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::umma_commit(&ctl.v_empty[st]);
           if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
         }
         if (!ok) break;
-        ptx::umma_commit(&ctl.o_full);
+        ptx::umma_commit(&ctl.o_full[ob]);
         kv_it += nt;
         s_it += nt;
         ++q_it;
@@ -296,11 +372,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ elementwise + epilogue
-    const int quarter = warp & 3;
+    const int wg = (warp - 2) >> 2;          // warpgroup: key columns [64 wg, 64 wg + 64)
+    const int quarter = warp & 3;            // TMEM lane quarter this warp may access
+    const int rloc = quarter * 32 + lane;    // row within the query tile
+    const int c0 = wg * 64;
+    constexpr int DH = D / 2;                // O columns per warpgroup
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const float half_alpha = 0.5f * p.alpha;
+    const uint64_t ha2 = f32x2(0.5f * p.alpha, 0.5f * p.alpha);
     const float scale_log2 = p.alpha * 1.4426950408889634f;
-    int s_it = 0, q_it = 0, sched_it = 0;
+    int s_it = 0, q_it = 0, sched_it = 0, l_it = 0;
     while (!ctl.abort_flag) {
       const int slot = sched_it % kSchedDepth;
       if (!warp_wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
@@ -311,72 +391,56 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (unit < 0) break;
       const UnitView u = decode_unit(p, unit);
       const int nt = u.k1 - u.k0;
-      const int row = u.m * kBlockM + quarter * 32 + lane;
+      const int row = u.m * kBlockM + rloc;
       const bool valid = row < u.s.Lq;
       int r_lo, r_hi;
       row_uih_keys(u.s, valid ? row : 0, r_lo, r_hi);
       int r_diag = row_diag_key(u.s, row);
       int r_ctx = u.s.c;
       if (!valid) { r_lo = r_hi = 0; r_diag = -1; r_ctx = 0; }
-      const uint32_t r_span = static_cast<uint32_t>(r_hi - r_lo);
       const float attn_scale = p.group_scale[u.g];
       const long long grow = static_cast<long long>(u.s.q0) + row;   // global token row
+      const int ob = q_it % OB;
+      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * D + wg * DH;
 
-      float m_run = -INFINITY, l_run = 0.f;   // softmax row state (log2 domain)
+      float m_run = -INFINITY, l_run = 0.f;   // softmax row state (log2 domain); l over own columns
       bool ok = true;
       for (int idx = 0; idx < nt; ++idx) {
         const int n = tileset_at(u.ts, u.k0 + idx);
-        const bool full = tile_fully_allowed(u.s, u.m, n);
+        const bool full = tile_fully_allowed(u.s, u.tb, n);
         const int j0 = n * kBlockN;
+        RowMask rm;
+        rm.ctx = r_ctx - j0;
+        rm.lo = r_lo - j0;
+        rm.span = static_cast<uint32_t>(r_hi - r_lo);
+        rm.diag = r_diag >= 0 ? r_diag - j0 : -1000000;
         const int si = s_it + idx;
         if (!warp_wait_or_abort(ctl, p, &ctl.s_full[si & 1], (si >> 1) & 1)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t s_tmem = tmem + lane_base + (si & 1) * 128;
+        const uint32_t s_tmem = tmem + lane_base + (si & 1) * 128 + c0;
+        uint32_t r[64];
+        ptx::tmem_ld64(s_tmem, r);
+        ptx::tmem_ld_wait(r);
         if constexpr (!SOFTMAX) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            ptx::tmem_ld32(s_tmem + c * 32, r);
-            ptx::tmem_ld_wait(r);
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              float pv[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float hh = __uint_as_float(r[k + e]) * half_alpha;
-                float v = fmaf(hh, tanh_approx(hh), hh);   // SiLU(2hh) = hh * (1 + tanh(hh))
-                if (!full) {
-                  const int j = j0 + c * 32 + k + e;
-                  const bool al = (j < r_ctx) | (static_cast<uint32_t>(j - r_lo) < r_span) | (j == r_diag);
-                  v = al ? v : 0.f;
-                }
-                pv[e] = v;
-              }
-              pk[k >> 1] = pack2<BF16>(pv[0], pv[1]);
-            }
-            ptx::tmem_st16(s_tmem + c * 16, pk);
-          }
+          if (full) silu_half<BF16, false>(r, s_tmem, ha2, rm, c0);
+          else silu_half<BF16, true>(r, s_tmem, ha2, rm, c0);
         } else {
-          uint32_t r[4][32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_tmem + c * 32, r[c]);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(r[c]);
           float mx = -INFINITY;
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int k = 0; k < 64; ++k) mx = fmaxf(mx, __uint_as_float(r[k]));
+          } else {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              float v = __uint_as_float(r[c][k]) * scale_log2;
-              if (!full) {
-                const int j = j0 + c * 32 + k;
-                const bool al = (j < r_ctx) | (static_cast<uint32_t>(j - r_lo) < r_span) | (j == r_diag);
-                v = al ? v : -INFINITY;
-              }
-              r[c][k] = __float_as_uint(v);
-              mx = fmaxf(mx, v);
+            for (int k = 0; k < 64; ++k) {
+              if (!rm.allowed(c0 + k)) r[k] = 0xFF800000u;   // -inf
+              mx = fmaxf(mx, __uint_as_float(r[k]));
             }
+          }
+          // row max over both halves
+          ctl.xmax[si & 1][wg][rloc] = mx;
+          ptx::mbar_arrive(&ctl.xch[si & 1]);
+          if (!warp_wait_or_abort(ctl, p, &ctl.xch[si & 1], (si >> 1) & 1)) { ok = false; break; }
+          mx = fmaxf(mx, ctl.xmax[si & 1][wg ^ 1][rloc]) * scale_log2;
           // PV of the tile before last must be complete before this tile; keeps the
           // parity tracking of pv_done unambiguous.
           if (si >= 2) {
@@ -384,15 +448,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           if (mx > m_run + 8.0f) {
             // New running max; rescale what O already holds (only after a previous
-            // tile of this unit, whose PV must have completed).
+            // tile of this unit, whose PV must have completed).  Both warpgroups take
+            // the same decision from the same maxima.
             if (idx > 0 && m_run != -INFINITY) {
               const int sp = si - 1;
               if (!warp_wait_or_abort(ctl, p, &ctl.pv_done[sp & 1], (sp >> 1) & 1)) { ok = false; break; }
               ptx::tc_fence_after();
               const float corr = ex2_approx(m_run - mx);
-              const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL;
 #pragma unroll 1
-              for (int c = 0; c < D / 32; ++c) {
+              for (int c = 0; c < DH / 32; ++c) {
                 uint32_t o[32];
                 ptx::tmem_ld32(o_tmem + c * 32, o);
                 ptx::tmem_ld_wait(o);
@@ -404,21 +468,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             m_run = mx;
           }
-          const float mref = m_run == -INFINITY ? 0.f : m_run;
-          float lsum = 0.f;
+          const float nm = m_run == -INFINITY ? 0.f : -m_run;
+          const uint64_t sc2 = f32x2(scale_log2, scale_log2), nm2 = f32x2(nm, nm);
+          float lsum0 = 0.f, lsum1 = 0.f;
+          uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const float e0 = ex2_approx(__uint_as_float(r[c][k]) - mref);
-              const float e1 = ex2_approx(__uint_as_float(r[c][k + 1]) - mref);
-              pk[k >> 1] = pack2<BF16>(e0, e1);
-              lsum += e0 + e1;
-            }
-            ptx::tmem_st16(s_tmem + c * 16, pk);
+          for (int k = 0; k < 32; ++k) {
+            uint64_t s2, x2;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(s2) : "r"(r[2 * k]), "r"(r[2 * k + 1]));
+            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x2) : "l"(s2), "l"(sc2), "l"(nm2));
+            float x0, x1;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(x2));
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            lsum0 += e0;
+            lsum1 += e1;
+            pk[k] = pack2<BF16>(e0, e1);
           }
-          l_run += lsum;
+          ptx::tmem_st32(s_tmem, pk);
+          l_run += lsum0 + lsum1;
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -428,15 +495,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
       // ---------------------------------------------------------- epilogue
       if (nt > 0) {
-        if (!warp_wait_or_abort(ctl, p, &ctl.o_full, q_it & 1)) break;
+        if (!warp_wait_or_abort(ctl, p, &ctl.o_full[ob], (q_it / OB) & 1)) break;
         ptx::tc_fence_after();
+      }
+      if constexpr (SOFTMAX) {
+        if (nt > 0) {   // full row sum = both warpgroups' column sums
+          ctl.xl[wg][rloc] = l_run;
+          ptx::mbar_arrive(&ctl.lxch);
+          if (!warp_wait_or_abort(ctl, p, &ctl.lxch, l_it & 1)) break;
+          l_run += ctl.xl[wg ^ 1][rloc];
+          ++l_it;
+        }
       }
       const bool write_part = p.splits > 1;
       float mul = attn_scale;
       if constexpr (SOFTMAX) mul = l_run > 0.f ? attn_scale / l_run : 0.f;
-      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         uint32_t o[32];
         if (nt > 0) {
           ptx::tmem_ld32(o_tmem + c * 32, o);
@@ -446,9 +521,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int k = 0; k < 32; ++k) o[k] = 0u;
         }
         if (!valid) continue;
+        const int col = wg * DH + c * 32;
         if (write_part) {
           float* dst = p.o_part +
-                       ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * D + c * 32;
+                       ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * D + col;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
@@ -457,7 +533,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
             pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
-          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * D + c * 32;
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * D + col;
 #pragma unroll
           for (int k = 0; k < 16; k += 4)
             *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
@@ -465,10 +541,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (nt > 0) {
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.o_empty);
+        ptx::mbar_arrive(&ctl.o_empty[ob]);
         ++q_it;
       }
-      if (valid) {
+      if (valid && wg == 0) {
         if (write_part) {
           if constexpr (SOFTMAX) {
             float* ml = p.ml_part + ((static_cast<long long>(u.sp) * p.nhead + u.h) * p.total_q + grow) * 2;

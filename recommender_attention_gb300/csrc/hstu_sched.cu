@@ -27,6 +27,7 @@ namespace {
 
 constexpr int kPrepThreads = 1024;
 constexpr int kSortMaxBatch = 2048;   // above this the sequences keep their input order
+constexpr int kPrepSmemBatch = 2048;  // scratch arrays live in shared memory up to this batch
 
 __device__ __forceinline__ int warp_incl_scan(int v) {
   const int lane = threadIdx.x & 31;
@@ -38,13 +39,58 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
   return v;
 }
 
+// Exclusive prefix sum of data[0, n) in place; data[n] receives the total.
+// Every thread of the block must call it.
+__device__ int block_exclusive_scan(int* data, int n, int* s_wsum) {
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
+  const int per = (n + nth - 1) / nth;
+  const int beg = min(tid * per, n), end = min(beg + per, n);
+  int local = 0;
+  for (int i = beg; i < end; ++i) local += data[i];
+  const int incl = warp_incl_scan(local);
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < nwarps ? s_wsum[lane] : 0;
+    v = warp_incl_scan(v);
+    s_wsum[lane] = v;
+  }
+  __syncthreads();
+  int run = incl - local + (warp > 0 ? s_wsum[warp - 1] : 0);
+  for (int i = beg; i < end; ++i) {
+    const int v = data[i];
+    data[i] = run;
+    run += v;
+  }
+  const int total = s_wsum[nwarps - 1];
+  if (tid == 0) data[n] = total;
+  __syncthreads();
+  return total;
+}
+
+// Largest index k in [0, n) with a[k] <= x (a non-decreasing, a[0] <= x).
+__device__ __forceinline__ int find_segment(const int* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_constant__ PrepParams p) {
+  extern __shared__ int dsm[];
   __shared__ int s_gmax[kMaxGroups];
   __shared__ int s_err;
   __shared__ unsigned long long s_tiles;
   __shared__ int s_wsum[32];
   const int tid = threadIdx.x, nth = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
+  const int B = p.batch;
+  int* tbase = B <= kPrepSmemBatch ? dsm : p.batch_scratch;   // [B+1] query-tile offsets
+  int* cost = tbase + (B + 1);                                 // [B] key tiles per sequence
+  int* order = cost + B;                                       // [B] sequences, longest first
+  int* ubase = order + B;                                      // [B+1] unit offsets by position
   for (int g = tid; g < kMaxGroups; g += nth) s_gmax[g] = 0;
   if (tid == 0) {
     s_err = 0;
@@ -52,12 +98,8 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
   }
   __syncthreads();
 
-  int* cost = p.batch_scratch;               // executed key tiles of sequence b (one head)
-  int* nq = p.batch_scratch + p.batch;       // query tiles of sequence b
-  int* order = p.batch_scratch + 2 * p.batch;
-
-  // 1. validate every sequence and count its tiles
-  for (int b = tid; b < p.batch; b += nth) {
+  // 1. validate every sequence; query tiles per sequence
+  for (int b = tid; b < B; b += nth) {
     const int g = b / p.batch_per_group;
     const int c = p.ctx[g];
     int err = 0;
@@ -73,18 +115,10 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
       if (Lkv < c) err |= kErrKvLayout;
     }
     if (q1 - q0 > p.max_seqlen_q || Lkv > p.max_seqlen_kv) err |= kErrMaxSeqlen;
-    int cst = 0, n = 0;
-    if (err == 0) {
-      const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, c, p.loc[g], p.mf[g], p.causal,
-                                  p.self_attn);
-      n = (s.Lq + kBlockM - 1) / kBlockM;
-      for (int m = 0; m < n; ++m) cst += query_tile_kv_tiles(s, m).count;
-      atomicMax(&s_gmax[g], s.u);
-    } else {
-      atomicOr(&s_err, err);
-    }
-    cost[b] = cst;
-    nq[b] = n;
+    if (err) atomicOr(&s_err, err);
+    else atomicMax(&s_gmax[g], q1 - q0 - c - t);
+    tbase[b] = err ? 0 : (q1 - q0 + kBlockM - 1) / kBlockM;
+    cost[b] = 0;
   }
   __syncthreads();
   if (s_err != 0) {
@@ -96,15 +130,32 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     }
     return;
   }
+  const int n_items = block_exclusive_scan(tbase, B, s_wsum);
 
-  // 2. longest sequence first (stable rank sort on the executed-tile count)
-  const bool sort = p.batch <= kSortMaxBatch;
-  for (int b = tid; b < p.batch; b += nth) {
+  // 2. key tiles of every (sequence, query tile)
+  unsigned long long tiles = 0ull;
+  for (int i = tid; i < n_items; i += nth) {
+    const int b = find_segment(tbase, B, i);
+    const int g = b / p.batch_per_group;
+    const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[g], p.loc[g], p.mf[g], p.causal,
+                                p.self_attn);
+    const int cnt = query_tile_kv_tiles(s, i - tbase[b]).count;
+    atomicAdd(&cost[b], cnt);
+    tiles += cnt;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tiles += __shfl_down_sync(0xffffffffu, tiles, o);
+  if ((tid & 31) == 0 && tiles) atomicAdd(&s_tiles, tiles * static_cast<unsigned long long>(p.nhead));
+  __syncthreads();
+
+  // 3. longest sequence first (stable rank sort on the executed-tile count)
+  const bool sort = B <= kSortMaxBatch;
+  for (int b = tid; b < B; b += nth) {
     int r = b;
     if (sort) {
       const int cb = cost[b];
       r = 0;
-      for (int b2 = 0; b2 < p.batch; ++b2) {
+      for (int b2 = 0; b2 < B; ++b2) {
         const int c2 = cost[b2];
         r += (c2 > cb) | ((c2 == cb) & (b2 < b));
       }
@@ -112,22 +163,12 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     order[r] = b;
   }
   __syncthreads();
-
-  // 3. unit offsets of each sorted position: block-wide exclusive scan
-  const int per = (p.batch + nth - 1) / nth;
-  const int pbeg = min(tid * per, p.batch), pend = min(pbeg + per, p.batch);
-  int local = 0;
-  for (int pos = pbeg; pos < pend; ++pos) local += nq[order[pos]] * p.nhead * p.splits;
-  const int incl = warp_incl_scan(local);
-  if (lane == 31) s_wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int v = lane < nwarps ? s_wsum[lane] : 0;
-    v = warp_incl_scan(v);
-    s_wsum[lane] = v;
+  for (int pos = tid; pos < B; pos += nth) {
+    const int b = order[pos];
+    ubase[pos] = (tbase[b + 1] - tbase[b]) * p.nhead * p.splits;
   }
   __syncthreads();
-  const int total = s_wsum[nwarps - 1];
+  const int total = block_exclusive_scan(ubase, B, s_wsum);
   if (total > p.max_units) {
     if (tid == 0) {
       p.ws_header[kWsError] = kErrMaxSeqlen;
@@ -137,20 +178,20 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     }
     return;
   }
-  int u = incl - local + (warp > 0 ? s_wsum[warp - 1] : 0);
 
   // 4. units: per sequence, heads outer, query tiles from the last (most key
   //    tiles under a causal mask) down, splits innermost
-  unsigned long long tiles = 0ull;
-  for (int pos = pbeg; pos < pend; ++pos) {
+  for (int u = tid; u < total; u += nth) {
+    const int pos = find_segment(ubase, B, u);
     const int b = order[pos];
-    const int n = nq[b];
-    for (int h = 0; h < p.nhead; ++h)
-      for (int m = n - 1; m >= 0; --m)
-        for (int sp = 0; sp < p.splits; ++sp) p.units[u++] = make_int4(b, m, h, sp);
-    tiles += static_cast<unsigned long long>(cost[b]) * p.nhead;
+    const int nq = tbase[b + 1] - tbase[b];
+    const int per_h = nq * p.splits;
+    const int local = u - ubase[pos];
+    const int h = local / per_h;
+    const int rem = local - h * per_h;
+    const int m = nq - 1 - rem / p.splits;
+    p.units[u] = make_int4(b, m, h, rem % p.splits);
   }
-  if (tiles) atomicAdd(&s_tiles, tiles);
 
   // 5. attn_scale per group: 0 means 1 / (max UIH length of the group)
   for (int g = tid; g < p.num_groups; g += nth) {
@@ -273,7 +314,8 @@ cudaError_t launch_wait_selftest(int* result, unsigned long long timeout_ns, cud
 }
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
-  hstu_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p);
+  const size_t dsmem = p.batch <= kPrepSmemBatch ? (4 * static_cast<size_t>(p.batch) + 2) * sizeof(int) : 0;
+  hstu_prep_kernel<<<1, kPrepThreads, dsmem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,7 @@ class FwdArgs(ctypes.Structure):
         ("context_len", ctypes.c_void_p), ("minfull_len", ctypes.c_void_p),
         ("max_uih_len", ctypes.c_void_p), ("attn_scale", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("event_fwd_begin", ctypes.c_void_p), ("event_fwd_end", ctypes.c_void_p),
     ]
 
 
@@ -173,8 +174,16 @@ class HstuCall:
         a.workspace = workspace.data_ptr()
         a.workspace_bytes = workspace.numel()
 
-    def launch(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+    def launch(self, stream: Optional[torch.cuda.Stream] = None,
+               events: Optional[tuple] = None) -> None:
+        """Enqueues the forward on `stream`.  `events` = (begin, end) torch.cuda.Event
+        pair recorded around the forward kernel alone (both recorded once before)."""
+        if events is not None:
+            self.args.event_fwd_begin = events[0].cuda_event
+            self.args.event_fwd_end = events[1].cuda_event
         st = self.lib.hstu_attn_fwd(ctypes.byref(self.args), ctypes.c_void_p(_stream_handle(stream)))
+        if events is not None:
+            self.args.event_fwd_begin = self.args.event_fwd_end = None
         if st != HSTU_OK:
             raise HstuError(st, "hstu_attn_fwd")
 
