@@ -134,68 +134,76 @@ HSTU_HD TileBounds tile_uih_bounds(const SeqGeom& s, int i0, int i1) {
 
 // Key tiles (of kBlockN keys) a query tile touches, as up to three sorted,
 // disjoint tile-index ranges: the context keys, the UIH hull, the target
-// diagonal.
+// diagonal.  Empty slots hold [kNoTile, kNoTile).  Written with fixed slots and
+// a compare-swap network (no runtime array indexing) so it stays in registers.
+constexpr int kNoTile = 0x3fffffff;
 struct TileSet {
-  int lo[3], hi[3];
-  int nr;      // number of ranges
+  int lo0, hi0, lo1, hi1, lo2, hi2;
   int count;   // number of tiles
 };
+
+HSTU_HD void tile_range_swap_if(int& alo, int& ahi, int& blo, int& bhi) {
+  if (blo < alo) {
+    const int tl = alo, th = ahi;
+    alo = blo; ahi = bhi;
+    blo = tl; bhi = th;
+  }
+}
 
 HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, int m) {
   const int i0 = m * kBlockM;
   const int i1 = (i0 + kBlockM < s.Lq) ? i0 + kBlockM : s.Lq;
-  int rlo[3], rhi[3], n = 0;
+  TileSet t;
+  t.lo0 = t.hi0 = t.lo1 = t.hi1 = t.lo2 = t.hi2 = kNoTile;
   if (s.c > 0 && i1 > i0) {
-    rlo[n] = 0;
-    rhi[n] = (s.c + kBlockN - 1) / kBlockN;
-    ++n;
+    t.lo0 = 0;
+    t.hi0 = (s.c + kBlockN - 1) / kBlockN;
   }
   const TileBounds b = tile_uih_bounds(s, i0, i1);
   if (b.HI > b.LO) {
-    rlo[n] = b.LO / kBlockN;
-    rhi[n] = (b.HI + kBlockN - 1) / kBlockN;
-    ++n;
+    t.lo1 = b.LO / kBlockN;
+    t.hi1 = (b.HI + kBlockN - 1) / kBlockN;
   }
   if (s.self_attn) {
     const int d0 = i0 > s.c + s.u ? i0 : s.c + s.u;
     if (i1 > d0) {
-      rlo[n] = d0 / kBlockN;
-      rhi[n] = (i1 + kBlockN - 1) / kBlockN;
-      ++n;
+      t.lo2 = d0 / kBlockN;
+      t.hi2 = (i1 + kBlockN - 1) / kBlockN;
     }
   }
-  // sort the (at most three) ranges by start, then merge overlapping/adjacent ones
-  for (int a = 0; a < n; ++a)
-    for (int c = a + 1; c < n; ++c)
-      if (rlo[c] < rlo[a]) {
-        int t0 = rlo[a], t1 = rhi[a];
-        rlo[a] = rlo[c]; rhi[a] = rhi[c];
-        rlo[c] = t0; rhi[c] = t1;
-      }
-  TileSet ts;
-  ts.nr = 0;
-  ts.count = 0;
-  for (int a = 0; a < n; ++a) {
-    if (ts.nr > 0 && rlo[a] <= ts.hi[ts.nr - 1]) {
-      if (rhi[a] > ts.hi[ts.nr - 1]) ts.hi[ts.nr - 1] = rhi[a];
-    } else {
-      ts.lo[ts.nr] = rlo[a];
-      ts.hi[ts.nr] = rhi[a];
-      ++ts.nr;
+  // sort the three slots by start (empty slots sort last)
+  tile_range_swap_if(t.lo0, t.hi0, t.lo1, t.hi1);
+  tile_range_swap_if(t.lo1, t.hi1, t.lo2, t.hi2);
+  tile_range_swap_if(t.lo0, t.hi0, t.lo1, t.hi1);
+  // merge overlapping or adjacent ranges into the earlier slot
+  if (t.lo1 != kNoTile && t.lo1 <= t.hi0) {
+    t.hi0 = t.hi1 > t.hi0 ? t.hi1 : t.hi0;
+    t.lo1 = t.lo2; t.hi1 = t.hi2;
+    t.lo2 = t.hi2 = kNoTile;
+  }
+  if (t.lo2 != kNoTile) {
+    if (t.lo2 <= t.hi1) {
+      t.hi1 = t.hi2 > t.hi1 ? t.hi2 : t.hi1;
+      t.lo2 = t.hi2 = kNoTile;
     }
   }
-  for (int a = 0; a < ts.nr; ++a) ts.count += ts.hi[a] - ts.lo[a];
-  for (int a = ts.nr; a < 3; ++a) ts.lo[a] = ts.hi[a] = 0;
-  return ts;
+  if (t.lo1 != kNoTile && t.lo1 <= t.hi0) {
+    t.hi0 = t.hi1 > t.hi0 ? t.hi1 : t.hi0;
+    t.lo1 = t.lo2; t.hi1 = t.hi2;
+    t.lo2 = t.hi2 = kNoTile;
+  }
+  t.count = (t.hi0 - t.lo0) + (t.hi1 - t.lo1) + (t.hi2 - t.lo2);
+  return t;
 }
 
 // The k-th tile (0-based) of a tile set.
 HSTU_HD int tileset_at(const TileSet& ts, int k) {
-  if (k < ts.hi[0] - ts.lo[0]) return ts.lo[0] + k;
-  k -= ts.hi[0] - ts.lo[0];
-  if (k < ts.hi[1] - ts.lo[1]) return ts.lo[1] + k;
-  k -= ts.hi[1] - ts.lo[1];
-  return ts.lo[2] + k;
+  const int n0 = ts.hi0 - ts.lo0;
+  if (k < n0) return ts.lo0 + k;
+  k -= n0;
+  const int n1 = ts.hi1 - ts.lo1;
+  if (k < n1) return ts.lo1 + k;
+  return ts.lo2 + (k - n1);
 }
 
 // Tiles [k0, k1) of the set belong to split `sp` of `splits`.

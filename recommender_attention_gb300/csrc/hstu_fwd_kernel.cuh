@@ -94,20 +94,22 @@ __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
 }
 
 // SiLU of two raw scores a, b (fp32 bit patterns), scaled by alpha, as a packed
-// 16-bit pair (a in the low half).  ha2 = (alpha/2, alpha/2).
+// 16-bit pair (a in the low half).  `ha` holds alpha/2: for bf16 as a packed
+// pair (the raw scores are rounded to bf16 first, whose range is fp32's); for
+// fp16 as an fp32 bit pattern (the scale is applied in fp32 so large raw
+// scores cannot overflow fp16 before scaling).
 template <bool BF16>
-__device__ __forceinline__ uint32_t silu_pair(uint32_t a, uint32_t b, uint64_t ha2) {
-  uint64_t s2, h2;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(s2) : "r"(a), "r"(b));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(h2) : "l"(s2), "l"(ha2));
-  float h0, h1;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(h0), "=f"(h1) : "l"(h2));
+__device__ __forceinline__ uint32_t silu_pair(uint32_t a, uint32_t b, uint32_t ha) {
   uint32_t hp, tp, pp;
   if constexpr (BF16) {
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hp) : "f"(h1), "f"(h0));
+    uint32_t sp;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(sp) : "r"(b), "r"(a));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hp) : "r"(sp), "r"(ha));
     asm("tanh.approx.bf16x2 %0, %1;" : "=r"(tp) : "r"(hp));
     asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(pp) : "r"(hp), "r"(tp), "r"(hp));
   } else {
+    const float h0 = __uint_as_float(a) * __uint_as_float(ha);
+    const float h1 = __uint_as_float(b) * __uint_as_float(ha);
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hp) : "f"(h1), "f"(h0));
     asm("tanh.approx.f16x2 %0, %1;" : "=r"(tp) : "r"(hp));
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(pp) : "r"(hp), "r"(tp), "r"(hp));
@@ -172,7 +174,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
 // SiLU of the 64 scores of key columns [c0, c0+64) of one row (fp32 bit
 // patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.
 template <bool BF16, bool MASKED>
-__device__ __forceinline__ void silu_half(uint32_t (&r)[64], uint32_t p_tmem, uint64_t ha2,
+__device__ __forceinline__ void silu_half(uint32_t (&r)[64], uint32_t p_tmem, uint32_t ha2,
                                           const RowMask& rm, int c0) {
   uint32_t pk[32];
 #pragma unroll
@@ -378,7 +380,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int c0 = wg * 64;
     constexpr int DH = D / 2;                // O columns per warpgroup
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint64_t ha2 = f32x2(0.5f * p.alpha, 0.5f * p.alpha);
+    uint32_t ha2;   // alpha/2 in the form silu_pair takes
+    if constexpr (BF16) ha2 = pack2<true>(0.5f * p.alpha, 0.5f * p.alpha);
+    else ha2 = __float_as_uint(0.5f * p.alpha);
     const float scale_log2 = p.alpha * 1.4426950408889634f;
     int s_it = 0, q_it = 0, sched_it = 0, l_it = 0;
     while (!ctl.abort_flag) {
@@ -469,17 +473,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             m_run = mx;
           }
           const float nm = m_run == -INFINITY ? 0.f : -m_run;
-          const uint64_t sc2 = f32x2(scale_log2, scale_log2), nm2 = f32x2(nm, nm);
           float lsum0 = 0.f, lsum1 = 0.f;
           uint32_t pk[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            uint64_t s2, x2;
-            asm("mov.b64 %0, {%1, %2};" : "=l"(s2) : "r"(r[2 * k]), "r"(r[2 * k + 1]));
-            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(x2) : "l"(s2), "l"(sc2), "l"(nm2));
-            float x0, x1;
-            asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(x2));
-            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            // masked scores are -inf and give 0
+            const float e0 = ex2_approx(fmaf(__uint_as_float(r[2 * k]), scale_log2, nm));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(r[2 * k + 1]), scale_log2, nm));
             lsum0 += e0;
             lsum1 += e1;
             pk[k] = pack2<BF16>(e0, e1);
