@@ -10,14 +10,16 @@
 // and writes O * attn_scale (softmax: / rowsum, plus LSE) or, with split-KV,
 // fp32 partials for the combine kernel.
 //
-// Roles (320 threads, one CTA per SM, all waits time-bounded):
+// Roles (448 threads, one CTA per SM, all waits time-bounded):
 //   warp 0       scheduler + TMA producer: fetches units from a global counter,
 //                loads Q once per unit and K and V tiles into separate rings
 //   warp 1       TMEM owner + MMA issuer (one thread)
-//   warps 2..9   elementwise groups: warpgroup g (warps 2+4g .. 5+4g) owns key
+//   warps 2..5   epilogue warpgroup, one query row per thread: reads a unit's O
+//                out of TMEM once its last P V product is done, hands the
+//                buffer back, scales (softmax: by 1/rowsum) and stores O / LSE
+//   warps 6..13  elementwise groups: warpgroup g (warps 6+4g .. 9+4g) owns key
 //                columns [64g, 64g+64) of every score row, one row per thread:
-//                TMEM S -> registers, mask + SiLU/softmax, P -> TMEM; then the
-//                epilogue writes its half of the O columns
+//                TMEM S -> registers, mask + SiLU/softmax, P -> TMEM
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores; the
 // 16-bit P of key columns [64g, 64g+64) is packed into S columns
@@ -50,25 +52,13 @@ struct FwdCfg {
   static constexpr int O_BUFS = D <= 128 ? 2 : 1;
 };
 
-constexpr int kFwdThreads = 320;
-constexpr int kEwThreads = 256;   // two elementwise warpgroups
+constexpr int kEpiWarps = 4;       // epilogue warpgroup
+constexpr int kEwThreads = 256;    // two elementwise warpgroups
+constexpr int kFwdThreads = 64 + 32 * kEpiWarps + kEwThreads;   // 448: 128 registers per thread
 constexpr int kSchedDepth = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
 
-struct FwdSmemCtl {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t o_full[2], o_empty[2];
-  uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
-  uint64_t xch[2];            // softmax row-max exchange between the warpgroups, per tile parity
-  uint64_t lxch;              // softmax row-sum exchange, per unit
-  float xmax[2][2][128];      // [tile parity][warpgroup][row]
-  float xl[2][128];           // [warpgroup][row]
-  int sched_unit[kSchedDepth];
-  uint32_t tmem_base;
-  volatile int abort_flag;
-};
+
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -93,30 +83,6 @@ __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   return r;
 }
 
-// SiLU of two raw scores a, b (fp32 bit patterns), scaled by alpha, as a packed
-// 16-bit pair (a in the low half).  `ha` holds alpha/2: for bf16 as a packed
-// pair (the raw scores are rounded to bf16 first, whose range is fp32's); for
-// fp16 as an fp32 bit pattern (the scale is applied in fp32 so large raw
-// scores cannot overflow fp16 before scaling).
-template <bool BF16>
-__device__ __forceinline__ uint32_t silu_pair(uint32_t a, uint32_t b, uint32_t ha) {
-  uint32_t hp, tp, pp;
-  if constexpr (BF16) {
-    uint32_t sp;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(sp) : "r"(b), "r"(a));
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hp) : "r"(sp), "r"(ha));
-    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(tp) : "r"(hp));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(pp) : "r"(hp), "r"(tp), "r"(hp));
-  } else {
-    const float h0 = __uint_as_float(a) * __uint_as_float(ha);
-    const float h1 = __uint_as_float(b) * __uint_as_float(ha);
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hp) : "f"(h1), "f"(h0));
-    asm("tanh.approx.f16x2 %0, %1;" : "=r"(tp) : "r"(hp));
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(pp) : "r"(hp), "r"(tp), "r"(hp));
-  }
-  return pp;
-}
-
 // Per-row mask in tile-local column terms: key column c (0..127) of the tile
 // is allowed iff c < ctx || (unsigned)(c - lo) < span || c == diag.
 struct RowMask {
@@ -132,6 +98,7 @@ struct UnitView {
   TileSet ts;
   TileBounds tb;
   int m, h, g, sp, k0, k1;
+  float scale;   // resolved attn_scale of the unit's group
 };
 
 __device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
@@ -147,8 +114,26 @@ __device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
   u.ts = query_tile_kv_tiles(u.s, u.m);
   u.tb = tile_uih_bounds(u.s, u.m * kBlockM, u.m * kBlockM + kBlockM);
   split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);
+  u.scale = p.group_scale[u.g];
   return u;
 }
+
+struct FwdSmemCtl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t o_full[2], o_empty[2];
+  uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
+  uint64_t xch[2];            // softmax row-max exchange between the warpgroups, per tile parity
+  uint64_t rs_full[2], rs_empty[2];   // softmax row statistics of O buffer ob: ready / consumed
+  float xmax[2][2][128];      // [tile parity][warpgroup][row]
+  float rs_m[2][128];         // [O buffer][row] running max (log2 units)
+  float rs_l[2][2][128];      // [O buffer][warpgroup][row] row sum over the warpgroup's columns
+  UnitView sched_view[kSchedDepth];   // decoded units published by the producer
+  int sched_live[kSchedDepth];        // 0: no more units
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
 
 // Bounded wait; on timeout flags the error word and asks every role to stop.
 __device__ __forceinline__ bool wait_or_abort(FwdSmemCtl& ctl, const FwdParams& p, uint64_t* bar,
@@ -172,22 +157,45 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
 }
 
 // SiLU of the 64 scores of key columns [c0, c0+64) of one row (fp32 bit
-// patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.
+// patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.  Each
+// 16-pair chunk runs stage by stage so the pairs' latencies overlap.
 template <bool BF16, bool MASKED>
-__device__ __forceinline__ void silu_half(uint32_t (&r)[64], uint32_t p_tmem, uint32_t ha2,
+__device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tmem, uint32_t ha,
                                           const RowMask& rm, int c0) {
-  uint32_t pk[32];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    uint32_t v = silu_pair<BF16>(r[2 * k], r[2 * k + 1], ha2);
-    if constexpr (MASKED) {
-      const uint32_t m = (rm.allowed(c0 + 2 * k) ? 0x0000FFFFu : 0u) |
-                         (rm.allowed(c0 + 2 * k + 1) ? 0xFFFF0000u : 0u);
-      v &= m;
+  for (int q = 0; q < 2; ++q) {
+    uint32_t h[16], t[16];
+    if constexpr (BF16) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "r"(r[32 * q + 2 * k + 1]), "r"(r[32 * q + 2 * k]));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) asm("fma.rn.bf16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
+    } else {
+      const float haf = __uint_as_float(ha);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float h0 = __uint_as_float(r[32 * q + 2 * k]) * haf;
+        const float h1 = __uint_as_float(r[32 * q + 2 * k + 1]) * haf;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "f"(h1), "f"(h0));
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) asm("tanh.approx.f16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) asm("fma.rn.f16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
     }
-    pk[k] = v;
+    if constexpr (MASKED) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        h[k] &= (rm.allowed(c0 + 32 * q + 2 * k) ? 0x0000FFFFu : 0u) |
+                (rm.allowed(c0 + 32 * q + 2 * k + 1) ? 0xFFFF0000u : 0u);
+    }
+    ptx::tmem_st16(p_tmem + 16 * q, h);
   }
-  ptx::tmem_st32(p_tmem, pk);
 }
 
 template <int D, bool BF16, bool SOFTMAX>
@@ -227,13 +235,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::mbar_init(&ctl.p_full[s], kEwThreads);
       ptx::mbar_init(&ctl.pv_done[s], 1);
       ptx::mbar_init(&ctl.o_full[s], 1);
-      ptx::mbar_init(&ctl.o_empty[s], kEwThreads);
+      ptx::mbar_init(&ctl.o_empty[s], 32 * kEpiWarps);
       ptx::mbar_init(&ctl.xch[s], kEwThreads);
+      ptx::mbar_init(&ctl.rs_full[s], kEwThreads);
+      ptx::mbar_init(&ctl.rs_empty[s], 32 * kEpiWarps);
     }
-    ptx::mbar_init(&ctl.lxch, kEwThreads);
     for (int s = 0; s < kSchedDepth; ++s) {
       ptx::mbar_init(&ctl.sched_full[s], 1);
-      ptx::mbar_init(&ctl.sched_empty[s], 1 + kEwThreads / 32);
+      ptx::mbar_init(&ctl.sched_empty[s], 1 + kEpiWarps + kEwThreads / 32);
     }
     ctl.abort_flag = 0;
     ptx::fence_barrier_init();
@@ -254,45 +263,85 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int q_it = 0, kv_it = 0, sched_it = 0;
-      while (!ctl.abort_flag) {
-        int unit = atomicAdd(&p.ws_header[kWsCounter], 1);
-        if (unit >= n_units) unit = -1;
-        const int slot = sched_it % kSchedDepth;
-        if (!wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((sched_it / kSchedDepth) & 1) ^ 1)) break;
-        ctl.sched_unit[slot] = unit;
-        ptx::mbar_arrive(&ctl.sched_full[slot]);
-        ++sched_it;
-        if (unit < 0) break;
-        const UnitView u = decode_unit(p, unit);
-        if (u.k1 <= u.k0) continue;
-        if (!wait_or_abort(ctl, p, &ctl.q_empty, (q_it & 1) ^ 1)) break;
-        ptx::mbar_arrive_expect_tx(&ctl.q_full, Cfg::TILE_BYTES);
-        const int qrow = u.s.q0 + u.m * kBlockM;
+      constexpr int PF = 4;   // K/V tiles prefetched into L2 ahead of the ring
+      auto prefetch_tile = [&](const UnitView& u, int k) {
+        const int krow = u.s.kv0 + tileset_at(u.ts, k) * kBlockN;
+#pragma unroll
+        for (int kc = 0; kc < KCH; ++kc) {
+          ptx::tma_prefetch_2d(&tm_k, u.h * D + kc * 64, krow);
+          ptx::tma_prefetch_2d(&tm_v, u.h * D + kc * 64, krow);
+        }
+      };
+      auto prefetch_unit = [&](const UnitView& u) {
+        if (u.k1 <= u.k0) return;
 #pragma unroll
         for (int kc = 0; kc < KCH; ++kc)
-          ptx::tma_load_2d(sQ + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full, u.h * D + kc * 64, qrow);
-        ++q_it;
+          ptx::tma_prefetch_2d(&tm_q, u.h * D + kc * 64, u.s.q0 + u.m * kBlockM);
+        for (int k = u.k0; k < u.k1 && k < u.k0 + PF; ++k) prefetch_tile(u, k);
+      };
+      int q_it = 0, kv_it = 0, sched_it = 0;
+      // Units are taken one ahead: the next unit's id is requested before the
+      // current unit's loads are issued, and it is decoded (and its first tiles
+      // prefetched into L2) while the current unit's K/V rings are full.
+      int cur_id = atomicAdd(&p.ws_header[kWsCounter], 1);
+      UnitView cur;
+      if (cur_id < n_units) {
+        cur = decode_unit(p, cur_id);
+        prefetch_unit(cur);
+      }
+      while (!ctl.abort_flag) {
+        const bool live = cur_id < n_units;
+        const int nxt_id = live ? atomicAdd(&p.ws_header[kWsCounter], 1) : n_units;
+        const int slot = sched_it % kSchedDepth;
+        if (!wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((sched_it / kSchedDepth) & 1) ^ 1)) break;
+        ctl.sched_view[slot] = cur;
+        ctl.sched_live[slot] = live ? 1 : 0;
+        ptx::mbar_arrive(&ctl.sched_full[slot]);
+        ++sched_it;
+        if (!live) break;
+        UnitView nxt;
+        bool have_nxt = false;
+        auto take_next = [&]() {
+          if (!have_nxt && nxt_id < n_units) {
+            nxt = decode_unit(p, nxt_id);
+            prefetch_unit(nxt);
+          }
+          have_nxt = true;
+        };
         bool ok = true;
-        for (int k = u.k0; k < u.k1 && ok; ++k) {
-          const int n = tileset_at(u.ts, k);
-          const int krow = u.s.kv0 + n * kBlockN;
-          const int ks = kv_it % KST, vs = kv_it % VST;
-          if (!wait_or_abort(ctl, p, &ctl.k_empty[ks], ((kv_it / KST) & 1) ^ 1)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&ctl.k_full[ks], Cfg::TILE_BYTES);
+        if (cur.k1 > cur.k0) {
+          if (!wait_or_abort(ctl, p, &ctl.q_empty, (q_it & 1) ^ 1)) break;
+          ptx::mbar_arrive_expect_tx(&ctl.q_full, Cfg::TILE_BYTES);
+          const int qrow = cur.s.q0 + cur.m * kBlockM;
 #pragma unroll
           for (int kc = 0; kc < KCH; ++kc)
-            ptx::tma_load_2d(sK + ks * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_k, &ctl.k_full[ks],
-                             u.h * D + kc * 64, krow);
-          if (!wait_or_abort(ctl, p, &ctl.v_empty[vs], ((kv_it / VST) & 1) ^ 1)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::TILE_BYTES);
+            ptx::tma_load_2d(sQ + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full, cur.h * D + kc * 64, qrow);
+          ++q_it;
+          for (int k = cur.k0; k < cur.k1 && ok; ++k) {
+            if (k == cur.k0 + 2) take_next();
+            if (k + PF < cur.k1) prefetch_tile(cur, k + PF);
+            const int n = tileset_at(cur.ts, k);
+            const int krow = cur.s.kv0 + n * kBlockN;
+            const int ks = kv_it % KST, vs = kv_it % VST;
+            if (!wait_or_abort(ctl, p, &ctl.k_empty[ks], ((kv_it / KST) & 1) ^ 1)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(&ctl.k_full[ks], Cfg::TILE_BYTES);
 #pragma unroll
-          for (int kc = 0; kc < KCH; ++kc)
-            ptx::tma_load_2d(sV + vs * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[vs],
-                             u.h * D + kc * 64, krow);
-          ++kv_it;
+            for (int kc = 0; kc < KCH; ++kc)
+              ptx::tma_load_2d(sK + ks * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_k, &ctl.k_full[ks],
+                               cur.h * D + kc * 64, krow);
+            if (!wait_or_abort(ctl, p, &ctl.v_empty[vs], ((kv_it / VST) & 1) ^ 1)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::TILE_BYTES);
+#pragma unroll
+            for (int kc = 0; kc < KCH; ++kc)
+              ptx::tma_load_2d(sV + vs * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[vs],
+                               cur.h * D + kc * 64, krow);
+            ++kv_it;
+          }
         }
         if (!ok) break;
+        take_next();
+        cur = nxt;
+        cur_id = nxt_id;
       }
     }
   } else if (warp == 1) {
@@ -325,11 +374,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       while (ok && !ctl.abort_flag) {
         const int slot = sched_it % kSchedDepth;
         if (!wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
-        const int unit = ctl.sched_unit[slot];
+        const bool live = ctl.sched_live[slot] != 0;
+        const UnitView u = ctl.sched_view[slot];
         ptx::mbar_arrive(&ctl.sched_empty[slot]);
         ++sched_it;
-        if (unit < 0) break;
-        const UnitView u = decode_unit(p, unit);
+        if (!live) break;
         const int nt = u.k1 - u.k0;
         if (nt <= 0) continue;
         const int ob = q_it % OB;
@@ -372,28 +421,113 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++q_it;
       }
     }
-  } else {
-    // ------------------------------------------------------------ elementwise + epilogue
-    const int wg = (warp - 2) >> 2;          // warpgroup: key columns [64 wg, 64 wg + 64)
-    const int quarter = warp & 3;            // TMEM lane quarter this warp may access
-    const int rloc = quarter * 32 + lane;    // row within the query tile
-    const int c0 = wg * 64;
-    constexpr int DH = D / 2;                // O columns per warpgroup
+  } else if (warp < 2 + kEpiWarps) {
+    // ------------------------------------------------------------ epilogue warpgroup
+    // One query row per thread, all D output columns: waits for the unit's last
+    // P V product, reads O out of TMEM, hands the buffer back, scales and stores.
+    const int quarter = warp & 3;
+    const int rloc = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    uint32_t ha2;   // alpha/2 in the form silu_pair takes
-    if constexpr (BF16) ha2 = pack2<true>(0.5f * p.alpha, 0.5f * p.alpha);
-    else ha2 = __float_as_uint(0.5f * p.alpha);
-    const float scale_log2 = p.alpha * 1.4426950408889634f;
-    int s_it = 0, q_it = 0, sched_it = 0, l_it = 0;
+    int q_it = 0, sched_it = 0;
     while (!ctl.abort_flag) {
       const int slot = sched_it % kSchedDepth;
       if (!warp_wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
-      const int unit = ctl.sched_unit[slot];
+      const bool live = ctl.sched_live[slot] != 0;
+      const UnitView u = ctl.sched_view[slot];
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ctl.sched_empty[slot]);
       ++sched_it;
-      if (unit < 0) break;
-      const UnitView u = decode_unit(p, unit);
+      if (!live) break;
+      const int nt = u.k1 - u.k0;
+      const int row = u.m * kBlockM + rloc;
+      const bool valid = row < u.s.Lq;
+      const long long grow = static_cast<long long>(u.s.q0) + row;   // global token row
+      const int ob = q_it % OB;
+      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * D;
+      float m_run = -INFINITY, l_run = 0.f;
+      if (nt > 0) {
+        if (!warp_wait_or_abort(ctl, p, &ctl.o_full[ob], (q_it / OB) & 1)) break;
+        if constexpr (SOFTMAX) {
+          if (!warp_wait_or_abort(ctl, p, &ctl.rs_full[ob], (q_it / OB) & 1)) break;
+          m_run = ctl.rs_m[ob][rloc];
+          l_run = ctl.rs_l[ob][0][rloc] + ctl.rs_l[ob][1][rloc];
+        }
+        ptx::tc_fence_after();
+      }
+      const bool write_part = p.splits > 1;
+      float mul = u.scale;
+      if constexpr (SOFTMAX) mul = l_run > 0.f ? u.scale / l_run : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (nt > 0) {
+          ptx::tmem_ld32(o_tmem + c * 32, o);
+          ptx::tmem_ld_wait(o);
+          if (c == D / 32 - 1) {   // all of O read: the buffer (and statistics) may be reused
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&ctl.o_empty[ob]);
+            if constexpr (SOFTMAX) ptx::mbar_arrive(&ctl.rs_empty[ob]);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = 0u;
+        }
+        if (!valid) continue;
+        if (write_part) {
+          float* dst = p.o_part + ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * D + c * 32;
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2)
+            pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * D + c * 32;
+#pragma unroll
+          for (int k = 0; k < 16; k += 4)
+            *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
+        }
+      }
+      if (nt > 0) ++q_it;
+      if (valid) {
+        if (write_part) {
+          if constexpr (SOFTMAX) {
+            float* ml = p.ml_part + ((static_cast<long long>(u.sp) * p.nhead + u.h) * p.total_q + grow) * 2;
+            ml[0] = m_run;
+            ml[1] = l_run;
+          }
+        } else if (SOFTMAX && p.lse != nullptr) {
+          p.lse[static_cast<long long>(u.h) * p.total_q + grow] =
+              l_run > 0.f ? m_run * 0.6931471805599453f + logf(l_run) : -INFINITY;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise warpgroups
+    const int wg = (warp - 2 - kEpiWarps) >> 2;   // warpgroup: key columns [64 wg, 64 wg + 64)
+    const int quarter = warp & 3;            // TMEM lane quarter this warp may access
+    const int rloc = quarter * 32 + lane;    // row within the query tile
+    const int c0 = wg * 64;
+    constexpr int DH = D / 2;                // O columns this warpgroup rescales (softmax)
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    // alpha/2: a packed bf16 pair (the raw scores are rounded to bf16, whose
+    // range is fp32's, before scaling) or an fp32 bit pattern for fp16 (scaled
+    // in fp32 first so large raw scores cannot overflow fp16)
+    uint32_t ha2;
+    if constexpr (BF16) ha2 = pack2<true>(0.5f * p.alpha, 0.5f * p.alpha);
+    else ha2 = __float_as_uint(0.5f * p.alpha);
+    const float scale_log2 = p.alpha * 1.4426950408889634f;
+    int s_it = 0, q_it = 0, sched_it = 0;
+    while (!ctl.abort_flag) {
+      const int slot = sched_it % kSchedDepth;
+      if (!warp_wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
+      const bool live = ctl.sched_live[slot] != 0;
+      const UnitView u = ctl.sched_view[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ctl.sched_empty[slot]);
+      ++sched_it;
+      if (!live) break;
       const int nt = u.k1 - u.k0;
       const int row = u.m * kBlockM + rloc;
       const bool valid = row < u.s.Lq;
@@ -402,8 +536,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int r_diag = row_diag_key(u.s, row);
       int r_ctx = u.s.c;
       if (!valid) { r_lo = r_hi = 0; r_diag = -1; r_ctx = 0; }
-      const float attn_scale = p.group_scale[u.g];
-      const long long grow = static_cast<long long>(u.s.q0) + row;   // global token row
       const int ob = q_it % OB;
       const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * D + wg * DH;
 
@@ -475,11 +607,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const float nm = m_run == -INFINITY ? 0.f : -m_run;
           float lsum0 = 0.f, lsum1 = 0.f;
           uint32_t pk[32];
+          // stage by stage so the exponentials of the 64 scores overlap
+#pragma unroll
+          for (int k = 0; k < 64; ++k)   // masked scores are -inf and give 0
+            r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), scale_log2, nm));
+#pragma unroll
+          for (int k = 0; k < 64; ++k) r[k] = __float_as_uint(ex2_approx(__uint_as_float(r[k])));
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            // masked scores are -inf and give 0
-            const float e0 = ex2_approx(fmaf(__uint_as_float(r[2 * k]), scale_log2, nm));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(r[2 * k + 1]), scale_log2, nm));
+            const float e0 = __uint_as_float(r[2 * k]), e1 = __uint_as_float(r[2 * k + 1]);
             lsum0 += e0;
             lsum1 += e1;
             pk[k] = pack2<BF16>(e0, e1);
@@ -493,69 +629,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (!ok) break;
 
-      // ---------------------------------------------------------- epilogue
-      if (nt > 0) {
-        if (!warp_wait_or_abort(ctl, p, &ctl.o_full[ob], (q_it / OB) & 1)) break;
-        ptx::tc_fence_after();
-      }
       if constexpr (SOFTMAX) {
-        if (nt > 0) {   // full row sum = both warpgroups' column sums
-          ctl.xl[wg][rloc] = l_run;
-          ptx::mbar_arrive(&ctl.lxch);
-          if (!warp_wait_or_abort(ctl, p, &ctl.lxch, l_it & 1)) break;
-          l_run += ctl.xl[wg ^ 1][rloc];
-          ++l_it;
-        }
-      }
-      const bool write_part = p.splits > 1;
-      float mul = attn_scale;
-      if constexpr (SOFTMAX) mul = l_run > 0.f ? attn_scale / l_run : 0.f;
-#pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
-        uint32_t o[32];
+        // hand this unit's row statistics to the epilogue warpgroup
         if (nt > 0) {
-          ptx::tmem_ld32(o_tmem + c * 32, o);
-          ptx::tmem_ld_wait(o);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0u;
-        }
-        if (!valid) continue;
-        const int col = wg * DH + c * 32;
-        if (write_part) {
-          float* dst = p.o_part +
-                       ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * D + col;
-#pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-        } else {
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 32; k += 2)
-            pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
-          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * D + col;
-#pragma unroll
-          for (int k = 0; k < 16; k += 4)
-            *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
+          if (!warp_wait_or_abort(ctl, p, &ctl.rs_empty[ob], ((q_it / OB) & 1) ^ 1)) break;
+          if (wg == 0) ctl.rs_m[ob][rloc] = m_run;
+          ctl.rs_l[ob][wg][rloc] = l_run;
+          ptx::mbar_arrive(&ctl.rs_full[ob]);
         }
       }
-      if (nt > 0) {
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.o_empty[ob]);
-        ++q_it;
-      }
-      if (valid && wg == 0) {
-        if (write_part) {
-          if constexpr (SOFTMAX) {
-            float* ml = p.ml_part + ((static_cast<long long>(u.sp) * p.nhead + u.h) * p.total_q + grow) * 2;
-            ml[0] = m_run;
-            ml[1] = l_run;
-          }
-        } else if (SOFTMAX && p.lse != nullptr) {
-          p.lse[static_cast<long long>(u.h) * p.total_q + grow] =
-              l_run > 0.f ? m_run * 0.6931471805599453f + logf(l_run) : -INFINITY;
-        }
-      }
+      if (nt > 0) ++q_it;
       s_it += nt;
     }
   }

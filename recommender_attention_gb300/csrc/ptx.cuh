@@ -86,6 +86,13 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* map, uin
       : "memory");
 }
 
+// Prefetch of a 2-D tile (same box as the tensor map) into L2; no completion.
+__device__ __forceinline__ void tma_prefetch_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x),
+               "r"(y)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
