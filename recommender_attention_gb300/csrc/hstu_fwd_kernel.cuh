@@ -10,9 +10,9 @@
 // and writes O * attn_scale (softmax: / rowsum, plus LSE) or, with split-KV,
 // fp32 partials for the combine kernel.
 //
-// Roles (448 threads, one CTA per SM, all waits time-bounded):
-//   warp 0       scheduler + TMA producer: fetches units from a global counter,
-//                loads Q once per unit and K and V tiles into separate rings
+// Roles (480 threads, one CTA per SM, all waits time-bounded):
+//   warp 0       TMA producer: loads Q once per unit and K and V tiles into
+//                separate rings, prefetching upcoming tiles into L2
 //   warp 1       TMEM owner + MMA issuer (one thread)
 //   warps 2..5   epilogue warpgroup, one query row per thread: reads a unit's O
 //                out of TMEM once its last P V product is done, hands the
@@ -20,6 +20,8 @@
 //   warps 6..13  elementwise groups: warpgroup g (warps 6+4g .. 9+4g) owns key
 //                columns [64g, 64g+64) of every score row, one row per thread:
 //                TMEM S -> registers, mask + SiLU/softmax, P -> TMEM
+//   warp 14      scheduler: takes units from the global queue, decodes them and
+//                publishes them to the other roles through a shared-memory ring
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores; the
 // 16-bit P of key columns [64g, 64g+64) is packed into S columns
@@ -54,7 +56,8 @@ struct FwdCfg {
 
 constexpr int kEpiWarps = 4;       // epilogue warpgroup
 constexpr int kEwThreads = 256;    // two elementwise warpgroups
-constexpr int kFwdThreads = 64 + 32 * kEpiWarps + kEwThreads;   // 448: 128 registers per thread
+constexpr int kFwdThreads = 64 + 32 * kEpiWarps + kEwThreads + 32;   // 480: 128 registers per thread
+constexpr int kSchedWarp = kFwdThreads / 32 - 1;   // the last warp
 constexpr int kSchedDepth = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
 
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int s = 0; s < kSchedDepth; ++s) {
       ptx::mbar_init(&ctl.sched_full[s], 1);
-      ptx::mbar_init(&ctl.sched_empty[s], 1 + kEpiWarps + kEwThreads / 32);
+      ptx::mbar_init(&ctl.sched_empty[s], 2 + kEpiWarps + kEwThreads / 32);   // producer, MMA, epilogue, elementwise
     }
     ctl.abort_flag = 0;
     ptx::fence_barrier_init();
@@ -280,33 +283,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int k = u.k0; k < u.k1 && k < u.k0 + PF; ++k) prefetch_tile(u, k);
       };
       int q_it = 0, kv_it = 0, sched_it = 0;
-      // Units are taken one ahead: the next unit's id is requested before the
-      // current unit's loads are issued, and it is decoded (and its first tiles
-      // prefetched into L2) while the current unit's K/V rings are full.
-      int cur_id = atomicAdd(&p.ws_header[kWsCounter], 1);
-      UnitView cur;
-      if (cur_id < n_units) {
-        cur = decode_unit(p, cur_id);
-        prefetch_unit(cur);
-      }
-      while (!ctl.abort_flag) {
-        const bool live = cur_id < n_units;
-        const int nxt_id = live ? atomicAdd(&p.ws_header[kWsCounter], 1) : n_units;
+      // reads the next published unit from the scheduler ring
+      auto take = [&](UnitView& u) -> int {   // 1 live, 0 end, -1 abort
         const int slot = sched_it % kSchedDepth;
-        if (!wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((sched_it / kSchedDepth) & 1) ^ 1)) break;
-        ctl.sched_view[slot] = cur;
-        ctl.sched_live[slot] = live ? 1 : 0;
-        ptx::mbar_arrive(&ctl.sched_full[slot]);
+        if (!wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) return -1;
+        const int live = ctl.sched_live[slot];
+        u = ctl.sched_view[slot];
+        ptx::mbar_arrive(&ctl.sched_empty[slot]);
         ++sched_it;
-        if (!live) break;
-        UnitView nxt;
+        return live;
+      };
+      UnitView cur, nxt;
+      int cur_live = take(cur);
+      if (cur_live > 0) prefetch_unit(cur);
+      while (cur_live > 0 && !ctl.abort_flag) {
+        int nxt_live = 0;
         bool have_nxt = false;
-        auto take_next = [&]() {
-          if (!have_nxt && nxt_id < n_units) {
-            nxt = decode_unit(p, nxt_id);
-            prefetch_unit(nxt);
-          }
+        // the next unit is read (and its first tiles prefetched into L2) about
+        // three tiles before this unit's last loads
+        auto look_ahead = [&]() -> bool {
+          if (have_nxt) return true;
           have_nxt = true;
+          nxt_live = take(nxt);
+          if (nxt_live < 0) return false;
+          if (nxt_live > 0) prefetch_unit(nxt);
+          return true;
         };
         bool ok = true;
         if (cur.k1 > cur.k0) {
@@ -317,8 +318,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int kc = 0; kc < KCH; ++kc)
             ptx::tma_load_2d(sQ + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full, cur.h * D + kc * 64, qrow);
           ++q_it;
+          const int k_ahead = cur.k1 - 3 > cur.k0 ? cur.k1 - 3 : cur.k0;
           for (int k = cur.k0; k < cur.k1 && ok; ++k) {
-            if (k == cur.k0 + 2) take_next();
+            if (k == k_ahead && !look_ahead()) { ok = false; break; }
             if (k + PF < cur.k1) prefetch_tile(cur, k + PF);
             const int n = tileset_at(cur.ts, k);
             const int krow = cur.s.kv0 + n * kBlockN;
@@ -338,10 +340,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ++kv_it;
           }
         }
-        if (!ok) break;
-        take_next();
+        if (!ok || !look_ahead()) break;
         cur = nxt;
-        cur_id = nxt_id;
+        cur_live = nxt_live;
+      }
+    }
+  } else if (warp == kSchedWarp) {
+    // ------------------------------------------------------------ scheduler
+    // Takes units from the global queue and decodes them (global memory reads)
+    // up to kSchedDepth units ahead of the other roles.
+    if (lane == 0) {
+      int sched_it = 0;
+      while (!ctl.abort_flag) {
+        const int id = atomicAdd(&p.ws_header[kWsCounter], 1);
+        const bool live = id < n_units;
+        UnitView u;
+        if (live) u = decode_unit(p, id);
+        const int slot = sched_it % kSchedDepth;
+        if (!wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((sched_it / kSchedDepth) & 1) ^ 1)) break;
+        if (live) ctl.sched_view[slot] = u;
+        ctl.sched_live[slot] = live ? 1 : 0;
+        ptx::mbar_arrive(&ctl.sched_full[slot]);
+        ++sched_it;
+        if (!live) break;
       }
     }
   } else if (warp == 1) {
@@ -354,18 +375,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t v_base = ptx::smem_u32(sV);
       int q_it = 0, kv_it = 0, s_it = 0, sched_it = 0;
       bool ok = true;
+      // The K-major operands of Q K^T advance by 32 bytes per 16-element step
+      // inside a 128-byte swizzle row and by one 128-row chunk every 4 steps;
+      // the descriptors are the stage's base plus that offset (16-byte units).
+      const uint64_t q_desc = ptx::sdesc_sw128(q_base, 16, 1024);
       // S = Q K^T for the tile held in K stage (kvi % KST), into S buffer (si & 1).
       auto issue_qk = [&](int kvi, int si) -> bool {
         const int st = kvi % KST;
         if (!wait_or_abort(ctl, p, &ctl.k_full[st], (kvi / KST) & 1)) return false;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + (si & 1) * 128;
+        const uint64_t k_desc = ptx::sdesc_sw128(k_base + st * Cfg::TILE_BYTES, 16, 1024);
+        constexpr int G = D / 16 >= 8 ? 8 : 4;   // k-steps per asm block
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * Cfg::CHUNK_BYTES + (ks & 3) * 32;
-          const uint64_t ad = ptx::sdesc_sw128(q_base + off, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(k_base + st * Cfg::TILE_BYTES + off, 16, 1024);
-          ptx::umma_ss(d_tmem, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+        for (int g = 0; g < D / 16; g += G) {
+          uint64_t ad[G], bd[G];
+#pragma unroll
+          for (int j = 0; j < G; ++j) {
+            const int ks = g + j;
+            const uint64_t off = static_cast<uint64_t>(((ks >> 2) * Cfg::CHUNK_BYTES + (ks & 3) * 32) >> 4);
+            ad[j] = q_desc + off;
+            bd[j] = k_desc + off;
+          }
+          if constexpr (G == 8) ptx::umma_ss_x8(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
+          else ptx::umma_ss_x4(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
         }
         ptx::umma_commit(&ctl.k_empty[st]);
         ptx::umma_commit(&ctl.s_full[si & 1]);
@@ -403,14 +436,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int st = kvi % VST;
           if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
+          // P: key columns [64 g, 64 g + 64) packed at S columns [64 g, 64 g + 32);
+          // V (MN-major) advances 16 rows = 2048 bytes per step
           const uint32_t p_tmem = tmem + (si & 1) * 128;
+          const uint64_t v_desc = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES, Cfg::CHUNK_BYTES, 1024);
+          uint32_t pa[8];
+          uint64_t vd[8];
 #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            const uint64_t bd = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES + kk * 2048,
-                                                 Cfg::CHUNK_BYTES, 1024);
-            ptx::umma_ts(o_tmem, p_tmem + (kk >> 2) * 64 + (kk & 3) * 8, bd, idesc_pv,
-                         (idx > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            pa[kk] = p_tmem + (kk >> 2) * 64 + (kk & 3) * 8;
+            vd[kk] = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
           }
+          ptx::umma_ts_x8(o_tmem, pa, vd, idesc_pv, idx > 0 ? 1u : 0u);
           ptx::umma_commit(&ctl.v_empty[st]);
           if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
         }
@@ -503,7 +540,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < kSchedWarp) {
     // ------------------------------------------------------------ elementwise warpgroups
     const int wg = (warp - 2 - kEpiWarps) >> 2;   // warpgroup: key columns [64 wg, 64 wg + 64)
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access

@@ -132,6 +132,59 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Eight kind::f16 MMAs into one accumulator from a single thread, in one asm
+// block (the first one overwrites D unless `accumulate`, the rest add).
+// a[k] / b[k] are the eight A / B shared-memory descriptors.
+__device__ __forceinline__ void umma_ss_x8(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, Q;\n\tsetp.ne.b32 P, %18, 0;\n\tsetp.eq.b32 Q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, P;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, Q;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Four kind::f16 MMAs (A and B in shared memory) in one asm block.
+__device__ __forceinline__ void umma_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, Q;\n\tsetp.ne.b32 P, %10, 0;\n\tsetp.eq.b32 Q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, P;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, Q;\n\t"
+      "}\n" ::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Eight MMAs with A in TMEM (columns a[k]) and B in shared memory (descriptors b[k]).
+__device__ __forceinline__ void umma_ts_x8(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, Q;\n\tsetp.ne.b32 P, %18, 0;\n\tsetp.eq.b32 Q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, P;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, Q;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
