@@ -41,14 +41,25 @@
 
 namespace hstu {
 
-template <int D>
+// Softmax-only exchange buffers (after the tiles in dynamic shared memory).
+struct SoftmaxScratch {
+  float xmax[2][2][128];      // [tile parity][warpgroup][row] row-max exchange
+  float rs_m[2][128];         // [O buffer][row] running max (log2 units)
+  float rs_l[2][2][128];      // [O buffer][warpgroup][row] row sum over the warpgroup's columns
+};
+
+template <int D, bool SOFTMAX>
 struct FwdCfg {
   static constexpr int KCH = D / 64;                  // 128-byte column chunks per row
   static constexpr int TILE_BYTES = kBlockN * D * 2;  // one Q, K or V tile
   static constexpr int CHUNK_BYTES = kBlockN * 128;   // one 128-row x 128-byte TMA box
-  static constexpr int KSTAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);   // K ring depth
-  static constexpr int VSTAGES = D == 64 ? 4 : (D == 128 ? 2 : 1);   // V ring depth
-  static constexpr int SMEM_BYTES = (1 + KSTAGES + VSTAGES) * TILE_BYTES + 1024;
+  // Q is double-buffered where it fits so the next unit's Q streams in early.
+  static constexpr int QBUF = D <= 128 ? 2 : 1;
+  static constexpr int KSTAGES = D == 64 ? 4 : (D == 128 ? (SOFTMAX ? 2 : 3) : 1);   // K ring depth
+  static constexpr int VSTAGES = D == 64 ? 4 : (D == 128 ? 2 : 1);                   // V ring depth
+  static constexpr int TILES_BYTES = (QBUF + KSTAGES + VSTAGES) * TILE_BYTES;
+  static constexpr int SMEM_BYTES =
+      TILES_BYTES + (SOFTMAX ? static_cast<int>(sizeof(SoftmaxScratch)) : 0) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
   static constexpr int O_BUFS = D <= 128 ? 2 : 1;
@@ -58,7 +69,8 @@ constexpr int kEpiWarps = 4;       // epilogue warpgroup
 constexpr int kEwThreads = 256;    // two elementwise warpgroups
 constexpr int kFwdThreads = 64 + 32 * kEpiWarps + kEwThreads + 32;   // 480: 128 registers per thread
 constexpr int kSchedWarp = kFwdThreads / 32 - 1;   // the last warp
-constexpr int kSchedDepth = 4;
+constexpr int kSchedDepth = 2;   // published-unit ring (deeper claims ahead hurt the tail balance)
+constexpr int kSchedBatch = 1;   // units taken from the global queue per atomic
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
 
 
@@ -122,16 +134,13 @@ __device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
 }
 
 struct FwdSmemCtl {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_full[2], o_empty[2];
   uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
   uint64_t xch[2];            // softmax row-max exchange between the warpgroups, per tile parity
   uint64_t rs_full[2], rs_empty[2];   // softmax row statistics of O buffer ob: ready / consumed
-  float xmax[2][2][128];      // [tile parity][warpgroup][row]
-  float rs_m[2][128];         // [O buffer][row] running max (log2 units)
-  float rs_l[2][2][128];      // [O buffer][warpgroup][row] row sum over the warpgroup's columns
   UnitView sched_view[kSchedDepth];   // decoded units published by the producer
   int sched_live[kSchedDepth];        // 0: no more units
   uint32_t tmem_base;
@@ -205,7 +214,7 @@ template <int D, bool BF16, bool SOFTMAX>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
-  using Cfg = FwdCfg<D>;
+  using Cfg = FwdCfg<D, SOFTMAX>;
   constexpr int KCH = Cfg::KCH;
   constexpr int KST = Cfg::KSTAGES;
   constexpr int VST = Cfg::VSTAGES;
@@ -214,17 +223,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __shared__ FwdSmemCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  constexpr int QB = Cfg::QBUF;
   uint8_t* sQ = smem;
-  uint8_t* sK = smem + Cfg::TILE_BYTES;
+  uint8_t* sK = smem + QB * Cfg::TILE_BYTES;
   uint8_t* sV = sK + KST * Cfg::TILE_BYTES;
+  SoftmaxScratch* sx = reinterpret_cast<SoftmaxScratch*>(smem + Cfg::TILES_BYTES);   // softmax only
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
   if (tid == 0) {
-    ptx::mbar_init(&ctl.q_full, 1);
-    ptx::mbar_init(&ctl.q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&ctl.q_full[s], 1);
+      ptx::mbar_init(&ctl.q_empty[s], 1);
+    }
     for (int s = 0; s < KST; ++s) {
       ptx::mbar_init(&ctl.k_full[s], 1);
       ptx::mbar_init(&ctl.k_empty[s], 1);
@@ -311,12 +324,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         };
         bool ok = true;
         if (cur.k1 > cur.k0) {
-          if (!wait_or_abort(ctl, p, &ctl.q_empty, (q_it & 1) ^ 1)) break;
-          ptx::mbar_arrive_expect_tx(&ctl.q_full, Cfg::TILE_BYTES);
+          const int qb = q_it % QB;
+          if (!wait_or_abort(ctl, p, &ctl.q_empty[qb], ((q_it / QB) & 1) ^ 1)) break;
+          ptx::mbar_arrive_expect_tx(&ctl.q_full[qb], Cfg::TILE_BYTES);
           const int qrow = cur.s.q0 + cur.m * kBlockM;
 #pragma unroll
           for (int kc = 0; kc < KCH; ++kc)
-            ptx::tma_load_2d(sQ + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full, cur.h * D + kc * 64, qrow);
+            ptx::tma_load_2d(sQ + qb * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full[qb],
+                             cur.h * D + kc * 64, qrow);
           ++q_it;
           const int k_ahead = cur.k1 - 3 > cur.k0 ? cur.k1 - 3 : cur.k0;
           for (int k = cur.k0; k < cur.k1 && ok; ++k) {
@@ -347,23 +362,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
-    // Takes units from the global queue and decodes them (global memory reads)
-    // up to kSchedDepth units ahead of the other roles.
-    if (lane == 0) {
-      int sched_it = 0;
-      while (!ctl.abort_flag) {
-        const int id = atomicAdd(&p.ws_header[kWsCounter], 1);
+    // Takes kSchedBatch units per atomic from the global queue; lanes
+    // 0..kSchedBatch-1 decode one each (their global reads overlap) and publish
+    // it into its own ring slot, running up to kSchedDepth units ahead.
+    int sched_it = 0;
+    while (!ctl.abort_flag) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&p.ws_header[kWsCounter], kSchedBatch);
+      base = __shfl_sync(0xffffffffu, base, 0);
+      bool ok = true, more = true;
+      if (lane < kSchedBatch) {
+        const int id = base + lane;
         const bool live = id < n_units;
         UnitView u;
         if (live) u = decode_unit(p, id);
-        const int slot = sched_it % kSchedDepth;
-        if (!wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((sched_it / kSchedDepth) & 1) ^ 1)) break;
-        if (live) ctl.sched_view[slot] = u;
-        ctl.sched_live[slot] = live ? 1 : 0;
-        ptx::mbar_arrive(&ctl.sched_full[slot]);
-        ++sched_it;
-        if (!live) break;
+        const int it = sched_it + lane;
+        const int slot = it % kSchedDepth;
+        ok = wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((it / kSchedDepth) & 1) ^ 1);
+        if (ok) {
+          if (live) ctl.sched_view[slot] = u;
+          ctl.sched_live[slot] = live ? 1 : 0;
+          ptx::mbar_arrive(&ctl.sched_full[slot]);
+        }
+        more = live;
       }
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!__all_sync(0xffffffffu, more)) break;   // the queue is drained: end markers published
+      sched_it += kSchedBatch;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -380,7 +405,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // the descriptors are the stage's base plus that offset (16-byte units).
       const uint64_t q_desc = ptx::sdesc_sw128(q_base, 16, 1024);
       // S = Q K^T for the tile held in K stage (kvi % KST), into S buffer (si & 1).
-      auto issue_qk = [&](int kvi, int si) -> bool {
+      auto issue_qk = [&](int kvi, int si, int qb) -> bool {
         const int st = kvi % KST;
         if (!wait_or_abort(ctl, p, &ctl.k_full[st], (kvi / KST) & 1)) return false;
         ptx::tc_fence_after();
@@ -394,7 +419,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int j = 0; j < G; ++j) {
             const int ks = g + j;
             const uint64_t off = static_cast<uint64_t>(((ks >> 2) * Cfg::CHUNK_BYTES + (ks & 3) * 32) >> 4);
-            ad[j] = q_desc + off;
+            ad[j] = q_desc + static_cast<uint64_t>((qb * Cfg::TILE_BYTES) >> 4) + off;
             bd[j] = k_desc + off;
           }
           if constexpr (G == 8) ptx::umma_ss_x8(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
@@ -416,14 +441,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (nt <= 0) continue;
         const int ob = q_it % OB;
         const uint32_t o_tmem = tmem + Cfg::O_COL + ob * D;
-        if (!wait_or_abort(ctl, p, &ctl.q_full, q_it & 1)) break;
+        const int qb = q_it % QB;
+        if (!wait_or_abort(ctl, p, &ctl.q_full[qb], (q_it / QB) & 1)) break;
         ptx::tc_fence_after();
-        if (!issue_qk(kv_it, s_it)) break;
+        if (!issue_qk(kv_it, s_it, qb)) break;
         for (int idx = 0; idx < nt; ++idx) {
           if (idx + 1 < nt) {
-            if (!issue_qk(kv_it + idx + 1, s_it + idx + 1)) { ok = false; break; }
+            if (!issue_qk(kv_it + idx + 1, s_it + idx + 1, qb)) { ok = false; break; }
           } else {
-            ptx::umma_commit(&ctl.q_empty);   // every QK of this unit is issued
+            ptx::umma_commit(&ctl.q_empty[qb]);   // every QK of this unit is issued
           }
           const int si = s_it + idx;
           if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) { ok = false; break; }
@@ -486,8 +512,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!warp_wait_or_abort(ctl, p, &ctl.o_full[ob], (q_it / OB) & 1)) break;
         if constexpr (SOFTMAX) {
           if (!warp_wait_or_abort(ctl, p, &ctl.rs_full[ob], (q_it / OB) & 1)) break;
-          m_run = ctl.rs_m[ob][rloc];
-          l_run = ctl.rs_l[ob][0][rloc] + ctl.rs_l[ob][1][rloc];
+          m_run = sx->rs_m[ob][rloc];
+          l_run = sx->rs_l[ob][0][rloc] + sx->rs_l[ob][1][rloc];
         }
         ptx::tc_fence_after();
       }
@@ -610,10 +636,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
           }
           // row max over both halves
-          ctl.xmax[si & 1][wg][rloc] = mx;
+          sx->xmax[si & 1][wg][rloc] = mx;
           ptx::mbar_arrive(&ctl.xch[si & 1]);
           if (!warp_wait_or_abort(ctl, p, &ctl.xch[si & 1], (si >> 1) & 1)) { ok = false; break; }
-          mx = fmaxf(mx, ctl.xmax[si & 1][wg ^ 1][rloc]) * scale_log2;
+          mx = fmaxf(mx, sx->xmax[si & 1][wg ^ 1][rloc]) * scale_log2;
           // PV of the tile before last must be complete before this tile; keeps the
           // parity tracking of pv_done unambiguous.
           if (si >= 2) {
@@ -670,8 +696,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // hand this unit's row statistics to the epilogue warpgroup
         if (nt > 0) {
           if (!warp_wait_or_abort(ctl, p, &ctl.rs_empty[ob], ((q_it / OB) & 1) ^ 1)) break;
-          if (wg == 0) ctl.rs_m[ob][rloc] = m_run;
-          ctl.rs_l[ob][wg][rloc] = l_run;
+          if (wg == 0) sx->rs_m[ob][rloc] = m_run;
+          sx->rs_l[ob][wg][rloc] = l_run;
           ptx::mbar_arrive(&ctl.rs_full[ob]);
         }
       }
