@@ -10,9 +10,10 @@
 // and writes O * attn_scale (softmax: / rowsum, plus LSE) or, with split-KV,
 // fp32 partials for the combine kernel.
 //
-// Roles (480 threads, one CTA per SM, all waits time-bounded):
-//   warp 0       TMA producer: loads Q once per unit and K and V tiles into
-//                separate rings, prefetching upcoming tiles into L2
+// Roles (512 threads, one CTA per SM, all waits time-bounded):
+//   warp 0       Q/K producer: TMA loads of Q once per unit and of K tiles into
+//                their ring, prefetching upcoming K/V tiles into L2
+//   warp 15      V producer: TMA loads of V tiles into their own ring
 //   warp 1       TMEM owner + MMA issuer (one thread)
 //   warps 2..5   epilogue warpgroup, one query row per thread: reads a unit's O
 //                out of TMEM once its last P V product is done, hands the
@@ -63,12 +64,14 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
   static constexpr int O_BUFS = D <= 128 ? 2 : 1;
+  static_assert(O_COL + O_BUFS * D <= TMEM_COLS, "TMEM budget");
 };
 
 constexpr int kEpiWarps = 4;       // epilogue warpgroup
 constexpr int kEwThreads = 256;    // two elementwise warpgroups
-constexpr int kFwdThreads = 64 + 32 * kEpiWarps + kEwThreads + 32;   // 480: 128 registers per thread
-constexpr int kSchedWarp = kFwdThreads / 32 - 1;   // the last warp
+constexpr int kFwdThreads = 64 + 32 * kEpiWarps + kEwThreads + 64;   // 512: 128 registers per thread
+constexpr int kSchedWarp = kFwdThreads / 32 - 2;
+constexpr int kVProdWarp = kFwdThreads / 32 - 1;
 constexpr int kSchedDepth = 2;   // published-unit ring (deeper claims ahead hurt the tail balance)
 constexpr int kSchedBatch = 1;   // units taken from the global queue per atomic
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
@@ -258,7 +261,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int s = 0; s < kSchedDepth; ++s) {
       ptx::mbar_init(&ctl.sched_full[s], 1);
-      ptx::mbar_init(&ctl.sched_empty[s], 2 + kEpiWarps + kEwThreads / 32);   // producer, MMA, epilogue, elementwise
+      // Q/K producer, V producer, MMA, epilogue and elementwise warps
+      ptx::mbar_init(&ctl.sched_empty[s], 3 + kEpiWarps + kEwThreads / 32);
     }
     ctl.abort_flag = 0;
     ptx::fence_barrier_init();
@@ -339,18 +343,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (k + PF < cur.k1) prefetch_tile(cur, k + PF);
             const int n = tileset_at(cur.ts, k);
             const int krow = cur.s.kv0 + n * kBlockN;
-            const int ks = kv_it % KST, vs = kv_it % VST;
+            const int ks = kv_it % KST;
             if (!wait_or_abort(ctl, p, &ctl.k_empty[ks], ((kv_it / KST) & 1) ^ 1)) { ok = false; break; }
             ptx::mbar_arrive_expect_tx(&ctl.k_full[ks], Cfg::TILE_BYTES);
 #pragma unroll
             for (int kc = 0; kc < KCH; ++kc)
               ptx::tma_load_2d(sK + ks * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_k, &ctl.k_full[ks],
-                               cur.h * D + kc * 64, krow);
-            if (!wait_or_abort(ctl, p, &ctl.v_empty[vs], ((kv_it / VST) & 1) ^ 1)) { ok = false; break; }
-            ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::TILE_BYTES);
-#pragma unroll
-            for (int kc = 0; kc < KCH; ++kc)
-              ptx::tma_load_2d(sV + vs * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[vs],
                                cur.h * D + kc * 64, krow);
             ++kv_it;
           }
@@ -358,6 +356,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!ok || !look_ahead()) break;
         cur = nxt;
         cur_live = nxt_live;
+      }
+    }
+  } else if (warp == kVProdWarp) {
+    // ------------------------------------------------------------ V producer
+    // Streams V tiles into their ring independently of the K ring, so that a
+    // K tile never waits behind a V slot (and vice versa).
+    if (lane == 0) {
+      int kv_it = 0, sched_it = 0;
+      while (!ctl.abort_flag) {
+        const int slot = sched_it % kSchedDepth;
+        if (!wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
+        const bool live = ctl.sched_live[slot] != 0;
+        const UnitView u = ctl.sched_view[slot];
+        ptx::mbar_arrive(&ctl.sched_empty[slot]);
+        ++sched_it;
+        if (!live) break;
+        bool ok = true;
+        for (int k = u.k0; k < u.k1; ++k) {
+          const int vs = kv_it % VST;
+          const int vrow = u.s.kv0 + tileset_at(u.ts, k) * kBlockN;
+          if (!wait_or_abort(ctl, p, &ctl.v_empty[vs], ((kv_it / VST) & 1) ^ 1)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::TILE_BYTES);
+#pragma unroll
+          for (int kc = 0; kc < KCH; ++kc)
+            ptx::tma_load_2d(sV + vs * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[vs],
+                             u.h * D + kc * 64, vrow);
+          ++kv_it;
+        }
+        if (!ok) break;
       }
     }
   } else if (warp == kSchedWarp) {
@@ -444,38 +471,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int qb = q_it % QB;
         if (!wait_or_abort(ctl, p, &ctl.q_full[qb], (q_it / QB) & 1)) break;
         ptx::tc_fence_after();
-        if (!issue_qk(kv_it, s_it, qb)) break;
-        for (int idx = 0; idx < nt; ++idx) {
-          if (idx + 1 < nt) {
-            if (!issue_qk(kv_it + idx + 1, s_it + idx + 1, qb)) { ok = false; break; }
-          } else {
-            ptx::umma_commit(&ctl.q_empty[qb]);   // every QK of this unit is issued
-          }
+        int qk_issued = 0;
+        auto qk = [&](int t) -> bool {
+          if (!issue_qk(kv_it + t, s_it + t, qb)) return false;
+          if (++qk_issued == nt) ptx::umma_commit(&ctl.q_empty[qb]);   // Q may be replaced
+          return true;
+        };
+        auto pv = [&](int idx) -> bool {
           const int si = s_it + idx;
-          if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) { ok = false; break; }
+          if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) return false;
           ptx::tc_fence_after();
           if (idx == 0) {
-            if (!wait_or_abort(ctl, p, &ctl.o_empty[ob], ((q_it / OB) & 1) ^ 1)) { ok = false; break; }
+            if (!wait_or_abort(ctl, p, &ctl.o_empty[ob], ((q_it / OB) & 1) ^ 1)) return false;
             ptx::tc_fence_after();
           }
           const int kvi = kv_it + idx;
           const int st = kvi % VST;
-          if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) { ok = false; break; }
+          if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) return false;
           ptx::tc_fence_after();
-          // P: key columns [64 g, 64 g + 64) packed at S columns [64 g, 64 g + 32);
-          // V (MN-major) advances 16 rows = 2048 bytes per step
-          const uint32_t p_tmem = tmem + (si & 1) * 128;
+          // P of key columns [64 g, 64 g + 64) is packed at S columns [64 g, 64 g + 32);
+          // V (MN-major) advances 2048 bytes per step.
           const uint64_t v_desc = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES, Cfg::CHUNK_BYTES, 1024);
           uint32_t pa[8];
           uint64_t vd[8];
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            pa[kk] = p_tmem + (kk >> 2) * 64 + (kk & 3) * 8;
+            pa[kk] = tmem + (si & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
             vd[kk] = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
           }
           ptx::umma_ts_x8(o_tmem, pa, vd, idesc_pv, idx > 0 ? 1u : 0u);
           ptx::umma_commit(&ctl.v_empty[st]);
           if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
+          return true;
+        };
+        // P is packed over its S buffer, so Q K^T of tile idx+1 goes after the
+        // P V product that last read that buffer
+        ok = qk(0);
+        for (int idx = 0; idx < nt && ok; ++idx) {
+          if (idx + 1 < nt && !qk(idx + 1)) { ok = false; break; }
+          if (!pv(idx)) { ok = false; break; }
         }
         if (!ok) break;
         ptx::umma_commit(&ctl.o_full[ob]);
@@ -621,6 +655,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tmem_ld64(s_tmem, r);
         ptx::tmem_ld_wait(r);
         if constexpr (!SOFTMAX) {
+          // P is packed over this warpgroup's S columns (already in registers)
           if (full) silu_half<BF16, false>(r, s_tmem, ha2, rm, c0);
           else silu_half<BF16, true>(r, s_tmem, ha2, rm, c0);
         } else {
