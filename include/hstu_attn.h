@@ -26,8 +26,9 @@
  *
  * Every entry point is host-callable and asynchronous on `stream` unless it
  * says otherwise.  The library allocates no device or host memory and keeps no
- * state between calls other than per-device caches of kernel attributes; the
- * caller owns every buffer, including the workspace.
+ * state between calls other than per-device caches of kernel attributes and the
+ * fixed scratch of hstu_attn_fwd_static_ws; the caller owns every other buffer,
+ * including the workspace.
  */
 #ifndef HSTU_ATTN_H_
 #define HSTU_ATTN_H_
@@ -178,6 +179,41 @@ size_t hstu_fwd_args_size(void);
  */
 hstu_status hstu_selftest_wait_timeout(int32_t* result_dev, uint64_t timeout_ns, void* stream,
                                        int32_t* timed_out);
+
+/* Size of the library's fixed scratch used by hstu_attn_fwd_static_ws. */
+#define HSTU_STATIC_WS_BYTES (4u << 20)
+
+/*
+ * The forward without a caller workspace (no counterpart in the README; the
+ * README's forward has the framework allocate its buffers).  Same arguments,
+ * launches and results as hstu_attn_fwd, except that args->workspace and
+ * args->workspace_bytes are ignored: the scratch is a fixed array of
+ * HSTU_STATIC_WS_BYTES bytes per device, built into this library, and the call
+ * makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * It is meant for callers that cannot allocate device memory per call: a plain
+ * C or C++ host loop without a caching allocator, where cudaFree waits for the
+ * whole device and a per-call cudaMalloc would stall other streams; or code
+ * that has given all its device memory to a fixed budget up front.
+ *
+ * Limits and ordering:
+ *  - Calls whose hstu_attn_fwd_workspace_size exceeds HSTU_STATIC_WS_BYTES are
+ *    rejected with HSTU_ERR_WORKSPACE before anything is launched (typically
+ *    split-KV on long batches, whose fp32 partials need more room).
+ *  - The first call on a device looks up the array's device address (which
+ *    may load this library's kernels into the context) and sets the kernels'
+ *    attributes; make that first call before any stream capture begins.
+ *  - There is one scratch per device.  Calls on one stream run one after
+ *    another and are safe; calls in flight at the same time on different
+ *    streams or from different host threads race on it and give wrong results.
+ *  - Each call first clears the scratch's header (its work counter and device
+ *    error word must start at zero) with cudaMemsetAsync on `stream`; the rest
+ *    of the scratch is written before it is read.
+ *
+ * *workspace_used ([host], may be NULL) receives the scratch's device address,
+ * for hstu_attn_fwd_check.
+ */
+hstu_status hstu_attn_fwd_static_ws(const hstu_fwd_args* args, void* stream, const void** workspace_used);
 
 #ifdef __cplusplus
 }

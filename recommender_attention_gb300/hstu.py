@@ -74,6 +74,8 @@ EXPORTS = {
     "hstu_fwd_args_size": (ctypes.c_size_t, []),
     "hstu_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                                   ctypes.POINTER(ctypes.c_int32)]),
+    "hstu_attn_fwd_static_ws": (ctypes.c_int, [ctypes.POINTER(FwdArgs), ctypes.c_void_p,
+                                               ctypes.POINTER(ctypes.c_void_p)]),
 }
 
 
@@ -125,7 +127,8 @@ class HstuCall:
                  num_groups: int = 1, softmax: bool = False, max_seqlen_q: int = 0,
                  max_seqlen_kv: int = 0, num_splits: int = 0,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                 save_lse: bool = True, workspace: Optional[torch.Tensor] = None):
+                 save_lse: bool = True, workspace: Optional[torch.Tensor] = None,
+                 static_workspace: bool = False):
         self.lib = load_library()
         if q.dtype not in DTYPE_CODES or k.dtype != q.dtype or v.dtype != q.dtype:
             raise TypeError("q, k, v must share a dtype, fp16 or bf16")
@@ -163,11 +166,16 @@ class HstuCall:
         a.local_len, a.context_len, a.minfull_len, a.max_uih_len, a.attn_scale = [
             ctypes.cast(x, ctypes.c_void_p) for x in self._groups]
         self.args = a
+        self.static_workspace = static_workspace
+        self.static_ws_ptr = None
         size = ctypes.c_size_t(0)
         st = self.lib.hstu_attn_fwd_workspace_size(ctypes.byref(a), ctypes.byref(size))
         if st != HSTU_OK:
             raise HstuError(st, "hstu_attn_fwd_workspace_size")
         self.workspace_bytes = size.value
+        if static_workspace:   # the library's own scratch; nothing to allocate here
+            self.workspace = None
+            return
         if workspace is None or workspace.numel() < self.workspace_bytes:
             workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=q.device)
         self.workspace = workspace
@@ -187,9 +195,19 @@ class HstuCall:
         if st != HSTU_OK:
             raise HstuError(st, "hstu_attn_fwd")
 
+    def launch_static_ws(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Enqueues the forward through ``hstu_attn_fwd_static_ws`` (library scratch)."""
+        used = ctypes.c_void_p(0)
+        st = self.lib.hstu_attn_fwd_static_ws(ctypes.byref(self.args),
+                                              ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(used))
+        if st != HSTU_OK:
+            raise HstuError(st, "hstu_attn_fwd_static_ws")
+        self.static_ws_ptr = used.value
+
     def check(self, stream: Optional[torch.cuda.Stream] = None) -> int:
         err = ctypes.c_int32(0)
-        st = self.lib.hstu_attn_fwd_check(ctypes.c_void_p(self.workspace.data_ptr()),
+        ws = self.static_ws_ptr if self.static_workspace else self.workspace.data_ptr()
+        st = self.lib.hstu_attn_fwd_check(ctypes.c_void_p(ws),
                                           ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(err))
         if st != HSTU_OK:
             raise HstuError(st, "hstu_attn_fwd_check", err.value)
@@ -212,6 +230,18 @@ def hstu_attn_fwd(q, k, v, seq_offsets_q, seq_offsets_kv=None, num_targets=None,
     ``include/hstu_attn.h``).  Returns ``(o, lse)``; lse is None in SiLU mode."""
     call = HstuCall(q, k, v, seq_offsets_q, seq_offsets_kv, num_targets, **kw)
     call.launch(stream)
+    if check:
+        call.check(stream)
+    return call.o, call.lse
+
+
+def hstu_attn_fwd_static_ws(q, k, v, seq_offsets_q, seq_offsets_kv=None, num_targets=None, *,
+                            stream: Optional[torch.cuda.Stream] = None, check: bool = False, **kw):
+    """The forward on the library's fixed scratch (``hstu_attn_fwd_static_ws`` in
+    ``include/hstu_attn.h``): same arguments and results as ``hstu_attn_fwd``,
+    no workspace.  Returns ``(o, lse)``."""
+    call = HstuCall(q, k, v, seq_offsets_q, seq_offsets_kv, num_targets, static_workspace=True, **kw)
+    call.launch_static_ws(stream)
     if check:
         call.check(stream)
     return call.o, call.lse
