@@ -456,9 +456,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::umma_commit(&ctl.s_full[si & 1]);
         return true;
       };
+      // O += P V for tile index si (K/V index kvi) into O buffer ob; `first`
+      // starts the accumulation, `last` hands the buffer to the epilogue.
+      auto issue_pv = [&](int si, int kvi, int ob, int o_round, bool first, bool last) -> bool {
+        if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) return false;
+        ptx::tc_fence_after();
+        if (first) {
+          if (!wait_or_abort(ctl, p, &ctl.o_empty[ob], (o_round & 1) ^ 1)) return false;
+          ptx::tc_fence_after();
+        }
+        const int st = kvi % VST;
+        if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) return false;
+        ptx::tc_fence_after();
+        // P of key columns [64 g, 64 g + 64) is packed at S columns [64 g, 64 g + 32);
+        // V (MN-major) advances 2048 bytes per step.
+        const uint64_t v_desc = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES, Cfg::CHUNK_BYTES, 1024);
+        uint32_t pa[8];
+        uint64_t vd[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          pa[kk] = tmem + (si & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+          vd[kk] = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
+        }
+        ptx::umma_ts_x8(tmem + Cfg::O_COL + ob * D, pa, vd, idesc_pv, first ? 0u : 1u);
+        ptx::umma_commit(&ctl.v_empty[st]);
+        if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
+        if (last) ptx::umma_commit(&ctl.o_full[ob]);
+        return true;
+      };
+      // Tiles of consecutive units form one stream: Q K^T of tile t is issued
+      // before the P V product of tile t-1, across unit boundaries too, so the
+      // elementwise warps find the next scores ready when a unit ends.  (P is
+      // packed over its S buffer: Q K^T of tile t overwrites the buffer that the
+      // already-issued P V product of tile t-2 read.)  With one Q buffer the
+      // next unit's Q load waits for this unit's last Q K^T, so the pending
+      // P V product is issued first.
+      bool pend = false;
+      int pend_si = 0, pend_kvi = 0, pend_ob = 0, pend_round = 0;
+      bool pend_first = false, pend_last = false;
+      auto flush = [&]() -> bool {
+        if (!pend) return true;
+        pend = false;
+        return issue_pv(pend_si, pend_kvi, pend_ob, pend_round, pend_first, pend_last);
+      };
       while (ok && !ctl.abort_flag) {
         const int slot = sched_it % kSchedDepth;
-        if (!wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) break;
+        if (!wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) { ok = false; break; }
         const bool live = ctl.sched_live[slot] != 0;
         const UnitView u = ctl.sched_view[slot];
         ptx::mbar_arrive(&ctl.sched_empty[slot]);
@@ -466,57 +509,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!live) break;
         const int nt = u.k1 - u.k0;
         if (nt <= 0) continue;
+        if (QB == 1 && !flush()) { ok = false; break; }
         const int ob = q_it % OB;
-        const uint32_t o_tmem = tmem + Cfg::O_COL + ob * D;
         const int qb = q_it % QB;
-        if (!wait_or_abort(ctl, p, &ctl.q_full[qb], (q_it / QB) & 1)) break;
+        if (!wait_or_abort(ctl, p, &ctl.q_full[qb], (q_it / QB) & 1)) { ok = false; break; }
         ptx::tc_fence_after();
-        int qk_issued = 0;
-        auto qk = [&](int t) -> bool {
-          if (!issue_qk(kv_it + t, s_it + t, qb)) return false;
-          if (++qk_issued == nt) ptx::umma_commit(&ctl.q_empty[qb]);   // Q may be replaced
-          return true;
-        };
-        auto pv = [&](int idx) -> bool {
-          const int si = s_it + idx;
-          if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) return false;
-          ptx::tc_fence_after();
-          if (idx == 0) {
-            if (!wait_or_abort(ctl, p, &ctl.o_empty[ob], ((q_it / OB) & 1) ^ 1)) return false;
-            ptx::tc_fence_after();
-          }
-          const int kvi = kv_it + idx;
-          const int st = kvi % VST;
-          if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) return false;
-          ptx::tc_fence_after();
-          // P of key columns [64 g, 64 g + 64) is packed at S columns [64 g, 64 g + 32);
-          // V (MN-major) advances 2048 bytes per step.
-          const uint64_t v_desc = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES, Cfg::CHUNK_BYTES, 1024);
-          uint32_t pa[8];
-          uint64_t vd[8];
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            pa[kk] = tmem + (si & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
-            vd[kk] = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
-          }
-          ptx::umma_ts_x8(o_tmem, pa, vd, idesc_pv, idx > 0 ? 1u : 0u);
-          ptx::umma_commit(&ctl.v_empty[st]);
-          if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
-          return true;
-        };
-        // P is packed over its S buffer, so Q K^T of tile idx+1 goes after the
-        // P V product that last read that buffer
-        ok = qk(0);
-        for (int idx = 0; idx < nt && ok; ++idx) {
-          if (idx + 1 < nt && !qk(idx + 1)) { ok = false; break; }
-          if (!pv(idx)) { ok = false; break; }
+        for (int t = 0; t < nt; ++t) {
+          if (!issue_qk(kv_it + t, s_it + t, qb)) { ok = false; break; }
+          if (t == nt - 1) ptx::umma_commit(&ctl.q_empty[qb]);   // Q may be replaced
+          if (!flush()) { ok = false; break; }
+          pend = true;
+          pend_si = s_it + t;
+          pend_kvi = kv_it + t;
+          pend_ob = ob;
+          pend_round = q_it / OB;
+          pend_first = t == 0;
+          pend_last = t == nt - 1;
         }
         if (!ok) break;
-        ptx::umma_commit(&ctl.o_full[ob]);
         kv_it += nt;
         s_it += nt;
         ++q_it;
       }
+      if (ok) flush();
     }
   } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue warpgroup
