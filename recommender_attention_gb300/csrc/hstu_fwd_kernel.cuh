@@ -419,7 +419,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop, so every descriptor is warp-uniform;
+    // one elected lane issues the tcgen05 instructions and barrier arrivals.
+    const bool leader = ptx::elect_one_sync();
+    {
       constexpr uint32_t idesc_qk = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
       constexpr uint32_t idesc_pv = ptx::idesc_f16_f32acc(BF16, true, kBlockM, D);
       const uint32_t q_base = ptx::smem_u32(sQ);
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // S = Q K^T for the tile held in K stage (kvi % KST), into S buffer (si & 1).
       auto issue_qk = [&](int kvi, int si, int qb) -> bool {
         const int st = kvi % KST;
-        if (!wait_or_abort(ctl, p, &ctl.k_full[st], (kvi / KST) & 1)) return false;
+        if (!warp_wait_or_abort(ctl, p, &ctl.k_full[st], (kvi / KST) & 1)) return false;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + (si & 1) * 128;
         const uint64_t k_desc = ptx::sdesc_sw128(k_base + st * Cfg::TILE_BYTES, 16, 1024);
@@ -449,24 +452,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ad[j] = q_desc + static_cast<uint64_t>((qb * Cfg::TILE_BYTES) >> 4) + off;
             bd[j] = k_desc + off;
           }
-          if constexpr (G == 8) ptx::umma_ss_x8(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
-          else ptx::umma_ss_x4(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
+          if (leader) {
+            if constexpr (G == 8) ptx::umma_ss_x8(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
+            else ptx::umma_ss_x4(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
+          }
         }
-        ptx::umma_commit(&ctl.k_empty[st]);
-        ptx::umma_commit(&ctl.s_full[si & 1]);
+        if (leader) {
+          ptx::umma_commit(&ctl.k_empty[st]);
+          ptx::umma_commit(&ctl.s_full[si & 1]);
+        }
+        __syncwarp();
         return true;
       };
       // O += P V for tile index si (K/V index kvi) into O buffer ob; `first`
       // starts the accumulation, `last` hands the buffer to the epilogue.
       auto issue_pv = [&](int si, int kvi, int ob, int o_round, bool first, bool last) -> bool {
-        if (!wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) return false;
+        if (!warp_wait_or_abort(ctl, p, &ctl.p_full[si & 1], (si >> 1) & 1)) return false;
         ptx::tc_fence_after();
         if (first) {
-          if (!wait_or_abort(ctl, p, &ctl.o_empty[ob], (o_round & 1) ^ 1)) return false;
+          if (!warp_wait_or_abort(ctl, p, &ctl.o_empty[ob], (o_round & 1) ^ 1)) return false;
           ptx::tc_fence_after();
         }
         const int st = kvi % VST;
-        if (!wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) return false;
+        if (!warp_wait_or_abort(ctl, p, &ctl.v_full[st], (kvi / VST) & 1)) return false;
         ptx::tc_fence_after();
         // P of key columns [64 g, 64 g + 64) is packed at S columns [64 g, 64 g + 32);
         // V (MN-major) advances 2048 bytes per step.
@@ -478,10 +486,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           pa[kk] = tmem + (si & 1) * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
           vd[kk] = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
         }
-        ptx::umma_ts_x8(tmem + Cfg::O_COL + ob * D, pa, vd, idesc_pv, first ? 0u : 1u);
-        ptx::umma_commit(&ctl.v_empty[st]);
-        if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
-        if (last) ptx::umma_commit(&ctl.o_full[ob]);
+        if (leader) {
+          ptx::umma_ts_x8(tmem + Cfg::O_COL + ob * D, pa, vd, idesc_pv, first ? 0u : 1u);
+          ptx::umma_commit(&ctl.v_empty[st]);
+          if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
+          if (last) ptx::umma_commit(&ctl.o_full[ob]);
+        }
+        __syncwarp();
         return true;
       };
       // Tiles of consecutive units form one stream: Q K^T of tile t is issued
@@ -501,10 +512,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       while (ok && !ctl.abort_flag) {
         const int slot = sched_it % kSchedDepth;
-        if (!wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) { ok = false; break; }
+        if (!warp_wait_or_abort(ctl, p, &ctl.sched_full[slot], (sched_it / kSchedDepth) & 1)) { ok = false; break; }
         const bool live = ctl.sched_live[slot] != 0;
         const UnitView u = ctl.sched_view[slot];
-        ptx::mbar_arrive(&ctl.sched_empty[slot]);
+        __syncwarp();
+        if (leader) ptx::mbar_arrive(&ctl.sched_empty[slot]);
         ++sched_it;
         if (!live) break;
         const int nt = u.k1 - u.k0;
@@ -512,11 +524,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (QB == 1 && !flush()) { ok = false; break; }
         const int ob = q_it % OB;
         const int qb = q_it % QB;
-        if (!wait_or_abort(ctl, p, &ctl.q_full[qb], (q_it / QB) & 1)) { ok = false; break; }
+        if (!warp_wait_or_abort(ctl, p, &ctl.q_full[qb], (q_it / QB) & 1)) { ok = false; break; }
         ptx::tc_fence_after();
         for (int t = 0; t < nt; ++t) {
           if (!issue_qk(kv_it + t, s_it + t, qb)) { ok = false; break; }
-          if (t == nt - 1) ptx::umma_commit(&ctl.q_empty[qb]);   // Q may be replaced
+          if (t == nt - 1 && leader) ptx::umma_commit(&ctl.q_empty[qb]);   // Q may be replaced
           if (!flush()) { ok = false; break; }
           pend = true;
           pend_si = s_it + t;
