@@ -228,6 +228,23 @@ HSTU_HD bool tile_fully_allowed(const SeqGeom& s, int m, int n) {
   return tile_fully_allowed(s, tile_uih_bounds(s, m * kBlockM, m * kBlockM + kBlockM), n);
 }
 
+// tile_fully_allowed(s, b, n) as index ranges: true exactly when n < ctx_hi
+// (key tiles inside the context prefix) or lo <= n < hi (UIH tiles every row
+// of the query tile sees in full).
+struct FullTiles {
+  int ctx_hi, lo, hi;
+};
+HSTU_HD FullTiles full_tile_ranges(const SeqGeom& s, const TileBounds& b) {
+  FullTiles f;
+  f.ctx_hi = (s.c < s.Lkv ? s.c : s.Lkv) / kBlockN;
+  int e = s.Lkv;
+  if (s.c + s.ukv < e) e = s.c + s.ukv;
+  if (b.minHI < e) e = b.minHI;
+  f.hi = e > 0 ? e / kBlockN : 0;
+  f.lo = s.c >= b.maxLO ? 0 : (b.maxLO + kBlockN - 1) / kBlockN;
+  return f;
+}
+
 // Launch parameters of the persistent forward kernel.
 struct FwdParams {
   void* o;                 // [total_q, o_stride] outputs (fp16/bf16)

@@ -101,13 +101,21 @@ __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
   return r;
 }
 
+// Bits [0, x) of a word, x clamped to [0, 32].
+__device__ __forceinline__ uint32_t low_bits(int x) {
+  return x <= 0 ? 0u : (x >= 32 ? 0xFFFFFFFFu : (1u << x) - 1u);
+}
+
 // Per-row mask in tile-local column terms: key column c (0..127) of the tile
 // is allowed iff c < ctx || (unsigned)(c - lo) < span || c == diag.
 struct RowMask {
   int ctx, lo, diag;
   uint32_t span;
-  __device__ __forceinline__ bool allowed(int c) const {
-    return (c < ctx) | (static_cast<uint32_t>(c - lo) < span) | (c == diag);
+  // whether column cb + i is allowed, as bit i (i = 0..31)
+  __device__ __forceinline__ uint32_t bits32(int cb) const {
+    const int d = diag - cb;
+    return low_bits(ctx - cb) | (low_bits(lo + static_cast<int>(span) - cb) & ~low_bits(lo - cb)) |
+           (static_cast<uint32_t>(d) < 32u ? 1u << d : 0u);
   }
 };
 
@@ -204,10 +212,14 @@ __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tm
       for (int k = 0; k < 16; ++k) asm("fma.rn.f16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
     }
     if constexpr (MASKED) {
+      // bit 2k (2k+1) of the chunk's mask keeps the low (high) half of pair k
+      const uint32_t mb = rm.bits32(c0 + 32 * q);
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        h[k] &= (rm.allowed(c0 + 32 * q + 2 * k) ? 0x0000FFFFu : 0u) |
-                (rm.allowed(c0 + 32 * q + 2 * k + 1) ? 0xFFFF0000u : 0u);
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(mb << (31 - 2 * k)) >> 31);
+        const uint32_t hi = static_cast<uint32_t>(static_cast<int32_t>(mb << (30 - 2 * k)) >> 31);
+        h[k] &= (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
+      }
     }
     ptx::tmem_st16(p_tmem + 16 * q, h);
   }
@@ -665,10 +677,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
       float m_run = -INFINITY, l_run = 0.f;   // softmax row state (log2 domain); l over own columns
       bool ok = true;
+      // Walk tiles [k0, k1) of the unit's tile set: n is the current key tile,
+      // n_end the end of its range, (n_lo1, n_hi1) the next range.  Ranges are
+      // sorted and empty ones come last, so one step to the next range suffices.
+      int n, n_end, n_lo1, n_hi1, n_lo2, n_hi2;
+      {
+        const int n0c = u.ts.hi0 - u.ts.lo0, n1c = u.ts.hi1 - u.ts.lo1;
+        const int k = u.k0;
+        if (k < n0c) {
+          n = u.ts.lo0 + k; n_end = u.ts.hi0;
+          n_lo1 = u.ts.lo1; n_hi1 = u.ts.hi1; n_lo2 = u.ts.lo2; n_hi2 = u.ts.hi2;
+        } else if (k - n0c < n1c) {
+          n = u.ts.lo1 + (k - n0c); n_end = u.ts.hi1;
+          n_lo1 = u.ts.lo2; n_hi1 = u.ts.hi2; n_lo2 = n_hi2 = kNoTile;
+        } else {
+          n = u.ts.lo2 + (k - n0c - n1c); n_end = u.ts.hi2;
+          n_lo1 = n_hi1 = n_lo2 = n_hi2 = kNoTile;
+        }
+      }
+      const FullTiles ft = full_tile_ranges(u.s, u.tb);
       for (int idx = 0; idx < nt; ++idx) {
-        const int n = tileset_at(u.ts, u.k0 + idx);
-        const bool full = tile_fully_allowed(u.s, u.tb, n);
+        const bool full = n < ft.ctx_hi || (n >= ft.lo && n < ft.hi);
         const int j0 = n * kBlockN;
+        if (++n == n_end) {
+          n = n_lo1; n_end = n_hi1;
+          n_lo1 = n_lo2; n_hi1 = n_hi2;
+        }
         RowMask rm;
         rm.ctx = r_ctx - j0;
         rm.lo = r_lo - j0;
@@ -691,9 +725,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
             for (int k = 0; k < 64; ++k) mx = fmaxf(mx, __uint_as_float(r[k]));
           } else {
+            const uint32_t mb0 = rm.bits32(c0), mb1 = rm.bits32(c0 + 32);
 #pragma unroll
             for (int k = 0; k < 64; ++k) {
-              if (!rm.allowed(c0 + k)) r[k] = 0xFF800000u;   // -inf
+              const uint32_t mb = k < 32 ? mb0 : mb1;
+              const uint32_t keep = static_cast<uint32_t>(static_cast<int32_t>(mb << (31 - (k & 31))) >> 31);
+              r[k] = (r[k] & keep) | (0xFF800000u & ~keep);   // masked scores become -inf
               mx = fmaxf(mx, __uint_as_float(r[k]));
             }
           }
