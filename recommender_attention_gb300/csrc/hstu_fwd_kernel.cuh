@@ -11,10 +11,11 @@
 // fp32 partials for the combine kernel.
 //
 // Roles (512 threads, one CTA per SM, all waits time-bounded):
-//   warp 0       Q/K producer: TMA loads of Q once per unit and of K tiles into
-//                their ring, prefetching upcoming K/V tiles into L2
+//   warp 0       Q/K producer: TMA loads of Q once per unit (the next unit's Q
+//                prefetched into L2) and of K tiles into their ring
 //   warp 15      V producer: TMA loads of V tiles into their own ring
-//   warp 1       TMEM owner + MMA issuer (one thread)
+//   warp 1       TMEM owner + MMA issuer (the whole warp runs the loop, one
+//                elected lane issues)
 //   warps 2..5   epilogue warpgroup, one query row per thread: reads a unit's O
 //                out of TMEM once its last P V product is done, hands the
 //                buffer back, scales (softmax: by 1/rowsum) and stores O / LSE
@@ -295,21 +296,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      constexpr int PF = 4;   // K/V tiles prefetched into L2 ahead of the ring
-      auto prefetch_tile = [&](const UnitView& u, int k) {
-        const int krow = u.s.kv0 + tileset_at(u.ts, k) * kBlockN;
-#pragma unroll
-        for (int kc = 0; kc < KCH; ++kc) {
-          ptx::tma_prefetch_2d(&tm_k, u.h * D + kc * 64, krow);
-          ptx::tma_prefetch_2d(&tm_v, u.h * D + kc * 64, krow);
-        }
-      };
+      // Only the next unit's Q tile is prefetched into L2: K/V tiles are mostly
+      // L2 hits (every query tile of a head re-reads them), and prefetching them
+      // as well doubled the L2 lookups of a path already near the L2 limit.
       auto prefetch_unit = [&](const UnitView& u) {
         if (u.k1 <= u.k0) return;
 #pragma unroll
         for (int kc = 0; kc < KCH; ++kc)
           ptx::tma_prefetch_2d(&tm_q, u.h * D + kc * 64, u.s.q0 + u.m * kBlockM);
-        for (int k = u.k0; k < u.k1 && k < u.k0 + PF; ++k) prefetch_tile(u, k);
       };
       int q_it = 0, kv_it = 0, sched_it = 0;
       // reads the next published unit from the scheduler ring
@@ -328,8 +322,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       while (cur_live > 0 && !ctl.abort_flag) {
         int nxt_live = 0;
         bool have_nxt = false;
-        // the next unit is read (and its first tiles prefetched into L2) about
-        // three tiles before this unit's last loads
+        // the next unit is read (and its Q tile prefetched into L2) about three
+        // tiles before this unit's last loads
         auto look_ahead = [&]() -> bool {
           if (have_nxt) return true;
           have_nxt = true;
@@ -352,7 +346,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int k_ahead = cur.k1 - 3 > cur.k0 ? cur.k1 - 3 : cur.k0;
           for (int k = cur.k0; k < cur.k1 && ok; ++k) {
             if (k == k_ahead && !look_ahead()) { ok = false; break; }
-            if (k + PF < cur.k1) prefetch_tile(cur, k + PF);
             const int n = tileset_at(cur.ts, k);
             const int krow = cur.s.kv0 + n * kBlockN;
             const int ks = kv_it % KST;
