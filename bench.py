@@ -221,6 +221,65 @@ def time_device_steps(call, steps, warmup, world, stream):
     return step_ms, fwd_ms
 
 
+def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float):
+    """The other workloads of the scope (tiny, jagged, batched, group cross
+    split-KV in SiLU and softmax): one whole call (scheduler + forward [+
+    combine]) timed with CUDA events on the launching stream, L2 flushed
+    between calls (their inputs fit in L2).  Reported as useful TFLOP/s and
+    algorithmic HBM GB/s (q, k, v read once, o and lse written once)."""
+    from recommender_attention_gb300.hstu import HstuCall
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    cases = [("tiny", W.tiny_batched(), {}), ("jagged", W.jagged_readme(), {}),
+             ("batched", W.batched_default(), {}),
+             ("group_cross_splitkv_silu", W.group_cross_splitkv(softmax=False), {}),
+             ("group_cross_splitkv_softmax", W.group_cross_splitkv(softmax=True), {})]
+    out = {}
+    for name, w, over in cases:
+        q, k, v = w.tensors()
+        off_q = torch.from_numpy(w.seq_offsets_q()).to(device)
+        okv = w.seq_offsets_kv()
+        off_kv = torch.from_numpy(okv).to(device) if okv is not None else None
+        tg = w.num_targets()
+        tg = torch.from_numpy(tg).to(device) if tg is not None else None
+        dq, dk, dv = q.to(device), k.to(device), v.to(device)
+        call = HstuCall(dq, dk, dv, off_q, off_kv, tg, alpha=w.alpha, attn_scale=list(w.attn_scale),
+                        causal=w.causal, local_len=list(w.local_len), context_len=list(w.context_len),
+                        minfull_len=list(w.minfull_len), max_uih_len=list(w.max_uih_len),
+                        num_groups=w.num_groups, softmax=w.softmax,
+                        max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()),
+                        **over)
+        st = call.stats(stream)
+        for _ in range(warmup):
+            call.launch(stream)
+        call.check(stream)
+        times = []
+        for _ in range(steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call.launch(stream)
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        call.check(stream)
+        ms = statistics.median(times)
+        tq, tkv = dq.shape[0], dk.shape[0]
+        nbytes = 2 * w.nhead * (tq * w.hdim_qk + tkv * (w.hdim_qk + w.hdim_v) + tq * w.hdim_v)
+        if w.softmax:
+            nbytes += 4 * w.nhead * tq
+        flops = 2.0 * (w.hdim_qk + w.hdim_v) * st["allowed_pairs"]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "tflops_useful": flops / (ms * 1e-3) / 1e12, "gbs_algorithmic": gbs,
+                     "hbm_frac": gbs / hbm_peak, "algorithmic_bytes": nbytes,
+                     "allowed_pairs": st["allowed_pairs"], "executed_tiles": st["executed_tiles"],
+                     "num_splits": st["num_splits"], "timing": f"median of {steps}, L2 flushed between calls"}
+        del call, dq, dk, dv
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_e2e_steps(call, host, dev, steps, warmup, world, stream):
     """Public-API round trip per step: pinned host q/k/v/offsets/targets -> device,
     forward, device o -> pinned host."""
@@ -300,6 +359,11 @@ def run_cuda(args):
                              "fwd_kernel_ms": fw2,
                              "fwd_kernel_tflops": f2 / (fw2 * 1e-3) / 1e12}}
         del call2, dev2
+
+    if rank == 0 and not args.no_configs:
+        peaks0, _ = load_peaks()
+        extra["configs"] = small_config_lines(device, stream, max(5, args.steps), args.warmup,
+                                              float(peaks0.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
 
     step_ms_max = reduce_max(step_ms, world, device)
     e2e_ms_max = reduce_max(e2e_ms, world, device)
@@ -431,6 +495,7 @@ def main(argv=None):
     ap.add_argument("--hdim", type=int, default=128, choices=[64, 128, 256])
     ap.add_argument("--no-d256", action="store_true", help="skip the hdim-256 repeat")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other scope workloads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args(argv)

@@ -179,8 +179,11 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     return;
   }
 
-  // 4. units: per sequence, heads outer, query tiles from the last (most key
-  //    tiles under a causal mask) down, splits innermost
+  // 4. units: per sequence, heads outer, splits innermost.  Query tiles go
+  //    largest first: the tiles holding context rows (those rows see every
+  //    key, so these tiles run all key tiles), then the rest from the last
+  //    (most key tiles under a causal mask) down.  The queue then ends on the
+  //    smallest units, which keeps the persistent CTAs' finish times close.
   for (int u = tid; u < total; u += nth) {
     const int pos = find_segment(ubase, B, u);
     const int b = order[pos];
@@ -189,7 +192,10 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     const int local = u - ubase[pos];
     const int h = local / per_h;
     const int rem = local - h * per_h;
-    const int m = nq - 1 - rem / p.splits;
+    const int c = p.ctx[b / p.batch_per_group];
+    const int mc = min(nq, (c + kBlockM - 1) / kBlockM);
+    const int r = rem / p.splits;
+    const int m = r < mc ? r : nq - 1 - (r - mc);
     p.units[u] = make_int4(b, m, h, rem % p.splits);
   }
 
