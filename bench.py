@@ -197,25 +197,34 @@ def device_call(w, q, k, v, device):
 
 
 def time_device_steps(call, steps, warmup, world, stream):
+    """K whole steps back to back (the metric), then K more with events around
+    the forward kernel alone (the roofline's kernel time).  The per-kernel
+    events sit between the scheduler and the forward launch, where they would
+    stop the forward kernel's prologue from overlapping the scheduler, so the
+    step pass records none."""
     for _ in range(warmup):
         call.launch(stream)
     call.check(stream)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    for a, b in ev:   # materialise the event handles
-        a.record(stream)
-        b.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
-    for i in range(steps):
-        call.launch(stream, events=ev[i])
+    for _ in range(steps):
+        call.launch(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     step_ms = start.elapsed_time(end) / steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:   # materialise the event handles
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        call.launch(stream, events=ev[i])
+    torch.cuda.synchronize()
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     call.check(stream)
     return step_ms, fwd_ms

@@ -24,8 +24,18 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  kern<<<grid, kFwdThreads, smem, stream>>>(q, k, v, p);
-  return cudaGetLastError();
+  // programmatic dependent of the scheduler kernel launched just before it
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFwdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
 }
 }  // namespace
 

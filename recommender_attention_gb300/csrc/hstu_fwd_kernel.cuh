@@ -291,6 +291,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
+  // Launched as a programmatic dependent of the scheduler kernel: everything
+  // above overlapped its tail; the work list and header are read only now.
+  ptx::grid_dependency_wait();
   const int n_units = p.ws_header[kWsUnits];
 
   if (warp == 0) {

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
   __shared__ int s_err;
   __shared__ unsigned long long s_tiles;
   __shared__ int s_wsum[32];
+  ptx::grid_launch_dependents();   // the forward kernel may start its prologue now
   const int tid = threadIdx.x, nth = blockDim.x;
   const int B = p.batch;
   int* tbase = B <= kPrepSmemBatch ? dsm : p.batch_scratch;   // [B+1] query-tile offsets
