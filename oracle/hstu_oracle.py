@@ -33,6 +33,14 @@ used (each one a named constant or a commented branch):
     row; key coordinate x_j = j - c; d = x_i - x_j.  Causal removes d < 0.  A
     row is "min-full" when F > 0 and x_i >= u_kv - F; a row that is not
     min-full and has W > 0 keeps only |d| <= W (WINDOW_KEEPS_DISTANCE_EQUAL_W).
+  * M-FALCON ("From transformer parallelism to HSTU", section 5.3): a
+    microbatch of candidates attends to the cached keys/values of the user's
+    history, candidates never to each other.  As a cross-attention call whose
+    key sequence is [context | history | the candidates' own keys] and whose
+    query sequence is [context | the candidates] (targets on both sides,
+    ``kv_targets``), candidate r sees exactly what it sees as a target row of
+    the self-attention over [context | history | candidates]: the context
+    keys, the history under the usual rules, and its own key.
   * softmax mode excludes masked entries (weight 0) rather than giving them
     exp(0); a row with no allowed key has o = 0 and lse = -inf.
   * alpha = 0 means 1/sqrt(hdim_qk); attn_scale = 0 means 1/max_uih where
@@ -63,9 +71,11 @@ def phy_seqlen_q(uih_seqlen: int, num_targets: int, context_len: int) -> int:
     return uih_seqlen + num_targets + context_len
 
 
-def phy_seqlen_kv(uih_seqlen_kv: int, num_targets: int, context_len: int, cross: bool) -> int:
-    """Self-attention: uih + targets + context; cross-attention: uih_kv + context."""
-    if cross:
+def phy_seqlen_kv(uih_seqlen_kv: int, num_targets: int, context_len: int, cross: bool,
+                  kv_targets: bool = False) -> int:
+    """Self-attention: uih + targets + context; cross-attention: uih_kv + context,
+    plus the targets' own keys when the key sequence carries them (M-FALCON)."""
+    if cross and not kv_targets:
         return uih_seqlen_kv + context_len
     return uih_seqlen_kv + num_targets + context_len
 
@@ -87,13 +97,15 @@ class SeqMaskParams:
     """Mask parameters of one sequence (already resolved for its group)."""
 
     L_q: int          # physical query length  c + u + t
-    L_kv: int         # physical key length     c + u + t (self) or c + u_kv (cross)
+    L_kv: int         # physical key length     c + u + t (self), c + u_kv (cross),
+                      # c + u_kv + t (cross with the targets' own keys)
     context: int      # c
-    targets: int      # t (query side only in cross-attention)
+    targets: int      # t
     causal: bool
     local: int        # W, 0 = no local window
     minfull: int      # F, 0 = no min-full tail
     cross: bool
+    kv_targets: bool = False   # cross-attention key sequence ends with the t targets' keys
 
     @property
     def uih_q(self) -> int:
@@ -101,7 +113,9 @@ class SeqMaskParams:
 
     @property
     def uih_kv(self) -> int:
-        return (self.L_kv - self.context) if self.cross else self.uih_q
+        if not self.cross:
+            return self.uih_q
+        return self.L_kv - self.context - (self.targets if self.kv_targets else 0)
 
 
 def mask_rows(p: SeqMaskParams, rows: np.ndarray) -> np.ndarray:
@@ -121,9 +135,11 @@ def mask_rows(p: SeqMaskParams, rows: np.ndarray) -> np.ndarray:
     allowed |= rule & ~decided
     decided |= rule
 
-    # 2. target key (self-attention only has them): visible to its own row only.
+    # 2. target key (self-attention, or cross-attention carrying the targets'
+    #    keys): visible to its own row only.  Target r sits at query row c+u+r
+    #    and key row c+u_kv+r, so "own" means j - u_kv == i - u.
     rule = np.broadcast_to(j >= c + u_kv, shape)
-    allowed |= rule & ~decided & (i == j)
+    allowed |= rule & ~decided & (j - u_kv == i - u)
     decided |= rule
 
     # 3. contextual query with a UIH key: no causal/local rule applies to it.
@@ -198,6 +214,7 @@ class HstuParams:
     alpha: float = 0.0                     # 0 = 1/sqrt(hdim_qk)
     causal: bool = True
     softmax: bool = False
+    kv_targets: bool = False               # cross-attention keys end with the targets' own keys
 
 
 def _seq_params(params: HstuParams, b: int, batch: int, off_q, off_kv, targets):
@@ -209,11 +226,12 @@ def _seq_params(params: HstuParams, b: int, batch: int, off_q, off_kv, targets):
     L_kv = int(off_kv[b + 1] - off_kv[b]) if cross else L_q
     if L_q < c + t:
         raise ValueError(f"batch {b}: query length {L_q} < context {c} + targets {t}")
-    if cross and L_kv < c:
-        raise ValueError(f"batch {b}: key length {L_kv} < context {c}")
+    kvt = bool(params.kv_targets) and cross
+    if cross and L_kv < c + (t if kvt else 0):
+        raise ValueError(f"batch {b}: key length {L_kv} < context {c}" + (f" + targets {t}" if kvt else ""))
     sp = SeqMaskParams(L_q=L_q, L_kv=L_kv, context=c, targets=t, causal=bool(params.causal),
                        local=int(params.local_len[g]), minfull=int(params.minfull_len[g]),
-                       cross=cross)
+                       cross=cross, kv_targets=kvt)
     return g, sp
 
 

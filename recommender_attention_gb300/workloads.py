@@ -7,7 +7,10 @@ CUDA path's tests/bench and the fp64 oracle can draw from it.
 Layout of one sequence (composable_kernel ``18_hstu_attention`` README,
 "Masking": physical length = context + UIH + targets): ``[context | UIH |
 targets]`` on the query side; the key side is the same sequence for
-self-attention and ``[context | UIH_kv]`` for cross-attention.  Jagged tensors
+self-attention and ``[context | UIH_kv]`` for cross-attention, or
+``[context | UIH_kv | targets]`` when it carries the targets' own keys (an
+M-FALCON microbatch over a cached history: "From transformer parallelism to
+HSTU", section 5.3).  Jagged tensors
 are flattened ``[total_tokens, nhead, hdim]`` with ``seq_offsets`` of length
 ``batch + 1`` (README "Batch modes"); batched mode is the special case of equal
 lengths.
@@ -52,6 +55,7 @@ class Workload:
     dist: str = "uniform"            # "uniform" | "normal"
     seed: int = 0
     has_targets: bool = True         # False: pass no num_targets array (all zero)
+    kv_targets: bool = False         # cross-attention: the key side ends with the targets' keys
 
     # ----------------------------------------------------------- layout
     @property
@@ -68,7 +72,8 @@ class Workload:
     def lengths_kv(self) -> np.ndarray:
         if not self.cross:
             return self.lengths_q()
-        return np.array([self.context_len[self.group(b)] + self.uih_kv[b]
+        return np.array([self.context_len[self.group(b)] + self.uih_kv[b] +
+                         (self.targets[b] if self.kv_targets else 0)
                          for b in range(self.batch)], dtype=np.int64)
 
     def seq_offsets_q(self) -> np.ndarray:
@@ -177,12 +182,28 @@ def group_cross_splitkv(softmax: bool = False, batch: int = 32, seed: int = 11) 
                     dist="normal", seed=seed)
 
 
+def mfalcon(batch: int = 16, candidates: int = 128, seed: int = 21, softmax: bool = False) -> Workload:
+    """M-FALCON microbatch ("From transformer parallelism to HSTU", section 5.3):
+    per request a cached history of UIH_kv ~ U_int[2048, 8192] keys/values plus
+    the keys of `candidates` candidates; the queries are the 6 context rows and
+    the candidates (no history rows).  nhead 4, hdim 128, bf16, causal, N(0,1).
+    attn_scale is 1/8192 (the longest history a request may have), since the
+    query side has no UIH rows to take the default from."""
+    rng = np.random.default_rng(seed)
+    ukv = _draw_ints(rng, 2048, 8192, batch)
+    return Workload(name="mfalcon", batch=batch, nhead=4, hdim_qk=128, hdim_v=128, dtype="bf16",
+                    uih_q=[0] * batch, uih_kv=ukv, targets=[candidates] * batch,
+                    context_len=[6], attn_scale=[1.0 / 8192], causal=True, softmax=softmax,
+                    dist="normal", seed=seed, kv_targets=True)
+
+
 CONFIGS = {
     "tiny": tiny_batched,
     "jagged": jagged_readme,
     "batched": batched_default,
     "large": large_jagged,
     "group_cross": group_cross_splitkv,
+    "mfalcon": mfalcon,
 }
 
 

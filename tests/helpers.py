@@ -10,7 +10,8 @@ def oracle_params(w) -> HstuParams:
     return HstuParams(num_groups=w.num_groups, context_len=list(w.context_len),
                       local_len=list(w.local_len), minfull_len=list(w.minfull_len),
                       max_uih_len=list(w.max_uih_len), attn_scale=list(w.attn_scale),
-                      alpha=w.alpha, causal=w.causal, softmax=w.softmax)
+                      alpha=w.alpha, causal=w.causal, softmax=w.softmax,
+                      kv_targets=w.kv_targets)
 
 
 def as_f64(t) -> np.ndarray:

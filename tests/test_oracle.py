@@ -283,6 +283,66 @@ def _pins_pass():
     return True
 
 
+def _mfalcon_case(rng, softmax):
+    """One random request: the full self-attention over [context | history |
+    candidates] and the same candidates as an M-FALCON cross-attention call
+    over the cached [context | history] keys plus the candidates' own keys."""
+    c = int(rng.choice([0, 2, 5]))
+    hist = int(rng.integers(0, 150))
+    t = int(rng.integers(1, 20))
+    H, D = 2, 8
+    L = c + hist + t
+    q = rng.standard_normal((L, H, D))
+    k = rng.standard_normal((L, H, D))
+    v = rng.standard_normal((L, H, D))
+    kw = dict(context_len=[c], local_len=[int(rng.choice([0, 3, 40]))],
+              minfull_len=[int(rng.choice([0, 4, 30]))], attn_scale=[0.25], alpha=0.5,
+              causal=bool(rng.integers(0, 2)), softmax=softmax)
+    full = hstu_attention_forward(q, k, v, np.array([0, L]), None, np.array([t]), HstuParams(**kw))
+    rows = np.r_[0:c, c + hist:L]
+    mf = hstu_attention_forward(q[rows], k, v, np.array([0, c + t]), np.array([0, L]), np.array([t]),
+                                HstuParams(kv_targets=True, **kw))
+    return full, mf, rows
+
+
+def test_mfalcon_equals_target_rows_of_full_sequence():
+    """M-FALCON ("From transformer parallelism to HSTU", section 5.3): scoring the
+    candidates against the cached history keys/values gives each candidate exactly
+    its output as a target row of the whole sequence, since candidates never
+    attend to one another.  Pins the key-side target rule of cross-attention
+    against the (separately pinned) self-attention rules."""
+    rng = np.random.default_rng(5)
+    for softmax in (False, True):
+        for _ in range(40):
+            (o_full, lse_full), (o_mf, lse_mf), rows = _mfalcon_case(rng, softmax)
+            np.testing.assert_allclose(o_mf, o_full[rows], rtol=1e-12, atol=1e-12)
+            if softmax:
+                np.testing.assert_array_equal(np.isinf(lse_mf), np.isinf(lse_full[:, rows]))
+                fin = np.isfinite(lse_mf)
+                np.testing.assert_allclose(lse_mf[fin], lse_full[:, rows][fin], rtol=1e-12)
+
+
+def test_mfalcon_candidates_see_only_their_own_key():
+    for c, u_kv, t in [(0, 5, 3), (2, 9, 4), (3, 0, 2)]:
+        p = SeqMaskParams(L_q=c + t, L_kv=c + u_kv + t, context=c, targets=t, causal=True,
+                          local=0, minfull=0, cross=True, kv_targets=True)
+        assert p.uih_kv == u_kv and phy_seqlen_kv(u_kv, t, c, True, kv_targets=True) == p.L_kv
+        m = dense_mask(p)
+        cand = m[c:, c + u_kv:]
+        assert np.array_equal(cand, np.eye(t, dtype=bool))
+        assert not m[:c, c + u_kv:].any()         # context rows never see candidate keys
+        assert m[:, :c].all()                     # context keys: everyone
+        assert m[c:, c:c + u_kv].all()            # causal: candidates sit after the whole history
+
+
+def _mfalcon_pin_passes():
+    try:
+        test_mfalcon_equals_target_rows_of_full_sequence()
+    except AssertionError:
+        return False
+    return True
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     assert _pins_pass()
     # 1. window off by one
@@ -312,4 +372,16 @@ def test_planted_mistakes_are_caught(monkeypatch):
                         lambda q, k, v, a, al, sc, sm: real_head(q, k[::-1].copy(), v, a, al, sc, sm))
     assert not _pins_pass()
     monkeypatch.undo()
-    assert _pins_pass()
+    # 5. M-FALCON candidates that see one another's keys
+    def candidates_see_each_other(p, rows):
+        m = real_mask_rows(p, rows)
+        if p.cross and p.kv_targets:
+            r = np.asarray(rows)
+            m[np.ix_(r >= p.context + p.uih_q, np.arange(p.L_kv) >= p.context + p.uih_kv)] = True
+        return m
+
+    assert _mfalcon_pin_passes()
+    monkeypatch.setattr(orc, "mask_rows", candidates_see_each_other)
+    assert not _mfalcon_pin_passes()
+    monkeypatch.undo()
+    assert _pins_pass() and _mfalcon_pin_passes()
