@@ -232,7 +232,8 @@ def time_device_steps(call, steps, warmup, world, stream):
 
 def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float):
     """The other workloads of the scope (tiny, jagged, batched, group cross
-    split-KV in SiLU and softmax): one whole call (scheduler + forward [+
+    split-KV in SiLU and softmax, an M-FALCON candidate microbatch over cached
+    history keys): one whole call (scheduler + forward [+
     combine]) timed with CUDA events on the launching stream, L2 flushed
     between calls (their inputs fit in L2).  Reported as useful TFLOP/s and
     algorithmic HBM GB/s (q, k, v read once, o and lse written once)."""
@@ -241,7 +242,8 @@ def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float)
     cases = [("tiny", W.tiny_batched(), {}), ("jagged", W.jagged_readme(), {}),
              ("batched", W.batched_default(), {}),
              ("group_cross_splitkv_silu", W.group_cross_splitkv(softmax=False), {}),
-             ("group_cross_splitkv_softmax", W.group_cross_splitkv(softmax=True), {})]
+             ("group_cross_splitkv_softmax", W.group_cross_splitkv(softmax=True), {}),
+             ("mfalcon_microbatch", W.mfalcon(), {})]
     out = {}
     for name, w, over in cases:
         q, k, v = w.tensors()
@@ -256,7 +258,7 @@ def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float)
                         minfull_len=list(w.minfull_len), max_uih_len=list(w.max_uih_len),
                         num_groups=w.num_groups, softmax=w.softmax,
                         max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()),
-                        **over)
+                        kv_targets=w.kv_targets, **over)
         st = call.stats(stream)
         for _ in range(warmup):
             call.launch(stream)

@@ -13,10 +13,13 @@
  *
  * over jagged sequences laid out [context | UIH | targets] (query side; the key
  * side is the same sequence for self-attention, [context | UIH_kv] for
- * cross-attention).  The mask is the composite of the causal, local-window,
+ * cross-attention, or [context | UIH_kv | targets] for cross-attention with
+ * kv_targets: an M-FALCON candidate microbatch over a cached history, "From
+ * transformer parallelism to HSTU", section 5.3).  The mask is the composite of the causal, local-window,
  * contextual, min-full and target components of the README's "Masking" table:
  *   - context keys (j < c) are visible to every query;
- *   - a target key is visible only to its own row;
+ *   - a target key is visible only to its own row (target r: query row
+ *     c + u + r, key row c + uih_kv + r);
  *   - context rows see context keys and every UIH key;
  *   - UIH and target rows see UIH keys by UIH coordinate x (query UIH row:
  *     x = (i - c) + (uih_kv - uih_q), bottom-right aligned; target row:
@@ -40,7 +43,7 @@
 extern "C" {
 #endif
 
-#define HSTU_ABI_VERSION 1
+#define HSTU_ABI_VERSION 2
 #define HSTU_MAX_GROUPS 256
 #define HSTU_MAX_SPLITS 16
 
@@ -56,7 +59,7 @@ typedef enum hstu_status {
 /* Bits of the device error word (hstu_attn_fwd_check). */
 #define HSTU_DEVERR_OFFSETS 1     /* offsets not non-decreasing or beyond total_q / total_kv */
 #define HSTU_DEVERR_Q_LAYOUT 2    /* a query length < context_len + num_targets */
-#define HSTU_DEVERR_KV_LAYOUT 4   /* a cross-attention key length < context_len */
+#define HSTU_DEVERR_KV_LAYOUT 4   /* a cross-attention key length < context_len (+ num_targets with kv_targets) */
 #define HSTU_DEVERR_MAXSEQ 8      /* a length exceeds max_seqlen_q / max_seqlen_kv */
 #define HSTU_DEVERR_TIMEOUT 16    /* a pipeline wait gave up; outputs are incomplete */
 
@@ -110,6 +113,11 @@ typedef struct hstu_fwd_args {
    * that kernel alone (the scheduler and combine kernels fall outside). */
   void* event_fwd_begin;
   void* event_fwd_end;
+  /* Cross-attention only (seq_offsets_kv set): 1 = each key sequence is
+   * [context | UIH_kv | targets] with the same num_targets as its query
+   * sequence, the targets' own keys; target r of the queries sees target key r
+   * of the keys and no other target key.  0 = [context | UIH_kv]. */
+  int32_t kv_targets;
 } hstu_fwd_args;
 
 /* Counters of one call's schedule (hstu_attn_fwd_stats). */

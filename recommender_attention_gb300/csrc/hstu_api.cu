@@ -61,6 +61,8 @@ hstu_status validate(const hstu_fwd_args* a) {
   if (a->softmax != 0 && a->softmax != 1) return HSTU_ERR_INVALID_ARG;
   if (!std::isfinite(a->alpha) || a->alpha < 0.f) return HSTU_ERR_INVALID_ARG;
   if (a->seq_offsets_kv == nullptr && a->total_kv != a->total_q) return HSTU_ERR_INVALID_ARG;
+  if (a->kv_targets != 0 && a->kv_targets != 1) return HSTU_ERR_INVALID_ARG;
+  if (a->kv_targets && a->seq_offsets_kv == nullptr) return HSTU_ERR_INVALID_ARG;
   const int64_t wq = static_cast<int64_t>(a->nhead) * a->hdim_qk;
   const int64_t wv = static_cast<int64_t>(a->nhead) * a->hdim_v;
   const int64_t qs = packed_or(a->q_row_stride, wq), ks = packed_or(a->k_row_stride, wq);
@@ -185,6 +187,7 @@ PrepParams make_prep(const hstu_fwd_args* a, const Plan& pl) {
   pp.max_units = pl.max_units;
   pp.causal = a->causal;
   pp.self_attn = a->seq_offsets_kv == nullptr;
+  pp.kv_targets = a->kv_targets;
   fill_group_params(a, pp.ctx, pp.loc, pp.mf);
   for (int g = 0; g < kMaxGroups; ++g) {
     const bool in = g < a->num_groups;
@@ -278,6 +281,7 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   fp.batch_per_group = a->batch / a->num_groups;
   fp.causal = a->causal;
   fp.self_attn = a->seq_offsets_kv == nullptr;
+  fp.kv_targets = a->kv_targets;
   fp.splits = pl.splits;
   fp.alpha = a->alpha != 0.f ? a->alpha : 1.f / std::sqrt(static_cast<float>(a->hdim_qk));
   fill_group_params(a, fp.ctx, fp.loc, fp.mf);

@@ -60,6 +60,8 @@ struct SeqGeom {
   int c, u, ukv;   // context, query UIH, key UIH lengths
   int W, F;        // local window, min-full tail
   int causal, self_attn;
+  int tkv;         // the key side ends with the targets' own keys (self-attention, or
+                   // cross-attention over a cached history: M-FALCON)
 };
 
 // UIH coordinate of query row i (meaningful for i >= c).
@@ -87,9 +89,10 @@ HSTU_HD void row_uih_keys(const SeqGeom& s, int i, int& lo, int& hi) {
   if (hi < lo) hi = lo;
 }
 
-// The single target key row i may see (itself), or -1.
+// The single target key row i may see (its own), or -1.  Target r is query row
+// c + u + r and key row c + ukv + r.
 HSTU_HD int row_diag_key(const SeqGeom& s, int i) {
-  return (s.self_attn && i >= s.c + s.u && i < s.Lq) ? i : -1;
+  return (s.tkv && i >= s.c + s.u && i < s.Lq) ? i + (s.ukv - s.u) : -1;
 }
 
 // Number of allowed keys of row i (0 <= i < Lq).
@@ -164,11 +167,12 @@ HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, int m) {
     t.lo1 = b.LO / kBlockN;
     t.hi1 = (b.HI + kBlockN - 1) / kBlockN;
   }
-  if (s.self_attn) {
+  if (s.tkv) {   // the target rows' own keys
     const int d0 = i0 > s.c + s.u ? i0 : s.c + s.u;
+    const int sh = s.ukv - s.u;
     if (i1 > d0) {
-      t.lo2 = d0 / kBlockN;
-      t.hi2 = (i1 + kBlockN - 1) / kBlockN;
+      t.lo2 = (d0 + sh) / kBlockN;
+      t.hi2 = (i1 + sh + kBlockN - 1) / kBlockN;
     }
   }
   // sort the three slots by start (empty slots sort last)
@@ -260,7 +264,7 @@ struct FwdParams {
   long long o_stride;      // elements between consecutive output tokens
   int total_q;
   int batch, nhead, num_groups, batch_per_group;
-  int causal, self_attn, splits;
+  int causal, self_attn, kv_targets, splits;
   float alpha;             // resolved QK scale
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
 };
@@ -276,7 +280,7 @@ struct PrepParams {
   int* batch_scratch;      // [4 * batch + 2] ints (used when batch is large)
   int batch, nhead, num_groups, batch_per_group, splits;
   int total_q, total_kv, max_seqlen_q, max_seqlen_kv, max_units;
-  int causal, self_attn;
+  int causal, self_attn, kv_targets;
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups], max_uih[kMaxGroups];
   float attn_scale[kMaxGroups];
 };
@@ -296,7 +300,7 @@ struct CombineParams {
 
 // Fills the geometry of sequence b from the device/host offset arrays.
 HSTU_HD SeqGeom make_geom(const int* off_q, const int* off_kv, const int* targets, int b,
-                          int c, int W, int F, int causal, int self_attn) {
+                          int c, int W, int F, int causal, int self_attn, int kv_targets) {
   SeqGeom s;
   s.q0 = off_q[b];
   s.Lq = off_q[b + 1] - s.q0;
@@ -305,11 +309,12 @@ HSTU_HD SeqGeom make_geom(const int* off_q, const int* off_kv, const int* target
   const int t = targets ? targets[b] : 0;
   s.c = c;
   s.u = s.Lq - c - t;
-  s.ukv = self_attn ? s.u : s.Lkv - c;
+  s.ukv = self_attn ? s.u : s.Lkv - c - (kv_targets ? t : 0);
   s.W = W;
   s.F = F;
   s.causal = causal;
   s.self_attn = self_attn;
+  s.tkv = self_attn || kv_targets;
   return s;
 }
 

@@ -137,7 +137,7 @@ __device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
   u.sp = w.w;
   u.g = b / p.batch_per_group;
   u.s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[u.g], p.loc[u.g], p.mf[u.g], p.causal,
-                  p.self_attn);
+                  p.self_attn, p.kv_targets);
   u.ts = query_tile_kv_tiles(u.s, u.m);
   u.tb = tile_uih_bounds(u.s, u.m * kBlockM, u.m * kBlockM + kBlockM);
   split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
       const int k0 = p.off_kv[b], k1 = p.off_kv[b + 1];
       if (k0 < 0 || k1 < k0 || k1 > p.total_kv) err |= kErrOffsets;
       Lkv = k1 - k0;
-      if (Lkv < c) err |= kErrKvLayout;
+      if (Lkv < c + (p.kv_targets ? t : 0)) err |= kErrKvLayout;
     }
     if (q1 - q0 > p.max_seqlen_q || Lkv > p.max_seqlen_kv) err |= kErrMaxSeqlen;
     if (err) atomicOr(&s_err, err);
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     const int b = find_segment(tbase, B, i);
     const int g = b / p.batch_per_group;
     const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[g], p.loc[g], p.mf[g], p.causal,
-                                p.self_attn);
+                                p.self_attn, p.kv_targets);
     const int cnt = query_tile_kv_tiles(s, i - tbase[b]).count;
     atomicAdd(&cost[b], cnt);
     tiles += cnt;
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(256) hstu_pairs_kernel(const __grid_constant__
   const int b = blockIdx.x;
   const int g = b / p.batch_per_group;
   const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[g], p.loc[g], p.mf[g], p.causal,
-                              p.self_attn);
+                              p.self_attn, p.kv_targets);
   long long sum = 0;
   for (int i = threadIdx.x; i < s.Lq; i += blockDim.x) sum += row_pair_count(s, i);
 #pragma unroll

@@ -53,6 +53,7 @@ class FwdArgs(ctypes.Structure):
         ("max_uih_len", ctypes.c_void_p), ("attn_scale", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("event_fwd_begin", ctypes.c_void_p), ("event_fwd_end", ctypes.c_void_p),
+        ("kv_targets", ctypes.c_int32),
     ]
 
 
@@ -128,7 +129,7 @@ class HstuCall:
                  max_seqlen_kv: int = 0, num_splits: int = 0,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                  save_lse: bool = True, workspace: Optional[torch.Tensor] = None,
-                 static_workspace: bool = False):
+                 static_workspace: bool = False, kv_targets: bool = False):
         self.lib = load_library()
         if q.dtype not in DTYPE_CODES or k.dtype != q.dtype or v.dtype != q.dtype:
             raise TypeError("q, k, v must share a dtype, fp16 or bf16")
@@ -153,6 +154,7 @@ class HstuCall:
         a.max_seqlen_q, a.max_seqlen_kv = max_seqlen_q, max_seqlen_kv
         a.causal, a.softmax = int(bool(causal)), int(bool(softmax))
         a.num_groups, a.num_splits, a.alpha = g, num_splits, alpha
+        a.kv_targets = int(bool(kv_targets))
         a.q_row_stride, a.k_row_stride = q.stride(0), k.stride(0)
         a.v_row_stride, a.o_row_stride = v.stride(0), out.stride(0)
         for t in (q, k, v, out):

@@ -182,15 +182,16 @@ def group_cross_splitkv(softmax: bool = False, batch: int = 32, seed: int = 11) 
                     dist="normal", seed=seed)
 
 
-def mfalcon(batch: int = 16, candidates: int = 128, seed: int = 21, softmax: bool = False) -> Workload:
+def mfalcon(batch: int = 16, candidates: int = 128, seed: int = 21, softmax: bool = False,
+            history=(2048, 8192)) -> Workload:
     """M-FALCON microbatch ("From transformer parallelism to HSTU", section 5.3):
-    per request a cached history of UIH_kv ~ U_int[2048, 8192] keys/values plus
+    per request a cached history of UIH_kv ~ U_int[history] (default [2048, 8192]) keys/values plus
     the keys of `candidates` candidates; the queries are the 6 context rows and
     the candidates (no history rows).  nhead 4, hdim 128, bf16, causal, N(0,1).
     attn_scale is 1/8192 (the longest history a request may have), since the
     query side has no UIH rows to take the default from."""
     rng = np.random.default_rng(seed)
-    ukv = _draw_ints(rng, 2048, 8192, batch)
+    ukv = _draw_ints(rng, history[0], history[1], batch)
     return Workload(name="mfalcon", batch=batch, nhead=4, hdim_qk=128, hdim_v=128, dtype="bf16",
                     uih_q=[0] * batch, uih_kv=ukv, targets=[candidates] * batch,
                     context_len=[6], attn_scale=[1.0 / 8192], causal=True, softmax=softmax,
@@ -208,13 +209,17 @@ CONFIGS = {
 
 
 def random_small(seed: int, *, dtype: str = "bf16", hdim: int = 64, softmax: bool = False,
-                 cross: Optional[bool] = None, max_uih: int = 300) -> Workload:
-    """A small random workload for fuzzing: ragged lengths, random mask parameters."""
+                 cross: Optional[bool] = None, max_uih: int = 300, kv_targets: bool = False) -> Workload:
+    """A small random workload for fuzzing: ragged lengths, random mask parameters.
+    kv_targets=True makes it a cross-attention call whose keys end with the
+    targets' own keys."""
     rng = np.random.default_rng(1000 + seed)
     num_groups = int(rng.choice([1, 1, 2, 3]))
     batch = num_groups * int(rng.integers(1, 4))
     if cross is None:
         cross = bool(rng.integers(0, 2))
+    if kv_targets:
+        cross = True
     uq = _draw_ints(rng, 0, max_uih, batch)
     ukv = _draw_ints(rng, 0, 2 * max_uih, batch) if cross else None
     tg = _draw_ints(rng, 0, 20, batch)
@@ -227,4 +232,5 @@ def random_small(seed: int, *, dtype: str = "bf16", hdim: int = 64, softmax: boo
                     max_uih_len=[0] * num_groups,
                     attn_scale=[0.0] * num_groups, alpha=0.0,
                     causal=bool(rng.integers(0, 4) > 0), softmax=softmax,
-                    dist="normal" if rng.integers(0, 2) else "uniform", seed=seed)
+                    dist="normal" if rng.integers(0, 2) else "uniform", seed=seed,
+                    kv_targets=kv_targets)

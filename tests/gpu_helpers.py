@@ -27,7 +27,8 @@ def call_kwargs(w, **over):
               local_len=list(w.local_len), context_len=list(w.context_len),
               minfull_len=list(w.minfull_len), max_uih_len=list(w.max_uih_len),
               num_groups=w.num_groups, softmax=w.softmax,
-              max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()))
+              max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()),
+              kv_targets=w.kv_targets)
     kw.update(over)
     return kw
 

@@ -75,6 +75,38 @@ def test_fuzz_small_parity(seed, softmax):
     check_full(w, num_splits=splits)
 
 
+# ---------------------------------------------------------------- M-FALCON (keys end with the targets')
+@pytest.mark.parametrize("softmax", [False, True])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_mfalcon_parity(softmax, splits):
+    w = W.mfalcon(batch=4, candidates=130, softmax=softmax, history=(300, 1500))
+    check_full(w, num_splits=splits)
+
+
+def test_mfalcon_equals_full_sequence_target_rows_on_gpu():
+    """Through the kernel: the candidates scored against the cached history keys
+    equal the context and target rows of the whole-sequence self-attention."""
+    full = W.Workload(name="mf_full", batch=2, nhead=2, hdim_qk=128, hdim_v=128, dtype="bf16",
+                      uih_q=[700, 333], targets=[64, 129], context_len=[6], attn_scale=[0.001],
+                      causal=True, dist="normal", seed=31)
+    q, k, v = full.tensors()
+    o_full, _ = gpu_forward(full, q, k, v)
+    off = full.seq_offsets_q()
+    rows = np.concatenate([np.r_[off[b]:off[b] + 6, off[b] + 6 + full.uih_q[b]:off[b + 1]]
+                           for b in range(full.batch)])
+    mf = full.with_(name="mf", uih_q=[0, 0], uih_kv=list(full.uih_q), kv_targets=True)
+    q_mf = q[torch.from_numpy(rows)]
+    o_mf, _ = gpu_forward(mf, q_mf, k, v)
+    np.testing.assert_allclose(o_mf, o_full[rows], rtol=2e-2, atol=2e-2 * np.abs(o_full).max())
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fuzz_kv_targets_parity(seed):
+    w = W.random_small(100 + seed, dtype="bf16" if seed % 2 else "fp16", hdim=[64, 128, 256][seed % 3],
+                       softmax=bool(seed % 2), kv_targets=True)
+    check_full(w, num_splits=[1, 2, 0][seed % 3])
+
+
 # ---------------------------------------------------------------- edge cases
 def test_edge_empty_sequences_and_no_targets_array():
     w = W.Workload(name="edge_empty", batch=4, nhead=2, hdim_qk=64, hdim_v=64, dtype="bf16",
@@ -120,7 +152,7 @@ def test_output_rows_outside_sequences_untouched():
 
 
 # ---------------------------------------------------------------- schedule accounting
-@pytest.mark.parametrize("cfg", ["tiny", "jagged", "batched", "group_cross"])
+@pytest.mark.parametrize("cfg", ["tiny", "jagged", "batched", "group_cross", "mfalcon"])
 def test_tile_skip_and_pair_accounting(cfg):
     w = W.CONFIGS[cfg]()
     q, k, v = w.tensors()
@@ -132,9 +164,9 @@ def test_tile_skip_and_pair_accounting(cfg):
     assert stats["device_error"] == 0
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(12))
 def test_tile_skip_accounting_fuzz(seed):
-    w = W.random_small(seed, hdim=64)
+    w = W.random_small(seed, hdim=64, kv_targets=seed >= 8)
     q, k, v = w.tensors()
     stats = gpu_call(w, q, k, v, num_splits=1).stats()
     p = oracle_params(w)
