@@ -353,23 +353,25 @@ def run_cuda(args):
                                           torch.from_numpy(w.num_targets())))
     e2e_ms, h2d, d2h = time_e2e_steps(call, host, dev, args.steps, args.warmup, world, stream)
 
-    # the same workload at hdim 256 (one forward kernel per step, same timing rules)
+    # the same workload at the other head dimensions (one forward kernel per
+    # step, same timing rules): 256, 96 and the asymmetric 96/64
     extra = {}
     if args.hdim == 128 and not args.no_d256:
         del call, dev
         torch.cuda.empty_cache()
-        w2 = rank_workload(rank, 256)
-        q2, k2, v2 = w2.tensors()
-        call2, dev2 = device_call(w2, q2, k2, v2, device)
-        st2 = call2.stats(stream)
-        f2 = 2.0 * (w2.hdim_qk + w2.hdim_v) * st2["allowed_pairs"]
-        s2, fw2 = time_device_steps(call2, args.steps, args.warmup, world, stream)
-        s2 = reduce_max(s2, world, device)
-        tot2 = reduce_sum(f2, world, device)
-        extra = {"hdim256": {"value": tot2 / (s2 * 1e-3) / 1e12, "ms_per_step": s2,
-                             "fwd_kernel_ms": fw2,
-                             "fwd_kernel_tflops": f2 / (fw2 * 1e-3) / 1e12}}
-        del call2, dev2
+        for key, dqk, dv in (("hdim256", 256, 256), ("hdim96", 96, 96), ("hdim96_64", 96, 64)):
+            w2 = W.large_jagged(hdim=dqk, hdim_v=dv, seed=7 + rank)
+            q2, k2, v2 = w2.tensors()
+            call2, dev2 = device_call(w2, q2, k2, v2, device)
+            st2 = call2.stats(stream)
+            f2 = 2.0 * (w2.hdim_qk + w2.hdim_v) * st2["allowed_pairs"]
+            s2, fw2 = time_device_steps(call2, args.steps, args.warmup, world, stream)
+            s2 = reduce_max(s2, world, device)
+            tot2 = reduce_sum(f2, world, device)
+            extra[key] = {"value": tot2 / (s2 * 1e-3) / 1e12, "ms_per_step": s2,
+                          "fwd_kernel_ms": fw2, "fwd_kernel_tflops": f2 / (fw2 * 1e-3) / 1e12}
+            del call2, dev2, q2, k2, v2
+            torch.cuda.empty_cache()
 
     if rank == 0 and not args.no_configs:
         peaks0, _ = load_peaks()
@@ -504,7 +506,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--hdim", type=int, default=128, choices=[64, 128, 256])
-    ap.add_argument("--no-d256", action="store_true", help="skip the hdim-256 repeat")
+    ap.add_argument("--no-d256", action="store_true", help="skip the hdim 256, 96 and 96/64 repeats")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other scope workloads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

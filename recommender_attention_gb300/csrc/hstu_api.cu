@@ -50,8 +50,9 @@ hstu_status validate(const hstu_fwd_args* a) {
   if (!a) return HSTU_ERR_INVALID_ARG;
   if (a->dtype != HSTU_DTYPE_FP16 && a->dtype != HSTU_DTYPE_BF16) return HSTU_ERR_UNSUPPORTED;
   if (a->batch < 1 || a->nhead < 1 || a->total_q < 1 || a->total_kv < 1) return HSTU_ERR_INVALID_ARG;
-  if (a->hdim_qk != 64 && a->hdim_qk != 128 && a->hdim_qk != 256) return HSTU_ERR_UNSUPPORTED;
-  if (a->hdim_v != a->hdim_qk) return HSTU_ERR_UNSUPPORTED;
+  if (a->hdim_qk != 64 && a->hdim_qk != 96 && a->hdim_qk != 128 && a->hdim_qk != 256)
+    return HSTU_ERR_UNSUPPORTED;
+  if (a->hdim_v != a->hdim_qk && !(a->hdim_qk == 96 && a->hdim_v == 64)) return HSTU_ERR_UNSUPPORTED;
   if (a->num_groups < 1 || a->batch % a->num_groups != 0) return HSTU_ERR_INVALID_ARG;
   if (a->num_groups > kMaxGroups) return HSTU_ERR_UNSUPPORTED;
   if (a->num_splits < 0) return HSTU_ERR_INVALID_ARG;
@@ -251,10 +252,11 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   const bool bf16 = a->dtype == HSTU_DTYPE_BF16;
   const int D = a->hdim_qk;
   const int64_t wq = static_cast<int64_t>(a->nhead) * D;
+  const int64_t wv = static_cast<int64_t>(a->nhead) * a->hdim_v;
   CUtensorMap tq, tk, tv;
   if (!encode_map(&tq, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq)) ||
       !encode_map(&tk, a->k, bf16, wq, a->total_kv, packed_or(a->k_row_stride, wq)) ||
-      !encode_map(&tv, a->v, bf16, wq, a->total_kv, packed_or(a->v_row_stride, wq)))
+      !encode_map(&tv, a->v, bf16, wv, a->total_kv, packed_or(a->v_row_stride, wv)))
     return HSTU_ERR_CUDA;
 
   const PrepParams pp = make_prep(a, pl);
@@ -273,7 +275,7 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   fp.units = pp.units;
   fp.ws_header = pp.ws_header;
   fp.group_scale = pp.group_scale;
-  fp.o_stride = packed_or(a->o_row_stride, wq);
+  fp.o_stride = packed_or(a->o_row_stride, wv);
   fp.total_q = a->total_q;
   fp.batch = a->batch;
   fp.nhead = a->nhead;
@@ -291,6 +293,7 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
     return HSTU_ERR_CUDA;
   cudaError_t e;
   if (D == 64) e = launch_fwd_d64(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
+  else if (D == 96) e = launch_fwd_d96(tq, tk, tv, fp, a->hdim_v, bf16, a->softmax != 0, grid, stream);
   else if (D == 128) e = launch_fwd_d128(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
   else e = launch_fwd_d256(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
   if (e != cudaSuccess) return HSTU_ERR_CUDA;
@@ -315,7 +318,7 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
     cp.batch_per_group = fp.batch_per_group;
     cp.splits = pl.splits;
     cp.softmax = a->softmax;
-    if (launch_combine(cp, D, bf16, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+    if (launch_combine(cp, a->hdim_v, bf16, stream) != cudaSuccess) return HSTU_ERR_CUDA;
   }
   return HSTU_OK;
 }

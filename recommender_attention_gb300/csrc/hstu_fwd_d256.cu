@@ -6,15 +6,15 @@ namespace hstu {
 
 // dynamic (tiles + alignment slack) plus static (barriers, exchange buffers) shared memory
 // must fit the 227 KB a CTA may use on sm_103a.
-static_assert(FwdCfg<256, false>::SMEM_BYTES + sizeof(FwdSmemCtl) <= 232448, "shared memory over the per-CTA limit");
-static_assert(FwdCfg<256, true>::SMEM_BYTES + sizeof(FwdSmemCtl) <= 232448, "shared memory over the per-CTA limit");
+static_assert(FwdCfg<256, 256, false>::SMEM_BYTES + sizeof(FwdSmemCtl) <= 232448, "shared memory over the per-CTA limit");
+static_assert(FwdCfg<256, 256, true>::SMEM_BYTES + sizeof(FwdSmemCtl) <= 232448, "shared memory over the per-CTA limit");
 
 namespace {
 template <bool BF16, bool SOFTMAX>
 cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const FwdParams& p, int grid, cudaStream_t stream) {
-  constexpr int smem = FwdCfg<256, SOFTMAX>::SMEM_BYTES;
-  auto kern = hstu_fwd_kernel<256, BF16, SOFTMAX>;
+  constexpr int smem = FwdCfg<256, 256, SOFTMAX>::SMEM_BYTES;
+  auto kern = hstu_fwd_kernel<256, 256, BF16, SOFTMAX>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -28,8 +28,14 @@
 // TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores; the
 // 16-bit P of key columns [64g, 64g+64) is packed into S columns
 // [64g, 64g+32) of the same buffer;
-// O [256, 256 + D) and, for D <= 128, a second O buffer right after it so the
+// O [256, 256 + DV) and, for DV <= 128, a second O buffer right after it so the
 // epilogue of one unit overlaps the next unit's P V products.
+//
+// Head dimensions: D (of q and k) in {64, 96, 128, 256}, DV (of v and o) equal
+// to D or, for D = 96, 64.  A 96-wide row occupies two 64-element swizzle
+// chunks; Q K^T runs 6 k-steps, so the unused half chunk (the next head's
+// columns, or TMA zero fill past the last head) is never read, and P V with
+// N = 96 reads only the first 96 columns of the V tile.
 //
 // SiLU is evaluated as SiLU(s) = h + h tanh(h), h = s/2, in packed 16-bit
 // arithmetic of the storage type (one tanh.approx per two elements); P is
@@ -50,22 +56,25 @@ struct SoftmaxScratch {
   float rs_l[2][2][128];      // [O buffer][warpgroup][row] row sum over the warpgroup's columns
 };
 
-template <int D, bool SOFTMAX>
+template <int D, int DV, bool SOFTMAX>
 struct FwdCfg {
-  static constexpr int KCH = D / 64;                  // 128-byte column chunks per row
-  static constexpr int TILE_BYTES = kBlockN * D * 2;  // one Q, K or V tile
+  static constexpr int KCH = (D + 63) / 64;           // 128-byte column chunks per Q / K row
+  static constexpr int VCH = (DV + 63) / 64;          // ... per V row
   static constexpr int CHUNK_BYTES = kBlockN * 128;   // one 128-row x 128-byte TMA box
+  static constexpr int TILE_BYTES = KCH * CHUNK_BYTES;    // one Q or K tile
+  static constexpr int VTILE_BYTES = VCH * CHUNK_BYTES;   // one V tile
   // Q is double-buffered where it fits so the next unit's Q streams in early.
   static constexpr int QBUF = D <= 128 ? 2 : 1;
-  static constexpr int KSTAGES = D == 64 ? 4 : (D == 128 ? (SOFTMAX ? 2 : 3) : 1);   // K ring depth
-  static constexpr int VSTAGES = D == 64 ? 4 : (D == 128 ? 2 : 1);                   // V ring depth
-  static constexpr int TILES_BYTES = (QBUF + KSTAGES + VSTAGES) * TILE_BYTES;
+  static constexpr int KSTAGES = D == 64 ? 4 : (D <= 128 ? (SOFTMAX ? 2 : 3) : 1);   // K ring depth
+  static constexpr int VSTAGES = D == 64 ? 4 : (D <= 128 ? 2 : 1);                   // V ring depth
+  static constexpr int TILES_BYTES = (QBUF + KSTAGES) * TILE_BYTES + VSTAGES * VTILE_BYTES;
   static constexpr int SMEM_BYTES =
       TILES_BYTES + (SOFTMAX ? static_cast<int>(sizeof(SoftmaxScratch)) : 0) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
-  static constexpr int O_BUFS = D <= 128 ? 2 : 1;
-  static_assert(O_COL + O_BUFS * D <= TMEM_COLS, "TMEM budget");
+  static constexpr int O_BUFS = DV <= 128 ? 2 : 1;
+  static_assert(O_COL + O_BUFS * DV <= TMEM_COLS, "TMEM budget");
+  static_assert(D % 16 == 0 && DV % 32 == 0 && DV <= 256, "head dimensions");
 };
 
 constexpr int kEpiWarps = 4;       // epilogue warpgroup
@@ -226,12 +235,13 @@ __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tm
   }
 }
 
-template <int D, bool BF16, bool SOFTMAX>
+template <int D, int DV, bool BF16, bool SOFTMAX>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
-  using Cfg = FwdCfg<D, SOFTMAX>;
+  using Cfg = FwdCfg<D, DV, SOFTMAX>;
   constexpr int KCH = Cfg::KCH;
+  constexpr int VCH = Cfg::VCH;
   constexpr int KST = Cfg::KSTAGES;
   constexpr int VST = Cfg::VSTAGES;
   constexpr int OB = Cfg::O_BUFS;
@@ -385,11 +395,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int vs = kv_it % VST;
           const int vrow = u.s.kv0 + tileset_at(u.ts, k) * kBlockN;
           if (!wait_or_abort(ctl, p, &ctl.v_empty[vs], ((kv_it / VST) & 1) ^ 1)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::TILE_BYTES);
+          ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::VTILE_BYTES);
 #pragma unroll
-          for (int kc = 0; kc < KCH; ++kc)
-            ptx::tma_load_2d(sV + vs * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[vs],
-                             u.h * D + kc * 64, vrow);
+          for (int kc = 0; kc < VCH; ++kc)
+            ptx::tma_load_2d(sV + vs * Cfg::VTILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_v, &ctl.v_full[vs],
+                             u.h * DV + kc * 64, vrow);
           ++kv_it;
         }
         if (!ok) break;
@@ -432,7 +442,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const bool leader = ptx::elect_one_sync();
     {
       constexpr uint32_t idesc_qk = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
-      constexpr uint32_t idesc_pv = ptx::idesc_f16_f32acc(BF16, true, kBlockM, D);
+      constexpr uint32_t idesc_pv = ptx::idesc_f16_f32acc(BF16, true, kBlockM, DV);
       const uint32_t q_base = ptx::smem_u32(sQ);
       const uint32_t k_base = ptx::smem_u32(sK);
       const uint32_t v_base = ptx::smem_u32(sV);
@@ -449,22 +459,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + (si & 1) * 128;
         const uint64_t k_desc = ptx::sdesc_sw128(k_base + st * Cfg::TILE_BYTES, 16, 1024);
-        constexpr int G = D / 16 >= 8 ? 8 : 4;   // k-steps per asm block
+        // k-steps in asm blocks of 8 while 8 remain, then of 4, then single (D = 96: 4 + 2)
+        constexpr int KS = D / 16;
+        auto desc_a = [&](int ks) {
+          return q_desc + static_cast<uint64_t>((qb * Cfg::TILE_BYTES) >> 4) +
+                 static_cast<uint64_t>(((ks >> 2) * Cfg::CHUNK_BYTES + (ks & 3) * 32) >> 4);
+        };
+        auto desc_b = [&](int ks) {
+          return k_desc + static_cast<uint64_t>(((ks >> 2) * Cfg::CHUNK_BYTES + (ks & 3) * 32) >> 4);
+        };
 #pragma unroll
-        for (int g = 0; g < D / 16; g += G) {
-          uint64_t ad[G], bd[G];
+        for (int g = 0; g + 8 <= KS; g += 8) {
+          uint64_t ad[8], bd[8];
 #pragma unroll
-          for (int j = 0; j < G; ++j) {
-            const int ks = g + j;
-            const uint64_t off = static_cast<uint64_t>(((ks >> 2) * Cfg::CHUNK_BYTES + (ks & 3) * 32) >> 4);
-            ad[j] = q_desc + static_cast<uint64_t>((qb * Cfg::TILE_BYTES) >> 4) + off;
-            bd[j] = k_desc + off;
-          }
-          if (leader) {
-            if constexpr (G == 8) ptx::umma_ss_x8(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
-            else ptx::umma_ss_x4(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
-          }
+          for (int j = 0; j < 8; ++j) { ad[j] = desc_a(g + j); bd[j] = desc_b(g + j); }
+          if (leader) ptx::umma_ss_x8(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
         }
+        if constexpr (KS % 8 >= 4) {
+          constexpr int g = KS / 8 * 8;
+          uint64_t ad[4], bd[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) { ad[j] = desc_a(g + j); bd[j] = desc_b(g + j); }
+          if (leader) ptx::umma_ss_x4(d_tmem, ad, bd, idesc_qk, g > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = KS / 4 * 4; ks < KS; ++ks)
+          if (leader) ptx::umma_ss(d_tmem, desc_a(ks), desc_b(ks), idesc_qk, ks > 0 ? 1u : 0u);
         if (leader) {
           ptx::umma_commit(&ctl.k_empty[st]);
           ptx::umma_commit(&ctl.s_full[si & 1]);
@@ -486,7 +506,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tc_fence_after();
         // P of key columns [64 g, 64 g + 64) is packed at S columns [64 g, 64 g + 32);
         // V (MN-major) advances 2048 bytes per step.
-        const uint64_t v_desc = ptx::sdesc_sw128(v_base + st * Cfg::TILE_BYTES, Cfg::CHUNK_BYTES, 1024);
+        const uint64_t v_desc = ptx::sdesc_sw128(v_base + st * Cfg::VTILE_BYTES, Cfg::CHUNK_BYTES, 1024);
         uint32_t pa[8];
         uint64_t vd[8];
 #pragma unroll
@@ -495,7 +515,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           vd[kk] = v_desc + static_cast<uint64_t>((kk * 2048) >> 4);
         }
         if (leader) {
-          ptx::umma_ts_x8(tmem + Cfg::O_COL + ob * D, pa, vd, idesc_pv, first ? 0u : 1u);
+          ptx::umma_ts_x8(tmem + Cfg::O_COL + ob * DV, pa, vd, idesc_pv, first ? 0u : 1u);
           ptx::umma_commit(&ctl.v_empty[st]);
           if constexpr (SOFTMAX) ptx::umma_commit(&ctl.pv_done[si & 1]);
           if (last) ptx::umma_commit(&ctl.o_full[ob]);
@@ -555,7 +575,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue warpgroup
-    // One query row per thread, all D output columns: waits for the unit's last
+    // One query row per thread, all DV output columns: waits for the unit's last
     // P V product, reads O out of TMEM, hands the buffer back, scales and stores.
     const int quarter = warp & 3;
     const int rloc = quarter * 32 + lane;
@@ -575,7 +595,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool valid = row < u.s.Lq;
       const long long grow = static_cast<long long>(u.s.q0) + row;   // global token row
       const int ob = q_it % OB;
-      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * D;
+      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * DV;
       float m_run = -INFINITY, l_run = 0.f;
       if (nt > 0) {
         if (!warp_wait_or_abort(ctl, p, &ctl.o_full[ob], (q_it / OB) & 1)) break;
@@ -590,12 +610,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float mul = u.scale;
       if constexpr (SOFTMAX) mul = l_run > 0.f ? u.scale / l_run : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
         if (nt > 0) {
           ptx::tmem_ld32(o_tmem + c * 32, o);
           ptx::tmem_ld_wait(o);
-          if (c == D / 32 - 1) {   // all of O read: the buffer (and statistics) may be reused
+          if (c == DV / 32 - 1) {   // all of O read: the buffer (and statistics) may be reused
             ptx::tc_fence_before();
             ptx::mbar_arrive(&ctl.o_empty[ob]);
             if constexpr (SOFTMAX) ptx::mbar_arrive(&ctl.rs_empty[ob]);
@@ -606,7 +626,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         if (!valid) continue;
         if (write_part) {
-          float* dst = p.o_part + ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * D + c * 32;
+          float* dst = p.o_part + ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * DV + c * 32;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
@@ -615,7 +635,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
             pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
-          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * D + c * 32;
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * DV + c * 32;
 #pragma unroll
           for (int k = 0; k < 16; k += 4)
             *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
@@ -641,7 +661,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access
     const int rloc = quarter * 32 + lane;    // row within the query tile
     const int c0 = wg * 64;
-    constexpr int DH = D / 2;                // O columns this warpgroup rescales (softmax)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     // alpha/2: a packed bf16 pair (the raw scores are rounded to bf16, whose
     // range is fp32's, before scaling) or an fp32 bit pattern for fp16 (scaled
@@ -669,7 +688,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int r_ctx = u.s.c;
       if (!valid) { r_lo = r_hi = 0; r_diag = -1; r_ctx = 0; }
       const int ob = q_it % OB;
-      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * D + wg * DH;
+      const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * DV;   // softmax rescale:
+                                                                        // 32-column chunks wg, wg+2, ...
 
       float m_run = -INFINITY, l_run = 0.f;   // softmax row state (log2 domain); l over own columns
       bool ok = true;
@@ -750,7 +770,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               ptx::tc_fence_after();
               const float corr = ex2_approx(m_run - mx);
 #pragma unroll 1
-              for (int c = 0; c < DH / 32; ++c) {
+              for (int c = wg; c < DV / 32; c += 2) {
                 uint32_t o[32];
                 ptx::tmem_ld32(o_tmem + c * 32, o);
                 ptx::tmem_ld_wait(o);

@@ -12,6 +12,10 @@ cudaError_t launch_fwd_d64(const CUtensorMap& q, const CUtensorMap& k, const CUt
                            const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
+// hdim_qk 96 with hdim_v 96 or 64
+cudaError_t launch_fwd_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
+                           cudaStream_t stream);
 cudaError_t launch_fwd_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);

@@ -276,25 +276,35 @@ __global__ void __launch_bounds__(256) hstu_combine_kernel(const __grid_constant
       L += w * ml[1];
     }
     const float* src = p.o_part + ((static_cast<long long>(sp) * p.total_q + row) * p.nhead + h) * D + lane * E;
+    if constexpr (E % 2 == 0) {
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 v = *reinterpret_cast<const float2*>(src + e);
-      acc[e] += w * v.x;
-      acc[e + 1] += w * v.y;
+      for (int e = 0; e < E; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src + e);
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += w * src[e];
     }
   }
   float mul = scale;
   if (p.softmax) mul = L > 0.f ? scale / L : 0.f;
-  uint32_t pk[E / 2];
-#pragma unroll
-  for (int e = 0; e < E; e += 2) pk[e / 2] = pack2c<BF16>(acc[e] * mul, acc[e + 1] * mul);
   uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + row * p.o_stride + h * D + lane * E;
-  if constexpr (E == 2) {
-    *reinterpret_cast<uint32_t*>(dst) = pk[0];
-  } else if constexpr (E == 4) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
-  } else {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  if constexpr (E % 2 == 0) {
+    uint32_t pk[E / 2];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) pk[e / 2] = pack2c<BF16>(acc[e] * mul, acc[e + 1] * mul);
+    if constexpr (E == 2) {
+      *reinterpret_cast<uint32_t*>(dst) = pk[0];
+    } else if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+    } else {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  } else {   // hdim_v 96: three elements per lane, stored one by one
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[e] = static_cast<uint16_t>(pack2c<BF16>(acc[e] * mul, 0.f) & 0xFFFFu);
   }
   if (p.softmax && p.lse != nullptr && lane == 0)
     p.lse[static_cast<long long>(h) * p.total_q + row] =
@@ -342,6 +352,7 @@ cudaError_t launch_combine(const CombineParams& p, int hdim, bool bf16, cudaStre
     return cudaGetLastError();                                                      \
   }
   HSTU_COMBINE(64)
+  HSTU_COMBINE(96)
   HSTU_COMBINE(128)
   HSTU_COMBINE(256)
 #undef HSTU_COMBINE

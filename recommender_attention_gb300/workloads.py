@@ -155,14 +155,15 @@ def batched_default() -> Workload:
                     causal=True, dist="normal", seed=1)
 
 
-def large_jagged(hdim: int = 128, batch: int = 64, seed: int = 7) -> Workload:
+def large_jagged(hdim: int = 128, batch: int = 64, seed: int = 7, hdim_v: Optional[int] = None) -> Workload:
     """B=64, nhead=4, bf16, UIH ~ U_int[1024, 4096], targets ~ U_int[1, 32],
     full causal (local 0), context 6, minfull 0, N(0,1), seed 7."""
     rng = np.random.default_rng(seed)
     uih = _draw_ints(rng, 1024, 4096, batch)
     tg = _draw_ints(rng, 1, 32, batch)
-    return Workload(name=f"large_jagged_silu_d{hdim}", batch=batch, nhead=4, hdim_qk=hdim,
-                    hdim_v=hdim, dtype="bf16", uih_q=uih, targets=tg, context_len=[6],
+    dv = hdim if hdim_v is None else hdim_v
+    return Workload(name=f"large_jagged_silu_d{hdim}" + ("" if dv == hdim else f"_{dv}"), batch=batch,
+                    nhead=4, hdim_qk=hdim, hdim_v=dv, dtype="bf16", uih_q=uih, targets=tg, context_len=[6],
                     local_len=[0], minfull_len=[0], causal=True, dist="normal", seed=seed)
 
 
@@ -209,7 +210,8 @@ CONFIGS = {
 
 
 def random_small(seed: int, *, dtype: str = "bf16", hdim: int = 64, softmax: bool = False,
-                 cross: Optional[bool] = None, max_uih: int = 300, kv_targets: bool = False) -> Workload:
+                 cross: Optional[bool] = None, max_uih: int = 300, kv_targets: bool = False,
+                 hdim_v: Optional[int] = None) -> Workload:
     """A small random workload for fuzzing: ragged lengths, random mask parameters.
     kv_targets=True makes it a cross-attention call whose keys end with the
     targets' own keys."""
@@ -227,7 +229,8 @@ def random_small(seed: int, *, dtype: str = "bf16", hdim: int = 64, softmax: boo
     loc = [int(rng.choice([0, 1, 5, 33, 200])) for _ in range(num_groups)]
     mf = [int(rng.choice([0, 3, 17, 150])) for _ in range(num_groups)]
     return Workload(name=f"fuzz{seed}", batch=batch, nhead=int(rng.integers(1, 4)),
-                    hdim_qk=hdim, hdim_v=hdim, dtype=dtype, uih_q=uq, uih_kv=ukv, targets=tg,
+                    hdim_qk=hdim, hdim_v=hdim if hdim_v is None else hdim_v, dtype=dtype,
+                    uih_q=uq, uih_kv=ukv, targets=tg,
                     num_groups=num_groups, context_len=ctx, local_len=loc, minfull_len=mf,
                     max_uih_len=[0] * num_groups,
                     attn_scale=[0.0] * num_groups, alpha=0.0,

@@ -69,6 +69,13 @@ def test_host_validation(lib, field, value, status):
     assert st == status
 
 
+@pytest.mark.parametrize("dqk,dv,status", [(96, 96, 0), (96, 64, 0), (64, 64, 0), (256, 256, 0),
+                                            (96, 128, 2), (128, 64, 2), (64, 96, 2), (32, 32, 2)])
+def test_head_dimension_pairs(lib, dqk, dv, status):
+    st, _ = _ws(lib, _args(hdim_qk=dqk, hdim_v=dv))
+    assert st == status
+
+
 def test_group_array_validation(lib):
     g = (ctypes.c_int32 * 2)(5, -1)
     a = _args(num_groups=2, local_len=ctypes.cast(g, ctypes.c_void_p))

@@ -75,6 +75,44 @@ def test_fuzz_small_parity(seed, softmax):
     check_full(w, num_splits=splits)
 
 
+# ---------------------------------------------------------------- head dimension 96, and 96/64
+@pytest.mark.parametrize("softmax", [False, True])
+@pytest.mark.parametrize("dv", [96, 64])
+def test_hdim96_jagged_parity(softmax, dv):
+    w = W.jagged_readme().with_(hdim_qk=96, hdim_v=dv, softmax=softmax)
+    check_full(w)
+
+
+@pytest.mark.parametrize("softmax", [False, True])
+@pytest.mark.parametrize("dv", [96, 64])
+def test_hdim96_group_cross_splitkv_parity(softmax, dv):
+    w = W.group_cross_splitkv(softmax=softmax, batch=8).with_(hdim_qk=96, hdim_v=dv)
+    check_full(w, num_splits=3)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fuzz_hdim96_parity(seed):
+    w = W.random_small(200 + seed, dtype="bf16" if seed % 2 else "fp16", hdim=96,
+                       hdim_v=[96, 64][seed % 2], softmax=seed % 3 == 1, kv_targets=seed == 5)
+    check_full(w, num_splits=[1, 2, 0][seed % 3])
+
+
+def test_large_jagged_hdim96_sampled_parity():
+    w = W.large_jagged(hdim=96, batch=16)
+    q, k, v = w.tensors()
+    o, _ = gpu_forward(w, q, k, v)
+    off = w.seq_offsets_q()
+    p = oracle_params(w)
+    qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
+    rng = np.random.default_rng(1)
+    for b in rng.choice(w.batch, size=3, replace=False).tolist():
+        L = int(off[b + 1] - off[b])
+        rows = sorted(set([0, 5, 6, 127, 128, L - 1] + rng.integers(0, L, size=16).tolist()))
+        for h in range(w.nhead):
+            ob, _ = hstu_attention_forward_rows(qd, kd, vd, off, None, w.num_targets(), p, b, h, rows)
+            assert_parity(o[off[b] + np.array(rows), h], ob, w.dtype, what=f"b{b} h{h}")
+
+
 # ---------------------------------------------------------------- M-FALCON (keys end with the targets')
 @pytest.mark.parametrize("softmax", [False, True])
 @pytest.mark.parametrize("splits", [1, 3])
