@@ -74,8 +74,8 @@ typedef struct hstu_fwd_args {
   int32_t dtype;          /* hstu_dtype of q, k, v and o (README "Data types": fp16 / bf16) */
   int32_t batch;          /* number of sequences B >= 1 */
   int32_t nhead;          /* heads H >= 1 */
-  int32_t hdim_qk;        /* 64, 128 or 256 */
-  int32_t hdim_v;         /* must equal hdim_qk */
+  int32_t hdim_qk;        /* 64, 96, 128 or 256 (the head sizes the README lists as supported) */
+  int32_t hdim_v;         /* equal to hdim_qk, or 64 with hdim_qk 96 (asymmetric 96/64) */
   int32_t total_q;        /* rows of q and o (tokens of all sequences) */
   int32_t total_kv;       /* rows of k and v; self-attention: == total_q */
   int32_t max_seqlen_q;   /* upper bound of every physical query length; 0 = total_q */
