@@ -117,8 +117,10 @@ Plan make_plan(const hstu_fwd_args* a, int sms) {
   pl.max_seq_q = a->max_seqlen_q > 0 ? a->max_seqlen_q : a->total_q;
   pl.max_seq_kv = a->max_seqlen_kv > 0 ? a->max_seqlen_kv : a->total_kv;
   pl.splits = choose_splits(a, pl.max_seq_q, pl.max_seq_kv, sms);
-  const long long tiles_a = static_cast<long long>(a->batch) * ((pl.max_seq_q + kBlockM - 1) / kBlockM);
-  const long long tiles_b = (static_cast<long long>(a->total_q) + kBlockM - 1) / kBlockM + a->batch;
+  // query tiles per sequence: ceil((L - c) / 128) main tiles plus at most
+  // ceil(c / 128) <= ceil(L / 128) context tiles (see q_layout)
+  const long long tiles_a = static_cast<long long>(a->batch) * (2 * ((pl.max_seq_q + kBlockM - 1) / kBlockM));
+  const long long tiles_b = 2 * ((static_cast<long long>(a->total_q) + kBlockM - 1) / kBlockM) + 2LL * a->batch;
   const long long q_tiles = tiles_a < tiles_b ? tiles_a : tiles_b;
   long long units = q_tiles * a->nhead * pl.splits;
   if (units > (1LL << 30)) units = 1LL << 30;
@@ -142,12 +144,12 @@ Plan make_plan(const hstu_fwd_args* a, int sms) {
 }
 
 bool encode_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_t rows,
-                int64_t row_stride_elems) {
+                int64_t row_stride_elems, uint32_t box_rows = kBlockN) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_elems * 2)};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockN)};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -253,8 +255,9 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   const int D = a->hdim_qk;
   const int64_t wq = static_cast<int64_t>(a->nhead) * D;
   const int64_t wv = static_cast<int64_t>(a->nhead) * a->hdim_v;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tq8;
   if (!encode_map(&tq, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq)) ||
+      !encode_map(&tq8, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq), 8) ||
       !encode_map(&tk, a->k, bf16, wq, a->total_kv, packed_or(a->k_row_stride, wq)) ||
       !encode_map(&tv, a->v, bf16, wv, a->total_kv, packed_or(a->v_row_stride, wv)))
     return HSTU_ERR_CUDA;
@@ -292,10 +295,10 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
       cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_begin), stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
   cudaError_t e;
-  if (D == 64) e = launch_fwd_d64(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
-  else if (D == 96) e = launch_fwd_d96(tq, tk, tv, fp, a->hdim_v, bf16, a->softmax != 0, grid, stream);
-  else if (D == 128) e = launch_fwd_d128(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
-  else e = launch_fwd_d256(tq, tk, tv, fp, bf16, a->softmax != 0, grid, stream);
+  if (D == 64) e = launch_fwd_d64(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
+  else if (D == 96) e = launch_fwd_d96(tq, tk, tv, tq8, fp, a->hdim_v, bf16, a->softmax != 0, grid, stream);
+  else if (D == 128) e = launch_fwd_d128(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
+  else e = launch_fwd_d256(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
   if (e != cudaSuccess) return HSTU_ERR_CUDA;
   if (a->event_fwd_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_end), stream) != cudaSuccess)

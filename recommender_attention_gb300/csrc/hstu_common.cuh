@@ -135,6 +135,71 @@ HSTU_HD TileBounds tile_uih_bounds(const SeqGeom& s, int i0, int i1) {
   return t;
 }
 
+HSTU_HD TileBounds merge_bounds(TileBounds a, const TileBounds& b) {
+  a.LO = a.LO < b.LO ? a.LO : b.LO;
+  a.HI = a.HI > b.HI ? a.HI : b.HI;
+  a.maxLO = a.maxLO > b.maxLO ? a.maxLO : b.maxLO;
+  a.minHI = a.minHI < b.minHI ? a.minHI : b.minHI;
+  return a;
+}
+
+// Query-tile layout of a sequence.  Query tile m holds rows [128 m, 128 m + 128)
+// on lanes 0..127, aligned with the key tiles so a causal diagonal stays within
+// one key tile.  Context rows see every UIH key, so the tile holding them runs
+// all of the sequence's key tiles; when the sequence has more than one query
+// tile and the context rows fit on the spare top lanes of the last tile (from
+// lane 128 - ceil8(c), so each 8-row group is a whole swizzle atom), they move
+// there: that tile already runs every UIH key tile in the common causal case,
+// and tile 0 then runs only its own diagonal.  Lanes [0, c) of tile 0 are then
+// unused.
+struct QLayout {
+  int nq;          // query tiles of the sequence
+  int ctx_lane0;   // >= 0: the context rows sit on lanes [ctx_lane0, ctx_lane0 + c) of tile nq - 1
+};
+HSTU_HD QLayout q_layout(int Lq, int c) {
+  QLayout L;
+  L.nq = (Lq + kBlockM - 1) / kBlockM;
+  L.ctx_lane0 = -1;
+  if (c > 0 && L.nq > 1) {
+    const int cpad = (c + 7) & ~7;
+    const int last_rows = Lq - (L.nq - 1) * kBlockM;
+    if (cpad <= kBlockM - last_rows) L.ctx_lane0 = kBlockM - cpad;
+  }
+  return L;
+}
+HSTU_HD QLayout q_layout(const SeqGeom& s) { return q_layout(s.Lq, s.c); }
+// Row of the sequence on lane r of query tile m, or -1 (an unused lane).
+HSTU_HD int q_row(const SeqGeom& s, const QLayout& L, int m, int r) {
+  if (L.ctx_lane0 >= 0) {
+    if (m == L.nq - 1 && r >= L.ctx_lane0) {
+      const int cr = r - L.ctx_lane0;
+      return cr < s.c ? cr : -1;
+    }
+    if (m == 0 && r < s.c) return -1;   // moved to the last tile
+  }
+  const int v = m * kBlockM + r;
+  return v < s.Lq ? v : -1;
+}
+// The rows of query tile m as up to two runs: [a0, a1) on lanes a0 - 128 m ..,
+// and the moved context rows [c0, c1) (empty unless m is the last tile).
+HSTU_HD void q_tile_runs(const SeqGeom& s, const QLayout& L, int m, int& a0, int& a1, int& c0, int& c1) {
+  a0 = m * kBlockM;
+  a1 = a0 + kBlockM < s.Lq ? a0 + kBlockM : s.Lq;
+  c0 = c1 = 0;
+  if (L.ctx_lane0 >= 0) {
+    if (m == 0) a0 = s.c;
+    if (m == L.nq - 1) c1 = s.c;
+  }
+}
+// tile_uih_bounds over all rows of query tile m.
+HSTU_HD TileBounds q_tile_bounds(const SeqGeom& s, const QLayout& L, int m) {
+  int a0, a1, c0, c1;
+  q_tile_runs(s, L, m, a0, a1, c0, c1);
+  TileBounds b = tile_uih_bounds(s, a0, a1);
+  if (c1 > c0) b = merge_bounds(b, tile_uih_bounds(s, c0, c1));
+  return b;
+}
+
 // Key tiles (of kBlockN keys) a query tile touches, as up to three sorted,
 // disjoint tile-index ranges: the context keys, the UIH hull, the target
 // diagonal.  Empty slots hold [kNoTile, kNoTile).  Written with fixed slots and
@@ -153,16 +218,16 @@ HSTU_HD void tile_range_swap_if(int& alo, int& ahi, int& blo, int& bhi) {
   }
 }
 
-HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, int m) {
-  const int i0 = m * kBlockM;
-  const int i1 = (i0 + kBlockM < s.Lq) ? i0 + kBlockM : s.Lq;
+HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, const QLayout& L, int m) {
+  int i0, i1, c0, c1;   // [i0, i1): the run that may hold target rows
+  q_tile_runs(s, L, m, i0, i1, c0, c1);
   TileSet t;
   t.lo0 = t.hi0 = t.lo1 = t.hi1 = t.lo2 = t.hi2 = kNoTile;
-  if (s.c > 0 && i1 > i0) {
+  if (s.c > 0 && (i1 > i0 || c1 > c0)) {
     t.lo0 = 0;
     t.hi0 = (s.c + kBlockN - 1) / kBlockN;
   }
-  const TileBounds b = tile_uih_bounds(s, i0, i1);
+  const TileBounds b = q_tile_bounds(s, L, m);
   if (b.HI > b.LO) {
     t.lo1 = b.LO / kBlockN;
     t.hi1 = (b.HI + kBlockN - 1) / kBlockN;
@@ -228,9 +293,7 @@ HSTU_HD bool tile_fully_allowed(const SeqGeom& s, const TileBounds& b, int n) {
   const int jlo = j0 > s.c ? j0 : s.c;
   return b.maxLO <= jlo && b.minHI >= j1;
 }
-HSTU_HD bool tile_fully_allowed(const SeqGeom& s, int m, int n) {
-  return tile_fully_allowed(s, tile_uih_bounds(s, m * kBlockM, m * kBlockM + kBlockM), n);
-}
+
 
 // tile_fully_allowed(s, b, n) as index ranges: true exactly when n < ctx_hi
 // (key tiles inside the context prefix) or lo <= n < hi (UIH tiles every row

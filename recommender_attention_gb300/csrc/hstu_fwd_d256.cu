@@ -11,7 +11,7 @@ static_assert(FwdCfg<256, 256, true>::SMEM_BYTES + sizeof(FwdSmemCtl) <= 232448,
 
 namespace {
 template <bool BF16, bool SOFTMAX>
-cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                        const FwdParams& p, int grid, cudaStream_t stream) {
   constexpr int smem = FwdCfg<256, 256, SOFTMAX>::SMEM_BYTES;
   auto kern = hstu_fwd_kernel<256, 256, BF16, SOFTMAX>;
@@ -35,16 +35,16 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, q8, p);
 }
 }  // namespace
 
-cudaError_t launch_fwd_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_fwd_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                            const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream) {
-  if (bf16) return softmax ? launch_one<true, true>(q, k, v, p, grid, stream)
-                           : launch_one<true, false>(q, k, v, p, grid, stream);
-  return softmax ? launch_one<false, true>(q, k, v, p, grid, stream)
-                 : launch_one<false, false>(q, k, v, p, grid, stream);
+  if (bf16) return softmax ? launch_one<true, true>(q, k, v, q8, p, grid, stream)
+                           : launch_one<true, false>(q, k, v, q8, p, grid, stream);
+  return softmax ? launch_one<false, true>(q, k, v, q8, p, grid, stream)
+                 : launch_one<false, false>(q, k, v, q8, p, grid, stream);
 }
 
 }  // namespace hstu

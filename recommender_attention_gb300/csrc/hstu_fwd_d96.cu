@@ -14,7 +14,7 @@ static_assert(FwdCfg<96, 64, true>::SMEM_BYTES + sizeof(FwdSmemCtl) <= 232448, "
 
 namespace {
 template <int DV, bool BF16, bool SOFTMAX>
-cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                        const FwdParams& p, int grid, cudaStream_t stream) {
   constexpr int smem = FwdCfg<96, DV, SOFTMAX>::SMEM_BYTES;
   auto kern = hstu_fwd_kernel<96, DV, BF16, SOFTMAX>;
@@ -38,24 +38,24 @@ cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, q8, p);
 }
 
 template <int DV>
-cudaError_t launch_dv(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_dv(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                       const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream) {
-  if (bf16) return softmax ? launch_one<DV, true, true>(q, k, v, p, grid, stream)
-                           : launch_one<DV, true, false>(q, k, v, p, grid, stream);
-  return softmax ? launch_one<DV, false, true>(q, k, v, p, grid, stream)
-                 : launch_one<DV, false, false>(q, k, v, p, grid, stream);
+  if (bf16) return softmax ? launch_one<DV, true, true>(q, k, v, q8, p, grid, stream)
+                           : launch_one<DV, true, false>(q, k, v, q8, p, grid, stream);
+  return softmax ? launch_one<DV, false, true>(q, k, v, q8, p, grid, stream)
+                 : launch_one<DV, false, false>(q, k, v, q8, p, grid, stream);
 }
 }  // namespace
 
-cudaError_t launch_fwd_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+cudaError_t launch_fwd_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                            const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
                            cudaStream_t stream) {
-  if (hdim_v == 96) return launch_dv<96>(q, k, v, p, bf16, softmax, grid, stream);
-  if (hdim_v == 64) return launch_dv<64>(q, k, v, p, bf16, softmax, grid, stream);
+  if (hdim_v == 96) return launch_dv<96>(q, k, v, q8, p, bf16, softmax, grid, stream);
+  if (hdim_v == 64) return launch_dv<64>(q, k, v, q8, p, bf16, softmax, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -131,6 +131,7 @@ struct RowMask {
 
 struct UnitView {
   SeqGeom s;
+  QLayout L;     // the sequence's query-tile layout (which rows tile m holds)
   TileSet ts;
   TileBounds tb;
   int m, h, g, sp, k0, k1;
@@ -147,8 +148,9 @@ __device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
   u.g = b / p.batch_per_group;
   u.s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[u.g], p.loc[u.g], p.mf[u.g], p.causal,
                   p.self_attn, p.kv_targets);
-  u.ts = query_tile_kv_tiles(u.s, u.m);
-  u.tb = tile_uih_bounds(u.s, u.m * kBlockM, u.m * kBlockM + kBlockM);
+  u.L = q_layout(u.s);
+  u.ts = query_tile_kv_tiles(u.s, u.L, u.m);
+  u.tb = q_tile_bounds(u.s, u.L, u.m);
   split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);
   u.scale = p.group_scale[u.g];
   return u;
@@ -238,7 +240,8 @@ __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tm
 template <int D, int DV, bool BF16, bool SOFTMAX>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q8,
+                    const __grid_constant__ FwdParams p) {
   using Cfg = FwdCfg<D, DV, SOFTMAX>;
   constexpr int KCH = Cfg::KCH;
   constexpr int VCH = Cfg::VCH;
@@ -350,11 +353,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const int qb = q_it % QB;
           if (!wait_or_abort(ctl, p, &ctl.q_empty[qb], ((q_it / QB) & 1) ^ 1)) break;
           ptx::mbar_arrive_expect_tx(&ctl.q_full[qb], Cfg::TILE_BYTES);
-          const int qrow = cur.s.q0 + cur.m * kBlockM;
+          const int qrow = cur.m * kBlockM;   // the tile's rows, lane r = row qrow + r
+          uint8_t* qdst = sQ + qb * Cfg::TILE_BYTES;
+          if (!(cur.L.ctx_lane0 >= 0 && cur.m == cur.L.nq - 1)) {   // one 128-row box per chunk
 #pragma unroll
-          for (int kc = 0; kc < KCH; ++kc)
-            ptx::tma_load_2d(sQ + qb * Cfg::TILE_BYTES + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full[qb],
-                             cur.h * D + kc * 64, qrow);
+            for (int kc = 0; kc < KCH; ++kc)
+              ptx::tma_load_2d(qdst + kc * Cfg::CHUNK_BYTES, &tm_q, &ctl.q_full[qb], cur.h * D + kc * 64,
+                               cur.s.q0 + qrow);
+          } else {
+            // the tile's own rows on lanes [0, ctx_lane0), the context rows on
+            // lanes [ctx_lane0, 128): 8-row boxes (one swizzle atom each), 16 per chunk
+            const int lane0 = cur.L.ctx_lane0;
+            for (int g = 0; g < kBlockM / 8; ++g) {
+              const int row = g * 8 < lane0 ? qrow + g * 8 : (g * 8 - lane0);
+#pragma unroll
+              for (int kc = 0; kc < KCH; ++kc)
+                ptx::tma_load_2d(qdst + kc * Cfg::CHUNK_BYTES + g * 1024, &tm_q8, &ctl.q_full[qb],
+                                 cur.h * D + kc * 64, cur.s.q0 + row);
+            }
+          }
           ++q_it;
           const int k_ahead = cur.k1 - 3 > cur.k0 ? cur.k1 - 3 : cur.k0;
           for (int k = cur.k0; k < cur.k1 && ok; ++k) {
@@ -591,8 +608,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ++sched_it;
       if (!live) break;
       const int nt = u.k1 - u.k0;
-      const int row = u.m * kBlockM + rloc;
-      const bool valid = row < u.s.Lq;
+      const int qr = q_row(u.s, u.L, u.m, rloc);   // this lane's row of the sequence, or -1
+      const bool valid = qr >= 0;
+      const int row = valid ? qr : 0;
       const long long grow = static_cast<long long>(u.s.q0) + row;   // global token row
       const int ob = q_it % OB;
       const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * DV;
@@ -680,10 +698,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ++sched_it;
       if (!live) break;
       const int nt = u.k1 - u.k0;
-      const int row = u.m * kBlockM + rloc;
-      const bool valid = row < u.s.Lq;
+      const int qr = q_row(u.s, u.L, u.m, rloc);   // this lane's row of the sequence, or -1
+      const bool valid = qr >= 0;
+      const int row = valid ? qr : 0;
       int r_lo, r_hi;
-      row_uih_keys(u.s, valid ? row : 0, r_lo, r_hi);
+      row_uih_keys(u.s, row, r_lo, r_hi);
       int r_diag = row_diag_key(u.s, row);
       int r_ctx = u.s.c;
       if (!valid) { r_lo = r_hi = 0; r_diag = -1; r_ctx = 0; }

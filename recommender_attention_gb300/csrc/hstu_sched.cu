@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     if (q1 - q0 > p.max_seqlen_q || Lkv > p.max_seqlen_kv) err |= kErrMaxSeqlen;
     if (err) atomicOr(&s_err, err);
     else atomicMax(&s_gmax[g], q1 - q0 - c - t);
-    tbase[b] = err ? 0 : (q1 - q0 + kBlockM - 1) / kBlockM;
+    tbase[b] = err ? 0 : q_layout(q1 - q0, c).nq;
     cost[b] = 0;
   }
   __syncthreads();
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     const int g = b / p.batch_per_group;
     const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[g], p.loc[g], p.mf[g], p.causal,
                                 p.self_attn, p.kv_targets);
-    const int cnt = query_tile_kv_tiles(s, i - tbase[b]).count;
+    const int cnt = query_tile_kv_tiles(s, q_layout(s), i - tbase[b]).count;
     atomicAdd(&cost[b], cnt);
     tiles += cnt;
   }
@@ -180,11 +180,10 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     return;
   }
 
-  // 4. units: per sequence, heads outer, splits innermost.  Query tiles go
-  //    largest first: the tiles holding context rows (those rows see every
-  //    key, so these tiles run all key tiles), then the rest from the last
-  //    (most key tiles under a causal mask) down.  The queue then ends on the
-  //    smallest units, which keeps the persistent CTAs' finish times close.
+  // 4. units: per sequence, heads outer, splits innermost, query tiles from
+  //    the last down: the tiles holding context rows (which see every key)
+  //    come last in the layout, and under a causal mask later tiles run more
+  //    key tiles, so the queue ends on the smallest units.
   for (int u = tid; u < total; u += nth) {
     const int pos = find_segment(ubase, B, u);
     const int b = order[pos];
@@ -193,10 +192,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     const int local = u - ubase[pos];
     const int h = local / per_h;
     const int rem = local - h * per_h;
-    const int c = p.ctx[b / p.batch_per_group];
-    const int mc = min(nq, (c + kBlockM - 1) / kBlockM);
-    const int r = rem / p.splits;
-    const int m = r < mc ? r : nq - 1 - (r - mc);
+    const int m = nq - 1 - rem / p.splits;
     p.units[u] = make_int4(b, m, h, rem % p.splits);
   }
 

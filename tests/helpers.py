@@ -36,3 +36,34 @@ def read_mask_fixture(path):
         elif line and not line.startswith("#"):
             rows.append([ch == "X" for ch in line])
     return params, np.array(rows, dtype=bool)
+
+
+def kernel_query_tiles(L_q: int, c: int):
+    """Rows (within a sequence) of each query tile the forward kernel runs.
+
+    Its layout: tile m holds rows [128 m, 128 m + 128); when there is more than
+    one tile and ceil(c/8)*8 lanes are free at the top of the last tile, the c
+    context rows (which see every UIH key) move from tile 0 to the last tile."""
+    nq = -(-L_q // 128)
+    tiles = [list(range(128 * m, min(128 * m + 128, L_q))) for m in range(nq)]
+    if c > 0 and nq > 1 and -(-c // 8) * 8 <= 128 - (L_q - 128 * (nq - 1)):
+        tiles[0] = [r for r in tiles[0] if r >= c]
+        tiles[-1] += list(range(c))
+    return tiles
+
+
+def kernel_executed_tiles(w) -> int:
+    """(b, h, query tile, 128-key tile) blocks of the kernel's layout that hold at
+    least one allowed entry of the oracle's dense mask."""
+    from oracle.hstu_oracle import _seq_params, dense_mask
+    p = oracle_params(w)
+    off_q, off_kv, tg = w.seq_offsets_q(), w.seq_offsets_kv(), w.num_targets()
+    total = 0
+    for b in range(w.batch):
+        _, sp = _seq_params(p, b, w.batch, off_q, off_kv, tg)
+        mask = dense_mask(sp)
+        nk = -(-sp.L_kv // 128)
+        for rows in kernel_query_tiles(sp.L_q, sp.context):
+            blk = mask[rows]
+            total += sum(1 for n in range(nk) if blk[:, 128 * n:128 * n + 128].any())
+    return total * w.nhead

@@ -6,11 +6,11 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.hstu_oracle import (allowed_pair_count, executed_tile_count,
+from oracle.hstu_oracle import (allowed_pair_count,
                                 hstu_attention_forward_rows)
 from recommender_attention_gb300 import workloads as W
 from tests.gpu_helpers import assert_parity, gpu_call, gpu_forward
-from tests.helpers import as_f64, oracle_forward, oracle_params
+from tests.helpers import as_f64, kernel_executed_tiles, oracle_forward, oracle_params
 
 pytestmark = pytest.mark.gpu
 
@@ -197,7 +197,7 @@ def test_tile_skip_and_pair_accounting(cfg):
     stats = gpu_call(w, q, k, v).stats()
     p = oracle_params(w)
     args = (w.seq_offsets_q(), w.seq_offsets_kv(), w.num_targets(), p, w.nhead)
-    assert stats["executed_tiles"] == executed_tile_count(*args)
+    assert stats["executed_tiles"] == kernel_executed_tiles(w)
     assert stats["allowed_pairs"] == allowed_pair_count(*args)
     assert stats["device_error"] == 0
 
@@ -209,7 +209,7 @@ def test_tile_skip_accounting_fuzz(seed):
     stats = gpu_call(w, q, k, v, num_splits=1).stats()
     p = oracle_params(w)
     args = (w.seq_offsets_q(), w.seq_offsets_kv(), w.num_targets(), p, w.nhead)
-    assert stats["executed_tiles"] == executed_tile_count(*args)
+    assert stats["executed_tiles"] == kernel_executed_tiles(w)
     assert stats["allowed_pairs"] == allowed_pair_count(*args)
 
 
