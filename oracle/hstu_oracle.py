@@ -48,6 +48,10 @@ used (each one a named constant or a commented branch):
     the batch's group; a group whose largest UIH length is 0 uses 1.0.
   * groups are consecutive blocks of batch/num_groups batches.
 
+The backward (``hstu_attention_backward``) is the exact gradient of that
+forward (the README's training mode keeps the softmax LSE for it); it is
+pinned against central finite differences of the forward.
+
 Parity of every function here is pinned by ``tests/test_oracle.py``.
 """
 from __future__ import annotations
@@ -344,3 +348,75 @@ def executed_tile_count(seq_offsets_q, seq_offsets_kv, num_targets, params: Hstu
                 if blk[:, c * block_n:(c + 1) * block_n].any():
                     total += 1
     return total * nhead
+
+
+# ----------------------------------------------------------------------------
+# Backward (the gradients of the forward above; the README's training mode saves
+# the softmax LSE for it)
+# ----------------------------------------------------------------------------
+def silu_grad(s: np.ndarray) -> np.ndarray:
+    """d/ds SiLU(s) = sigma(s) * (1 + s * (1 - sigma(s))), elementwise, fp64."""
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-s))
+    return sig * (1.0 + s * (1.0 - sig))
+
+
+def _head_backward(q, k, v, g, allowed, alpha, attn_scale, softmax):
+    """One (sequence, head): the gradients of _head_forward's o with respect to q,
+    k and v for the output gradient g [n, Dv].
+
+    SiLU:    o = c * (M . SiLU(s)) v,            s = alpha q k^T
+             dv = c a^T g,  da = c g v^T,  ds = M . da . SiLU'(s)
+    softmax: o = c * p v,   p = M . exp(s - lse) (row-normalised over allowed keys)
+             dv = c p^T g,  dp = c g v^T,  ds = p . (dp - rowsum(p . dp))
+    both:    dq = alpha ds k,  dk = alpha ds^T q."""
+    s = alpha * (q @ k.T)
+    if not softmax:
+        a = np.where(allowed, silu(s), 0.0)
+        dv = attn_scale * (a.T @ g)
+        da = attn_scale * (g @ v.T)
+        ds = np.where(allowed, da * silu_grad(s), 0.0)
+    else:
+        masked = np.where(allowed, s, -np.inf)
+        m = masked.max(axis=1) if masked.shape[1] else np.full(masked.shape[0], -np.inf)
+        has_key = np.isfinite(m)
+        m_safe = np.where(has_key, m, 0.0)
+        e = np.where(allowed, np.exp(s - m_safe[:, None]), 0.0)
+        l = e.sum(axis=1)
+        p = e / np.where(has_key, l, 1.0)[:, None]
+        dv = attn_scale * (p.T @ g)
+        dp = attn_scale * (g @ v.T)
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+    return alpha * (ds @ k), alpha * (ds.T @ q), dv
+
+
+def hstu_attention_backward(q, k, v, d_o, seq_offsets_q, seq_offsets_kv, num_targets,
+                            params: HstuParams):
+    """Gradients (dq, dk, dv) of the full forward for the output gradient d_o
+    [total_q, H, Dv], in float64.  Rows outside every sequence get zero."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    d_o = np.asarray(d_o, dtype=np.float64)
+    off_q = np.asarray(seq_offsets_q, dtype=np.int64)
+    off_kv = None if seq_offsets_kv is None else np.asarray(seq_offsets_kv, dtype=np.int64)
+    batch = off_q.shape[0] - 1
+    H = q.shape[1]
+    alpha = resolved_alpha(params, q.shape[2])
+    scales = resolved_attn_scales(params, batch, off_q, num_targets)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(batch):
+        g_, sp = _seq_params(params, b, batch, off_q, off_kv, num_targets)
+        allowed = dense_mask(sp)
+        q0 = off_q[b]
+        kv0 = off_kv[b] if off_kv is not None else q0
+        for h in range(H):
+            a, bk, c = _head_backward(q[q0:q0 + sp.L_q, h], k[kv0:kv0 + sp.L_kv, h],
+                                      v[kv0:kv0 + sp.L_kv, h], d_o[q0:q0 + sp.L_q, h], allowed,
+                                      alpha, scales[g_], params.softmax)
+            dq[q0:q0 + sp.L_q, h] += a
+            dk[kv0:kv0 + sp.L_kv, h] += bk
+            dv[kv0:kv0 + sp.L_kv, h] += c
+    return dq, dk, dv

@@ -335,6 +335,78 @@ def test_mfalcon_candidates_see_only_their_own_key():
         assert m[c:, c:c + u_kv].all()            # causal: candidates sit after the whole history
 
 
+def _fd_case(rng, softmax, cross=False, kv_targets=False):
+    """A tiny random call; returns (args, params) for the forward and backward."""
+    B, H, D, Dv = 2, 2, 6, 5
+    c = int(rng.choice([0, 2]))
+    u = [int(x) for x in rng.integers(3, 12, size=B)]
+    t = [int(x) for x in rng.integers(0, 4, size=B)]
+    Lq = [c + u[b] + t[b] for b in range(B)]
+    if cross:
+        ukv = [int(x) for x in rng.integers(2, 14, size=B)]
+        Lkv = [c + ukv[b] + (t[b] if kv_targets else 0) for b in range(B)]
+    else:
+        Lkv = Lq
+    off_q = np.concatenate([[0], np.cumsum(Lq)])
+    off_kv = np.concatenate([[0], np.cumsum(Lkv)]) if cross else None
+    q = rng.standard_normal((off_q[-1], H, D))
+    k = rng.standard_normal((int(np.sum(Lkv)), H, D))
+    v = rng.standard_normal((int(np.sum(Lkv)), H, Dv))
+    g = rng.standard_normal((off_q[-1], H, Dv))
+    p = HstuParams(context_len=[c], local_len=[int(rng.choice([0, 2, 5]))],
+                   minfull_len=[int(rng.choice([0, 3]))], attn_scale=[0.3], alpha=0.7,
+                   causal=bool(rng.integers(0, 2)), softmax=softmax, kv_targets=kv_targets)
+    return q, k, v, g, off_q, off_kv, np.array(t), p
+
+
+def _fd_check(q, k, v, g, off_q, off_kv, t, p, rng):
+    dq, dk, dv = orc.hstu_attention_backward(q, k, v, g, off_q, off_kv, t, p)
+
+    def loss(qq, kk, vv):
+        o, _ = hstu_attention_forward(qq, kk, vv, off_q, off_kv, t, p)
+        return float((o * g).sum())
+
+    eps = 1e-6
+    for grad, which in ((dq, 0), (dk, 1), (dv, 2)):
+        for _ in range(3):
+            d = rng.standard_normal(grad.shape)
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which] = args_p[which] + eps * d
+            args_m[which] = args_m[which] - eps * d
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            an = float((grad * d).sum())
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (which, fd, an)
+
+
+def test_backward_matches_finite_differences():
+    """The backward is the gradient of the (separately pinned) forward: each of
+    dq, dk, dv against central differences of the forward along random
+    directions, over random masks (targets, windows, min-full, cross, M-FALCON
+    keys), in SiLU and softmax mode."""
+    rng = np.random.default_rng(11)
+    for softmax in (False, True):
+        for cross, kvt in ((False, False), (True, False), (True, True)):
+            for _ in range(4):
+                _fd_check(*_fd_case(rng, softmax, cross, kvt), rng)
+
+
+def test_backward_silu_grad_closed_form():
+    s = np.linspace(-12, 12, 97)
+    h = 1e-6
+    fd = (orc.silu(s + h) - orc.silu(s - h)) / (2 * h)
+    np.testing.assert_allclose(orc.silu_grad(s), fd, rtol=1e-7, atol=1e-9)
+    assert orc.silu_grad(np.array([0.0]))[0] == 0.5
+
+
+def _backward_pin_passes():
+    try:
+        test_backward_matches_finite_differences()
+    except AssertionError:
+        return False
+    return True
+
+
 def _mfalcon_pin_passes():
     try:
         test_mfalcon_equals_target_rows_of_full_sequence()
@@ -384,4 +456,9 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(orc, "mask_rows", candidates_see_each_other)
     assert not _mfalcon_pin_passes()
     monkeypatch.undo()
-    assert _pins_pass() and _mfalcon_pin_passes()
+    # 6. a backward that drops the s (1 - sigma) term of the SiLU derivative
+    assert _backward_pin_passes()
+    monkeypatch.setattr(orc, "silu_grad", lambda s: 1.0 / (1.0 + np.exp(-s)))
+    assert not _backward_pin_passes()
+    monkeypatch.undo()
+    assert _pins_pass() and _mfalcon_pin_passes() and _backward_pin_passes()
