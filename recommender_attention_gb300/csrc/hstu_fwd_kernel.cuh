@@ -565,7 +565,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++sched_it;
         if (!live) break;
         const int nt = u.k1 - u.k0;
-        if (nt <= 0) continue;
+        if (nt <= 0) {
+          // An empty split unit: issue the pending P V now.  Holding it across
+          // empty units would stall the epilogue on that unit's O, and with
+          // it the scheduler ring this loop is waiting on.
+          if (!flush()) { ok = false; break; }
+          continue;
+        }
         if (QB == 1 && !flush()) { ok = false; break; }
         const int ob = q_it % OB;
         const int qb = q_it % QB;
@@ -642,13 +648,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = 0u;
         }
-        if (!valid) continue;
-        if (write_part) {
+        // unused lanes store nothing (a branch, not a `continue`: the warp stays
+        // converged for the next collective TMEM load)
+        if (valid && write_part) {
           float* dst = p.o_part + ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * DV + c * 32;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-        } else {
+        } else if (valid) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
@@ -779,28 +786,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (si >= 2) {
             if (!warp_wait_or_abort(ctl, p, &ctl.pv_done[si & 1], ((si - 2) >> 1) & 1)) { ok = false; break; }
           }
-          if (mx > m_run + 8.0f) {
-            // New running max; rescale what O already holds (only after a previous
-            // tile of this unit, whose PV must have completed).  Both warpgroups take
-            // the same decision from the same maxima.
-            if (idx > 0 && m_run != -INFINITY) {
-              const int sp = si - 1;
-              if (!warp_wait_or_abort(ctl, p, &ctl.pv_done[sp & 1], (sp >> 1) & 1)) { ok = false; break; }
-              ptx::tc_fence_after();
-              const float corr = ex2_approx(m_run - mx);
+          // A new running max more than 2^8 above the old one: rescale what O
+          // already holds (only after a previous tile of this unit, whose PV
+          // must have completed).  The need is per row, but the wait and the
+          // TMEM accesses are warp-collective, so a warp rescales when any of
+          // its rows needs it and the other rows multiply by 1.  Both
+          // warpgroups see the same maxima, so the same warps of each take
+          // the branch.
+          const bool grow = mx > m_run + 8.0f;
+          const bool rescale = grow && idx > 0 && m_run != -INFINITY;
+          if (__any_sync(0xffffffffu, rescale)) {
+            const int sp = si - 1;
+            if (!warp_wait_or_abort(ctl, p, &ctl.pv_done[sp & 1], (sp >> 1) & 1)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const float corr = rescale ? ex2_approx(m_run - mx) : 1.0f;
 #pragma unroll 1
-              for (int c = wg; c < DV / 32; c += 2) {
-                uint32_t o[32];
-                ptx::tmem_ld32(o_tmem + c * 32, o);
-                ptx::tmem_ld_wait(o);
+            for (int c = wg; c < DV / 32; c += 2) {
+              uint32_t o[32];
+              ptx::tmem_ld32(o_tmem + c * 32, o);
+              ptx::tmem_ld_wait(o);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
-                ptx::tmem_st32(o_tmem + c * 32, o);
-              }
-              l_run *= corr;
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+              ptx::tmem_st32(o_tmem + c * 32, o);
             }
-            m_run = mx;
+            l_run *= corr;
           }
+          if (grow) m_run = mx;
           const float nm = m_run == -INFINITY ? 0.f : -m_run;
           float lsum0 = 0.f, lsum1 = 0.f;
           uint32_t pk[32];

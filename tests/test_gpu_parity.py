@@ -43,6 +43,37 @@ def test_group_cross_splitkv_parity(softmax, splits):
     check_full(w, num_splits=splits)
 
 
+def test_softmax_rescale_in_some_rows_of_a_warp():
+    """Softmax rows whose running max jumps by far more than 2^8 on the second
+    key tile next to rows whose max stays put, in every warp: the kernel's O
+    rescale is needed by some rows of a warp and not by the others.  Keys of
+    tile 0 are zero (every score 0); keys of tile 1 are large; odd query rows
+    are large, even rows zero."""
+    w = W.Workload(name="rescale_mix", batch=1, nhead=2, hdim_qk=64, hdim_v=64, dtype="bf16",
+                   uih_q=[256], targets=[0], context_len=[0], causal=False, softmax=True,
+                   alpha=1.0 / 8, seed=17)
+    rng = np.random.default_rng([17, 5])
+    q = rng.standard_normal((256, 2, 64)).astype(np.float32) * 4
+    q[0::2] = 0.0
+    k = rng.standard_normal((256, 2, 64)).astype(np.float32) * 4
+    k[:128] = 0.0
+    v = rng.standard_normal((256, 2, 64)).astype(np.float32)
+    q, k, v = (torch.from_numpy(x).to(torch.bfloat16) for x in (q, k, v))
+    o, lse = gpu_forward(w, q, k, v)
+    o_ref, lse_ref = oracle_forward(w, q, k, v)
+    assert_parity(o, o_ref, w.dtype, lse, lse_ref, what=w.name)
+
+
+@pytest.mark.parametrize("softmax", [False, True])
+@pytest.mark.parametrize("splits", [0, 5, 16])
+def test_splitkv_runs_of_empty_split_units(softmax, splits):
+    """Local-window groups give query tiles of 2-3 key tiles: with 5 or 16
+    splits (and the automatic choice on 8 sequences, 5) most of their split
+    units are empty, several in a row, between non-empty ones."""
+    w = W.group_cross_splitkv(softmax=softmax, batch=8)
+    check_full(w, num_splits=splits)
+
+
 @pytest.mark.parametrize("hdim", [128, 256])
 def test_large_jagged_sampled_parity(hdim):
     """Full-size large jagged workload, same launch as the bench; oracle on sampled rows."""
