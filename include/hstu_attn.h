@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define HSTU_ABI_VERSION 2
+#define HSTU_ABI_VERSION 3
 #define HSTU_MAX_GROUPS 256
 #define HSTU_MAX_SPLITS 16
 
@@ -187,6 +187,56 @@ size_t hstu_fwd_args_size(void);
  */
 hstu_status hstu_selftest_wait_timeout(int32_t* result_dev, uint64_t timeout_ns, void* stream,
                                        int32_t* timed_out);
+
+/*
+ * Arguments of one backward call (the gradients of the forward above): the
+ * forward call's own arguments plus the output gradient and the three input
+ * gradients, all [dev] and 16-byte aligned, in the storage type of q.
+ */
+typedef struct hstu_bwd_args {
+  /* The forward call's arguments.  Read: every shape, mask, group and scale
+   * field, alpha, q, k, v, the offsets and num_targets; softmax mode also reads
+   * o and lse as the forward wrote them.  fwd.workspace / fwd.workspace_bytes
+   * hold the backward's own workspace (hstu_attn_bwd_workspace_size);
+   * num_splits and the two events are ignored. */
+  hstu_fwd_args fwd;
+  const void* d_o;        /* [dev] [total_q, H, hdim_v] gradient of the loss with respect to o */
+  void* dq;               /* [dev] [total_q, H, hdim_qk] written: gradient with respect to q */
+  void* dk;               /* [dev] [total_kv, H, hdim_qk] written: gradient with respect to k */
+  void* dv;               /* [dev] [total_kv, H, hdim_v] written: gradient with respect to v */
+  /* Elements between consecutive tokens; 0 = packed (nhead * hdim).  Row
+   * strides * 2 bytes must be multiples of 16. */
+  int64_t do_row_stride, dq_row_stride, dk_row_stride, dv_row_stride;
+} hstu_bwd_args;
+
+/* sizeof(hstu_bwd_args) as compiled into the library (binding layout check). */
+size_t hstu_bwd_args_size(void);
+
+/*
+ * Workspace bytes of a backward call (pointer fields are not read).
+ * Synchronous, host only; same argument errors as hstu_attn_bwd.
+ */
+hstu_status hstu_attn_bwd_workspace_size(const hstu_bwd_args* args, size_t* bytes);
+
+/*
+ * The backward of the forward (the exact derivative of "Forward computation";
+ * the README's training mode keeps the softmax LSE for it).  With
+ * s = alpha q k^T on the allowed entries, c = attn_scale of the group and
+ * g = d_o, per sequence and head:
+ *   SiLU:    a = SiLU(s) masked       dv = c a^T g,  ds = (c g v^T) . SiLU'(s) masked
+ *   softmax: p = exp(s - lse) masked  dv = c p^T g,  ds = p . (c g v^T - rowsum(g . o))
+ *   both:    dq = alpha ds k,  dk = alpha ds^T q
+ * Head dimensions: hdim_qk == hdim_v, 64 or 128 (others HSTU_ERR_UNSUPPORTED).
+ * Launches on `stream` the scheduler, in softmax mode a row-sum kernel, then
+ * one persistent tcgen05 kernel per query tile (dq) and one per key tile (dk,
+ * dv); returns without synchronising.  Every row of every sequence gets its
+ * gradient (0 where the mask allows nothing); rows outside every sequence are
+ * left untouched.  Host-checkable errors return before any launch and write
+ * nothing; data-dependent errors set the device error word in the workspace,
+ * read back by hstu_attn_fwd_check(args->fwd.workspace, ...).  Not thread-safe
+ * against concurrent calls sharing one workspace.
+ */
+hstu_status hstu_attn_bwd(const hstu_bwd_args* args, void* stream);
 
 /* Size of the library's fixed scratch used by hstu_attn_fwd_static_ws. */
 #define HSTU_STATIC_WS_BYTES (4u << 20)

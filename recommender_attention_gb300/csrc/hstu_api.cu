@@ -1,5 +1,6 @@
-// C ABI of the HSTU forward: argument validation, workspace planning, TMA
-// tensor-map encoding and the launches (scheduler -> forward -> combine).
+// C ABI of the HSTU forward and backward: argument validation, workspace
+// planning, TMA tensor-map encoding and the launches (scheduler -> forward ->
+// combine; scheduler -> row sums -> dQ -> dK/dV).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -129,7 +130,7 @@ Plan make_plan(const hstu_fwd_args* a, int sms) {
   pl.off_scale = off;
   off = align256(off + kMaxGroups * sizeof(float));
   pl.off_scratch = off;
-  off = align256(off + (4ull * a->batch + 2) * sizeof(int));
+  off = align256(off + (5ull * a->batch + 3) * sizeof(int));
   pl.off_units = off;
   off = align256(off + static_cast<size_t>(pl.max_units) * sizeof(int4));
   pl.off_opart = pl.off_mlpart = 0;
@@ -198,6 +199,62 @@ PrepParams make_prep(const hstu_fwd_args* a, const Plan& pl) {
     pp.attn_scale[g] = (in && a->attn_scale) ? a->attn_scale[g] : 0.f;
   }
   return pp;
+}
+
+// ---------------------------------------------------------------- backward
+// The forward's layout with one split (header, group scales, batch scratch,
+// query-tile units), then the query-tile records, the key-tile units and, in
+// softmax mode, the row sums delta [H, total_q].
+struct BwdPlan {
+  Plan fwd;
+  int q_tiles, max_kv_units;
+  size_t off_qbase, off_qtiles, off_kvunits, off_delta, total;
+};
+
+hstu_fwd_args bwd_fwd_view(const hstu_bwd_args* a) {
+  hstu_fwd_args f = a->fwd;
+  f.num_splits = 1;
+  return f;
+}
+
+hstu_status validate_bwd(const hstu_bwd_args* a) {
+  if (!a) return HSTU_ERR_INVALID_ARG;
+  const hstu_fwd_args f = bwd_fwd_view(a);
+  const hstu_status st = validate(&f);
+  if (st != HSTU_OK) return st;
+  if (f.hdim_v != f.hdim_qk || (f.hdim_qk != 64 && f.hdim_qk != 128)) return HSTU_ERR_UNSUPPORTED;
+  const int64_t w = static_cast<int64_t>(f.nhead) * f.hdim_qk;
+  const int64_t strides[4] = {packed_or(a->do_row_stride, w), packed_or(a->dq_row_stride, w),
+                              packed_or(a->dk_row_stride, w), packed_or(a->dv_row_stride, w)};
+  for (int64_t x : strides)
+    if (x < w || (x * 2) % 16) return HSTU_ERR_INVALID_ARG;
+  return HSTU_OK;
+}
+
+BwdPlan make_bwd_plan(const hstu_bwd_args* a, int sms) {
+  const hstu_fwd_args f = bwd_fwd_view(a);
+  BwdPlan bp{};
+  bp.fwd = make_plan(&f, sms);
+  bp.q_tiles = bp.fwd.max_units / f.nhead;
+  const long long kv_a = static_cast<long long>(f.batch) * ((bp.fwd.max_seq_kv + kBlockN - 1) / kBlockN);
+  const long long kv_b = (static_cast<long long>(f.total_kv) + kBlockN - 1) / kBlockN + f.batch;
+  long long kv_units = (kv_a < kv_b ? kv_a : kv_b) * f.nhead;
+  if (kv_units > (1LL << 30)) kv_units = 1LL << 30;
+  bp.max_kv_units = static_cast<int>(kv_units);
+  size_t off = bp.fwd.total;
+  bp.off_qbase = off;
+  off = align256(off + (static_cast<size_t>(f.batch) + 1) * sizeof(int));
+  bp.off_qtiles = off;
+  off = align256(off + static_cast<size_t>(bp.q_tiles) * kQTileInts * sizeof(int));
+  bp.off_kvunits = off;
+  off = align256(off + static_cast<size_t>(bp.max_kv_units) * sizeof(int4));
+  bp.off_delta = 0;
+  if (f.softmax) {
+    bp.off_delta = off;
+    off = align256(off + static_cast<size_t>(f.nhead) * f.total_q * sizeof(float));
+  }
+  bp.total = off;
+  return bp;
 }
 
 }  // namespace
@@ -367,6 +424,96 @@ hstu_status hstu_attn_fwd_stats(const hstu_fwd_args* a, void* stream_ptr, hstu_f
   out->device_error = hdr[kWsError];
   out->reserved = 0;
   return hdr[kWsError] ? HSTU_ERR_DEVICE : HSTU_OK;
+}
+
+size_t hstu_bwd_args_size(void) { return sizeof(hstu_bwd_args); }
+
+hstu_status hstu_attn_bwd_workspace_size(const hstu_bwd_args* a, size_t* bytes) {
+  if (!bytes) return HSTU_ERR_INVALID_ARG;
+  const hstu_status st = validate_bwd(a);
+  if (st != HSTU_OK) return st;
+  *bytes = make_bwd_plan(a, sm_count_current()).total;
+  return HSTU_OK;
+}
+
+hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
+  hstu_status st = validate_bwd(a);
+  if (st != HSTU_OK) return st;
+  const hstu_fwd_args f = bwd_fwd_view(a);
+  if (!f.q || !f.k || !f.v || !f.seq_offsets_q || !a->d_o || !a->dq || !a->dk || !a->dv)
+    return HSTU_ERR_INVALID_ARG;
+  if (f.softmax && (!f.o || !f.lse)) return HSTU_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(f.q) | reinterpret_cast<uintptr_t>(f.k) |
+                        reinterpret_cast<uintptr_t>(f.v) | reinterpret_cast<uintptr_t>(f.o) |
+                        reinterpret_cast<uintptr_t>(a->d_o) | reinterpret_cast<uintptr_t>(a->dq) |
+                        reinterpret_cast<uintptr_t>(a->dk) | reinterpret_cast<uintptr_t>(a->dv);
+  if (mis & 15) return HSTU_ERR_INVALID_ARG;
+  if (f.workspace == nullptr || (reinterpret_cast<uintptr_t>(f.workspace) & 255)) return HSTU_ERR_WORKSPACE;
+  const int sms = sm_count_current();
+  if (sms <= 0) return HSTU_ERR_CUDA;
+  const BwdPlan bp = make_bwd_plan(a, sms);
+  if (f.workspace_bytes < bp.total) return HSTU_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const bool bf16 = f.dtype == HSTU_DTYPE_BF16;
+  const int D = f.hdim_qk;
+  const int64_t w = static_cast<int64_t>(f.nhead) * D;
+  const int64_t do_stride = packed_or(a->do_row_stride, w);
+  BwdMaps maps;
+  if (!encode_map(&maps.q, f.q, bf16, w, f.total_q, packed_or(f.q_row_stride, w)) ||
+      !encode_map(&maps.q8, f.q, bf16, w, f.total_q, packed_or(f.q_row_stride, w), 8) ||
+      !encode_map(&maps.k, f.k, bf16, w, f.total_kv, packed_or(f.k_row_stride, w)) ||
+      !encode_map(&maps.v, f.v, bf16, w, f.total_kv, packed_or(f.v_row_stride, w)) ||
+      !encode_map(&maps.d_o, a->d_o, bf16, w, f.total_q, do_stride) ||
+      !encode_map(&maps.d_o8, a->d_o, bf16, w, f.total_q, do_stride, 8))
+    return HSTU_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(f.workspace);
+  PrepParams pp = make_prep(&f, bp.fwd);
+  pp.qtile_base = reinterpret_cast<int*>(ws + bp.off_qbase);
+  pp.qtiles = reinterpret_cast<int*>(ws + bp.off_qtiles);
+  pp.kv_units = reinterpret_cast<int4*>(ws + bp.off_kvunits);
+  pp.max_kv_units = bp.max_kv_units;
+  if (launch_prep(pp, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+
+  float* delta = f.softmax ? reinterpret_cast<float*>(ws + bp.off_delta) : nullptr;
+  if (f.softmax && launch_bwd_delta(f.o, packed_or(f.o_row_stride, w), a->d_o, do_stride, delta, f.total_q,
+                                    f.nhead, f.hdim_v, bf16, stream) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+
+  BwdParams bw;
+  std::memset(&bw, 0, sizeof(bw));
+  bw.dq = a->dq;
+  bw.dk = a->dk;
+  bw.dv = a->dv;
+  bw.lse = f.softmax ? f.lse : nullptr;
+  bw.delta = delta;
+  bw.off_q = f.seq_offsets_q;
+  bw.off_kv = f.seq_offsets_kv ? f.seq_offsets_kv : f.seq_offsets_q;
+  bw.targets = f.num_targets;
+  bw.units = pp.units;
+  bw.kv_units = pp.kv_units;
+  bw.qtile_base = pp.qtile_base;
+  bw.qtiles = pp.qtiles;
+  bw.ws_header = pp.ws_header;
+  bw.group_scale = pp.group_scale;
+  bw.dq_stride = packed_or(a->dq_row_stride, w);
+  bw.dk_stride = packed_or(a->dk_row_stride, w);
+  bw.dv_stride = packed_or(a->dv_row_stride, w);
+  bw.total_q = f.total_q;
+  bw.batch = f.batch;
+  bw.nhead = f.nhead;
+  bw.batch_per_group = f.batch / f.num_groups;
+  bw.causal = f.causal;
+  bw.self_attn = f.seq_offsets_kv == nullptr;
+  bw.kv_targets = f.kv_targets;
+  bw.alpha = f.alpha != 0.f ? f.alpha : 1.f / std::sqrt(static_cast<float>(D));
+  fill_group_params(&f, bw.ctx, bw.loc, bw.mf);
+  const int mu = bp.fwd.max_units, mk = bp.max_kv_units;
+  const int grid_q = mu < sms ? (mu > 0 ? mu : 1) : sms;
+  const int grid_kv = mk < sms ? (mk > 0 ? mk : 1) : sms;
+  const cudaError_t e = D == 64 ? launch_bwd_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream)
+                                : launch_bwd_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
+  return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 
 }  // extern "C"

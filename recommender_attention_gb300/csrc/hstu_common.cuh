@@ -51,6 +51,7 @@ enum : int {
   kWsCounter = 2,    // dynamic work counter of the persistent kernel
   kWsTilesLo = 4,    // executed (b, h, q-tile, kv-tile) blocks, int64 in slots 4-5
   kWsPairsLo = 6,    // allowed (b, h, i, j) pairs, int64 in slots 6-7 (stats only)
+  kWsKvUnits = 8,    // backward: number of key-tile work units
   kWsHeaderInts = 64,
 };
 
@@ -332,6 +333,10 @@ struct FwdParams {
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
 };
 
+// Per query tile, for the backward's key-tile units: its TileSet (6 range ends
+// and the count) and TileBounds (4), padded to 12 ints.
+constexpr int kQTileInts = 12;
+
 // Launch parameters of the scheduler (prep) kernel.
 struct PrepParams {
   const int* off_q;
@@ -340,12 +345,41 @@ struct PrepParams {
   int4* units;
   int* ws_header;
   float* group_scale;
-  int* batch_scratch;      // [4 * batch + 2] ints (used when batch is large)
+  int* batch_scratch;      // [5 * batch + 3] ints (used when batch is large)
+  // backward scheduling (null for the forward): the first query tile of each
+  // sequence [batch + 1], every query tile's key-tile set and bounds
+  // [query tiles][kQTileInts], and the key-tile units {b, n, h, 0}
+  int* qtile_base;
+  int* qtiles;
+  int4* kv_units;
+  int max_kv_units;
   int batch, nhead, num_groups, batch_per_group, splits;
   int total_q, total_kv, max_seqlen_q, max_seqlen_kv, max_units;
   int causal, self_attn, kv_targets;
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups], max_uih[kMaxGroups];
   float attn_scale[kMaxGroups];
+};
+
+// Backward kernel parameters (dQ and dK/dV kernels).
+struct BwdParams {
+  void* dq;                // [total_q, dq_stride] gradients (storage type)
+  void* dk;                // [total_kv, dk_stride]
+  void* dv;                // [total_kv, dv_stride]
+  const float* lse;        // [nhead, total_q] natural-log LSE of the forward (softmax)
+  const float* delta;      // [nhead, total_q] rowsum(dO . O) (softmax)
+  const int* off_q;
+  const int* off_kv;       // == off_q for self-attention
+  const int* targets;
+  const int4* units;       // dQ units {b, m, h, 0}
+  const int4* kv_units;    // dK/dV units {b, n, h, 0}
+  const int* qtile_base;   // [batch + 1] first query tile of each sequence
+  const int* qtiles;       // [query tiles][kQTileInts]
+  int* ws_header;
+  const float* group_scale;
+  long long dq_stride, dk_stride, dv_stride;
+  int total_q, batch, nhead, batch_per_group, causal, self_attn, kv_targets;
+  float alpha;
+  int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
 };
 
 // Combine kernel parameters (split-KV).

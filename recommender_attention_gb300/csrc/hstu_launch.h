@@ -19,6 +19,19 @@ cudaError_t launch_fwd_d96(const CUtensorMap& q, const CUtensorMap& k, const CUt
                            cudaStream_t stream);
 cudaError_t launch_fwd_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                             const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
+// Tensor maps of the backward: 128-row boxes, and 8-row boxes for query tiles
+// whose rows come in two runs.
+struct BwdMaps {
+  CUtensorMap q, k, v, d_o, q8, d_o8;
+};
+// dQ kernel then dK/dV kernel over the scheduler's query-tile and key-tile units.
+cudaError_t launch_bwd_d64(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q, int grid_kv,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_d128(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q, int grid_kv,
+                            cudaStream_t stream);
+// delta[h, i] = sum_e dO[i, h, e] O[i, h, e] in fp32 over every row in [0, total_q).
+cudaError_t launch_bwd_delta(const void* o, long long o_stride, const void* d_o, long long do_stride, float* delta,
+                             int total_q, int nhead, int hdim_v, bool bf16, cudaStream_t stream);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
 cudaError_t launch_pairs(const PrepParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, int hdim, bool bf16, cudaStream_t stream);

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
   int* cost = tbase + (B + 1);                                 // [B] key tiles per sequence
   int* order = cost + B;                                       // [B] sequences, longest first
   int* ubase = order + B;                                      // [B+1] unit offsets by position
+  int* kbase = ubase + (B + 1);                                // [B+1] key-tile unit offsets (backward)
   for (int g = tid; g < kMaxGroups; g += nth) s_gmax[g] = 0;
   if (tid == 0) {
     s_err = 0;
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     if (tid == 0) {
       p.ws_header[kWsError] = s_err;
       p.ws_header[kWsUnits] = 0;
+      p.ws_header[kWsKvUnits] = 0;
       p.ws_header[kWsCounter] = 0;
       reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
     }
@@ -140,7 +142,16 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     const int g = b / p.batch_per_group;
     const SeqGeom s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[g], p.loc[g], p.mf[g], p.causal,
                                 p.self_attn, p.kv_targets);
-    const int cnt = query_tile_kv_tiles(s, q_layout(s), i - tbase[b]).count;
+    const QLayout L = q_layout(s);
+    const TileSet ts = query_tile_kv_tiles(s, L, i - tbase[b]);
+    const int cnt = ts.count;
+    if (p.qtiles) {
+      const TileBounds tb = q_tile_bounds(s, L, i - tbase[b]);
+      int* o = p.qtiles + static_cast<long long>(i) * kQTileInts;
+      o[0] = ts.lo0; o[1] = ts.hi0; o[2] = ts.lo1; o[3] = ts.hi1; o[4] = ts.lo2; o[5] = ts.hi2;
+      o[6] = ts.count;
+      o[7] = tb.LO; o[8] = tb.HI; o[9] = tb.maxLO; o[10] = tb.minHI;
+    }
     atomicAdd(&cost[b], cnt);
     tiles += cnt;
   }
@@ -174,6 +185,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     if (tid == 0) {
       p.ws_header[kWsError] = kErrMaxSeqlen;
       p.ws_header[kWsUnits] = 0;
+      p.ws_header[kWsKvUnits] = 0;
       p.ws_header[kWsCounter] = 0;
       reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
     }
@@ -196,6 +208,39 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     p.units[u] = make_int4(b, m, h, rem % p.splits);
   }
 
+  // 4b. backward: the query-tile base of each sequence, and key-tile units in
+  //     the same sequence order, heads outer, key tiles from the first (seen
+  //     by most query tiles under a causal mask) up
+  int total_kv_units = 0;
+  if (p.qtiles) {
+    for (int b = tid; b <= B; b += nth) p.qtile_base[b] = tbase[b];
+    for (int pos = tid; pos < B; pos += nth) {
+      const int b = order[pos];
+      const int k0 = p.self_attn ? p.off_q[b] : p.off_kv[b];
+      const int k1 = p.self_attn ? p.off_q[b + 1] : p.off_kv[b + 1];
+      kbase[pos] = ((k1 - k0 + kBlockN - 1) / kBlockN) * p.nhead;   // every key row gets its gradient
+    }
+    __syncthreads();
+    total_kv_units = block_exclusive_scan(kbase, B, s_wsum);
+    if (total_kv_units > p.max_kv_units) {
+      if (tid == 0) {
+        p.ws_header[kWsError] = kErrMaxSeqlen;
+        p.ws_header[kWsUnits] = 0;
+        p.ws_header[kWsKvUnits] = 0;
+        p.ws_header[kWsCounter] = 0;
+        reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
+      }
+      return;
+    }
+    for (int u = tid; u < total_kv_units; u += nth) {
+      const int pos = find_segment(kbase, B, u);
+      const int b = order[pos];
+      const int per_h = (kbase[pos + 1] - kbase[pos]) / p.nhead;
+      const int local = u - kbase[pos];
+      p.kv_units[u] = make_int4(b, local % per_h, local / per_h, 0);
+    }
+  }
+
   // 5. attn_scale per group: 0 means 1 / (max UIH length of the group)
   for (int g = tid; g < p.num_groups; g += nth) {
     float sc = p.attn_scale[g];
@@ -209,6 +254,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
   if (tid == 0) {
     p.ws_header[kWsError] = 0;
     p.ws_header[kWsUnits] = total;
+    p.ws_header[kWsKvUnits] = total_kv_units;
     p.ws_header[kWsCounter] = 0;
     reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = static_cast<long long>(s_tiles);
   }
@@ -319,7 +365,73 @@ __global__ void hstu_wait_selftest_kernel(int* result, unsigned long long timeou
   if (threadIdx.x == 0) *result = ptx::mbar_wait(&bar, 0, timeout_ns) ? 0 : 1;
 }
 
+// delta[h, i] = sum_e dO[i, h, e] O[i, h, e] (fp32), the row term of the
+// softmax backward.  TPR threads per (row, head), 8 elements (16 bytes) each.
+template <bool BF16, int TPR>
+__global__ void __launch_bounds__(256) hstu_bwd_delta_kernel(const uint16_t* __restrict__ o, long long o_stride,
+                                                             const uint16_t* __restrict__ d_o, long long do_stride,
+                                                             float* __restrict__ delta, int total_q, int nhead,
+                                                             int hdim_v) {
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long pair = gid / TPR;
+  const int sub = static_cast<int>(gid % TPR);
+  const bool live = pair < static_cast<long long>(total_q) * nhead;
+  const int row = live ? static_cast<int>(pair / nhead) : 0;
+  const int h = live ? static_cast<int>(pair % nhead) : 0;
+  float acc = 0.f;
+  if (live && sub * 8 < hdim_v) {
+    const long long col = static_cast<long long>(h) * hdim_v + sub * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * o_stride + col);
+    const uint4 b = *reinterpret_cast<const uint4*>(d_o + row * do_stride + col);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float a0, a1, b0, b1;
+      if constexpr (BF16) {
+        a0 = __uint_as_float(av[k] << 16);
+        a1 = __uint_as_float(av[k] & 0xFFFF0000u);
+        b0 = __uint_as_float(bv[k] << 16);
+        b1 = __uint_as_float(bv[k] & 0xFFFF0000u);
+      } else {
+        a0 = __half2float(__ushort_as_half(static_cast<unsigned short>(av[k] & 0xFFFFu)));
+        a1 = __half2float(__ushort_as_half(static_cast<unsigned short>(av[k] >> 16)));
+        b0 = __half2float(__ushort_as_half(static_cast<unsigned short>(bv[k] & 0xFFFFu)));
+        b1 = __half2float(__ushort_as_half(static_cast<unsigned short>(bv[k] >> 16)));
+      }
+      acc = fmaf(a0, b0, acc);
+      acc = fmaf(a1, b1, acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (live && sub == 0) delta[static_cast<long long>(h) * total_q + row] = acc;
+}
+
+template <bool BF16, int TPR>
+cudaError_t launch_delta_t(const void* o, long long o_stride, const void* d_o, long long do_stride, float* delta,
+                           int total_q, int nhead, int hdim_v, cudaStream_t stream) {
+  const long long threads = static_cast<long long>(total_q) * nhead * TPR;
+  const long long blocks = (threads + 255) / 256;
+  if (blocks <= 0) return cudaSuccess;
+  hstu_bwd_delta_kernel<BF16, TPR><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), o_stride, static_cast<const uint16_t*>(d_o), do_stride, delta, total_q,
+      nhead, hdim_v);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_delta(const void* o, long long o_stride, const void* d_o, long long do_stride, float* delta,
+                             int total_q, int nhead, int hdim_v, bool bf16, cudaStream_t stream) {
+  const int per = (hdim_v + 7) / 8;
+  if (per <= 8) return bf16 ? launch_delta_t<true, 8>(o, o_stride, d_o, do_stride, delta, total_q, nhead, hdim_v, stream)
+                            : launch_delta_t<false, 8>(o, o_stride, d_o, do_stride, delta, total_q, nhead, hdim_v, stream);
+  if (per <= 16) return bf16 ? launch_delta_t<true, 16>(o, o_stride, d_o, do_stride, delta, total_q, nhead, hdim_v, stream)
+                             : launch_delta_t<false, 16>(o, o_stride, d_o, do_stride, delta, total_q, nhead, hdim_v, stream);
+  if (per <= 32) return bf16 ? launch_delta_t<true, 32>(o, o_stride, d_o, do_stride, delta, total_q, nhead, hdim_v, stream)
+                             : launch_delta_t<false, 32>(o, o_stride, d_o, do_stride, delta, total_q, nhead, hdim_v, stream);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_wait_selftest(int* result, unsigned long long timeout_ns, cudaStream_t stream) {
   hstu_wait_selftest_kernel<<<1, 32, 0, stream>>>(result, timeout_ns);
@@ -327,7 +439,7 @@ cudaError_t launch_wait_selftest(int* result, unsigned long long timeout_ns, cud
 }
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
-  const size_t dsmem = p.batch <= kPrepSmemBatch ? (4 * static_cast<size_t>(p.batch) + 2) * sizeof(int) : 0;
+  const size_t dsmem = p.batch <= kPrepSmemBatch ? (5 * static_cast<size_t>(p.batch) + 3) * sizeof(int) : 0;
   hstu_prep_kernel<<<1, kPrepThreads, dsmem, stream>>>(p);
   return cudaGetLastError();
 }

@@ -1,7 +1,7 @@
 """Thin ctypes binding over ``libhstu_attn.so`` (see ``include/hstu_attn.h``).
 
-Argument marshalling only: every step of the forward runs in the library's
-CUDA kernels.  PyTorch provides device memory and streams.  There is no CPU or
+Argument marshalling only: every step of the forward and the backward runs in
+the library's CUDA kernels.  PyTorch provides device memory and streams.  There is no CPU or
 framework fallback: when the library is missing every call raises.
 """
 from __future__ import annotations
@@ -57,6 +57,15 @@ class FwdArgs(ctypes.Structure):
     ]
 
 
+class BwdArgs(ctypes.Structure):
+    """Mirror of ``hstu_bwd_args``."""
+    _fields_ = [
+        ("fwd", FwdArgs), ("d_o", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+        ("dv", ctypes.c_void_p), ("do_row_stride", ctypes.c_int64), ("dq_row_stride", ctypes.c_int64),
+        ("dk_row_stride", ctypes.c_int64), ("dv_row_stride", ctypes.c_int64),
+    ]
+
+
 class FwdStats(ctypes.Structure):
     """Mirror of ``hstu_fwd_stats``."""
     _fields_ = [("executed_tiles", ctypes.c_int64), ("allowed_pairs", ctypes.c_int64),
@@ -77,6 +86,9 @@ EXPORTS = {
                                                   ctypes.POINTER(ctypes.c_int32)]),
     "hstu_attn_fwd_static_ws": (ctypes.c_int, [ctypes.POINTER(FwdArgs), ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_void_p)]),
+    "hstu_bwd_args_size": (ctypes.c_size_t, []),
+    "hstu_attn_bwd_workspace_size": (ctypes.c_int, [ctypes.POINTER(BwdArgs), ctypes.POINTER(ctypes.c_size_t)]),
+    "hstu_attn_bwd": (ctypes.c_int, [ctypes.POINTER(BwdArgs), ctypes.c_void_p]),
 }
 
 
@@ -224,6 +236,72 @@ class HstuCall:
         return {"executed_tiles": s.executed_tiles, "allowed_pairs": s.allowed_pairs,
                 "work_units": s.work_units, "num_splits": s.num_splits,
                 "device_error": s.device_error}
+
+
+class HstuBwdCall:
+    """One marshalled backward call.  ``o`` and ``lse`` are the forward's outputs
+    (read in softmax mode only); the keyword arguments are the forward's."""
+
+    def __init__(self, q, k, v, d_o, seq_offsets_q, seq_offsets_kv=None, num_targets=None, *,
+                 o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                 dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, **kw):
+        kw.pop("num_splits", None)
+        kw.pop("save_lse", None)
+        self.fwd = HstuCall(q, k, v, seq_offsets_q, seq_offsets_kv, num_targets, out=o, lse=lse,
+                            save_lse=False, static_workspace=True, **kw)
+        self.lib = self.fwd.lib
+        if d_o.dtype != q.dtype or d_o.shape != self.fwd.o.shape:
+            raise ValueError("d_o must match o in shape and dtype")
+        self.dq = torch.empty_like(q) if dq is None else dq
+        self.dk = torch.empty_like(k) if dk is None else dk
+        self.dv = torch.empty_like(v) if dv is None else dv
+        for t in (d_o, self.dq, self.dk, self.dv):
+            if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+                raise ValueError("d_o/dq/dk/dv must be [tokens, nhead, hdim] with packed heads")
+        self._keep = [d_o]
+        b = BwdArgs()
+        b.fwd = self.fwd.args
+        b.d_o, b.dq, b.dk, b.dv = _ptr(d_o), _ptr(self.dq), _ptr(self.dk), _ptr(self.dv)
+        b.do_row_stride, b.dq_row_stride = d_o.stride(0), self.dq.stride(0)
+        b.dk_row_stride, b.dv_row_stride = self.dk.stride(0), self.dv.stride(0)
+        size = ctypes.c_size_t(0)
+        st = self.lib.hstu_attn_bwd_workspace_size(ctypes.byref(b), ctypes.byref(size))
+        if st != HSTU_OK:
+            raise HstuError(st, "hstu_attn_bwd_workspace_size")
+        self.workspace_bytes = size.value
+        if workspace is None or workspace.numel() < self.workspace_bytes:
+            workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=q.device)
+        self.workspace = workspace
+        b.fwd.workspace = workspace.data_ptr()
+        b.fwd.workspace_bytes = workspace.numel()
+        self.args = b
+
+    def launch(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        st = self.lib.hstu_attn_bwd(ctypes.byref(self.args), ctypes.c_void_p(_stream_handle(stream)))
+        if st != HSTU_OK:
+            raise HstuError(st, "hstu_attn_bwd")
+
+    def check(self, stream: Optional[torch.cuda.Stream] = None) -> int:
+        err = ctypes.c_int32(0)
+        st = self.lib.hstu_attn_fwd_check(ctypes.c_void_p(self.workspace.data_ptr()),
+                                          ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(err))
+        if st != HSTU_OK:
+            raise HstuError(st, "hstu_attn_bwd (device check)", err.value)
+        return err.value
+
+
+def hstu_attn_bwd(q, k, v, d_o, seq_offsets_q, seq_offsets_kv=None, num_targets=None, *,
+                  stream: Optional[torch.cuda.Stream] = None, check: bool = False, **kw):
+    """HSTU attention backward (``hstu_attn_bwd`` in ``include/hstu_attn.h``):
+    the gradients of the forward with the same keyword arguments for the output
+    gradient ``d_o``.  Softmax mode needs the forward's ``o=`` and ``lse=``.
+    Returns ``(dq, dk, dv)``."""
+    call = HstuBwdCall(q, k, v, d_o, seq_offsets_q, seq_offsets_kv, num_targets, **kw)
+    call.launch(stream)
+    if check:
+        call.check(stream)
+    return call.dq, call.dk, call.dv
 
 
 def hstu_attn_fwd(q, k, v, seq_offsets_q, seq_offsets_kv=None, num_targets=None, *,

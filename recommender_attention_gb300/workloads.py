@@ -119,6 +119,17 @@ class Workload:
             out.append(torch.from_numpy(x).to(DTYPES[self.dtype]))
         return tuple(out)
 
+    def grad_output(self):
+        """An output gradient dO [total_q, nhead, hdim_v] (CPU, storage dtype)
+        for the backward, from its own stream of the seed, same distribution."""
+        grng = np.random.default_rng([self.seed, 2])
+        shp = (self.total_q, self.nhead, self.hdim_v)
+        if self.dist == "normal":
+            x = grng.standard_normal(size=shp, dtype=np.float32)
+        else:
+            x = grng.uniform(-1.0, 1.0, size=shp).astype(np.float32)
+        return torch.from_numpy(x).to(DTYPES[self.dtype])
+
 
 def _draw_ints(rng, lo, hi, n):
     """n integers uniform on [lo, hi] inclusive."""

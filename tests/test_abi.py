@@ -34,11 +34,12 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_strings_and_struct_layout(lib):
-    assert lib.hstu_abi_version() == 2
+    assert lib.hstu_abi_version() == 3
     for s in range(6):
         assert lib.hstu_status_string(s)
     assert lib.hstu_status_string(99) == b"unknown status"
     assert lib.hstu_fwd_args_size() == ctypes.sizeof(hstu.FwdArgs)
+    assert lib.hstu_bwd_args_size() == ctypes.sizeof(hstu.BwdArgs)
 
 
 def _args(**kw):
@@ -103,6 +104,55 @@ def test_forward_rejects_before_launch(lib):
     a.q = 4096 + 2
     a.workspace = 8192
     assert lib.hstu_attn_fwd(ctypes.byref(a), None) == 1
+
+
+def _bwd(**kw):
+    b = hstu.BwdArgs()
+    b.fwd = _args(**{k: v for k, v in kw.items() if k in dict(hstu.FwdArgs._fields_)})
+    for k, v in kw.items():
+        if k in dict(hstu.BwdArgs._fields_):
+            setattr(b, k, v)
+    return b
+
+
+def _bwd_ws(lib, b):
+    n = ctypes.c_size_t(0)
+    st = lib.hstu_attn_bwd_workspace_size(ctypes.byref(b), ctypes.byref(n))
+    return st, n.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0), ({"hdim_qk": 64, "hdim_v": 64}, 0), ({"num_splits": 5}, 0),   # splits are ignored
+    ({"hdim_qk": 96, "hdim_v": 96}, 2), ({"hdim_qk": 256, "hdim_v": 256}, 2),
+    ({"hdim_qk": 96, "hdim_v": 64}, 2), ({"dtype": 7}, 2), ({"batch": 0}, 1),
+    ({"do_row_stride": 100}, 1), ({"dk_row_stride": 258}, 1), ({"dv_row_stride": 260}, 1)])
+def test_backward_host_validation(lib, kw, status):
+    assert _bwd_ws(lib, _bwd(**kw))[0] == status
+
+
+def test_backward_workspace_holds_row_sums_in_softmax_mode(lib):
+    st0, n0 = _bwd_ws(lib, _bwd(softmax=0))
+    st1, n1 = _bwd_ws(lib, _bwd(softmax=1))
+    assert st0 == st1 == 0
+    assert n1 - n0 >= 2 * 1000 * 4            # delta: [H, total_q] fp32
+    stf, nf = _ws(lib, _args(num_splits=1))
+    assert n0 > nf                            # plus query-tile records and key-tile units
+
+
+def test_backward_rejects_before_launch(lib):
+    b = _bwd()
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1
+    b.fwd.q = b.fwd.k = b.fwd.v = b.fwd.seq_offsets_q = 4096
+    b.d_o = b.dq = b.dk = b.dv = 8192
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 3     # no workspace
+    b.fwd.workspace = 4096 + 16
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 3     # misaligned workspace
+    b.fwd.workspace = 1 << 20
+    b.dk = 8192 + 4
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1     # misaligned gradient
+    b.dk = 8192
+    b.fwd.softmax = 1
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1     # softmax needs o and lse
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -1,0 +1,170 @@
+"""Backward parity: dQ, dK, dV of the CUDA path (through the C ABI) against the
+fp64 oracle's hstu_attention_backward, element by element, on the same seeded
+inputs and output gradient.
+
+Softmax mode feeds the backward the forward's own o and lse (from the CUDA
+forward, as a training step would).  Tolerance: the forward's per-dtype bound
+on max |err| relative to max |reference| of each gradient, plus the same
+elementwise rtol; the kernels round P and dS to the storage type before the
+two gradient products, exactly as the forward rounds P before P V."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.hstu_oracle import hstu_attention_backward, resolved_attn_scales
+from recommender_attention_gb300 import hstu
+from recommender_attention_gb300 import workloads as W
+from tests.gpu_helpers import assert_parity, call_kwargs, device_inputs
+from tests.helpers import as_f64, oracle_params
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    hstu.load_library()
+
+
+def _host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def gpu_backward(w, q, k, v, d_o, **over):
+    dq, dk, dv, off_q, off_kv, tg = device_inputs(w, q, k, v)
+    kw = call_kwargs(w, **over)
+    o = lse = None
+    if w.softmax:
+        o, lse = hstu.hstu_attn_fwd(dq, dk, dv, off_q, off_kv, tg, check=True, **kw)
+    g = hstu.hstu_attn_bwd(dq, dk, dv, d_o.cuda(), off_q, off_kv, tg, o=o, lse=lse, check=True, **kw)
+    torch.cuda.synchronize()
+    return tuple(_host(x) for x in g)
+
+
+def check_backward(w, **over):
+    q, k, v = w.tensors()
+    d_o = w.grad_output()
+    got = gpu_backward(w, q, k, v, d_o, **over)
+    ref = hstu_attention_backward(as_f64(q), as_f64(k), as_f64(v), as_f64(d_o), w.seq_offsets_q(),
+                                  w.seq_offsets_kv(), w.num_targets(), oracle_params(w))
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert_parity(a, b, w.dtype, what=f"{w.name} {name}")
+
+
+# ---------------------------------------------------------------- the small configs
+@pytest.mark.parametrize("cfg", ["tiny", "jagged", "batched"])
+@pytest.mark.parametrize("softmax", [False, True])
+def test_small_configs_backward(cfg, softmax):
+    w = W.CONFIGS[cfg]().with_(softmax=softmax)
+    check_backward(w)
+
+
+@pytest.mark.parametrize("softmax", [False, True])
+def test_group_cross_backward(softmax):
+    check_backward(W.group_cross_splitkv(softmax=softmax, batch=8))
+
+
+@pytest.mark.parametrize("softmax", [False, True])
+def test_mfalcon_backward(softmax):
+    check_backward(W.mfalcon(batch=3, candidates=200, softmax=softmax, history=(300, 900)))
+
+
+# ---------------------------------------------------------------- fuzz
+@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("softmax", [False, True])
+def test_fuzz_backward(seed, softmax):
+    hdim = [64, 128][seed % 2]
+    dtype = "bf16" if seed % 3 else "fp16"
+    w = W.random_small(seed, dtype=dtype, hdim=hdim, softmax=softmax, kv_targets=seed % 5 == 4)
+    check_backward(w)
+
+
+# ---------------------------------------------------------------- edges
+def test_backward_edge_empty_sequences_and_rows_without_keys():
+    # cross-attention with an empty key sequence: its query rows see nothing
+    # (dq = 0), an empty query sequence leaves its keys without a query
+    # (dk = dv = 0), plus a sequence with only context rows
+    w = W.Workload(name="edges_bwd", batch=4, nhead=2, hdim_qk=64, hdim_v=64, dtype="bf16",
+                   uih_q=[0, 130, 0, 300], uih_kv=[0, 0, 260, 129], targets=[0, 3, 0, 5],
+                   context_len=[0], local_len=[0], causal=True, seed=5)
+    for softmax in (False, True):
+        check_backward(w.with_(softmax=softmax))
+    w2 = W.Workload(name="ctx_only", batch=2, nhead=1, hdim_qk=128, hdim_v=128, dtype="bf16",
+                    uih_q=[0, 200], targets=[0, 1], context_len=[7], causal=True, seed=6,
+                    max_uih_len=[64])
+    check_backward(w2)
+
+
+def test_backward_rows_outside_sequences_untouched():
+    w = W.random_small(3, hdim=64)
+    q, k, v = w.tensors()
+    d_o = w.grad_output()
+    pad = 37
+    qp = torch.cat([q, torch.zeros((pad,) + q.shape[1:], dtype=q.dtype)])
+    kp = torch.cat([k, torch.zeros((pad,) + k.shape[1:], dtype=k.dtype)])
+    vp = torch.cat([v, torch.zeros((pad,) + v.shape[1:], dtype=v.dtype)])
+    dop = torch.cat([d_o, torch.zeros((pad,) + d_o.shape[1:], dtype=d_o.dtype)])
+    dq, dk, dv, off_q, off_kv, tg = device_inputs(w, qp, kp, vp)
+    sentinel = 3.0
+    gq, gk, gv = (torch.full_like(x, sentinel) for x in (dq, dk, dv))
+    hstu.hstu_attn_bwd(dq, dk, dv, dop.cuda(), off_q, off_kv, tg, dq=gq, dk=gk, dv=gv, check=True,
+                       **call_kwargs(w))
+    torch.cuda.synchronize()
+    nq, nkv = w.total_q, w.total_kv
+    assert torch.all(gq[nq:] == sentinel) and torch.all(gk[nkv:] == sentinel) and torch.all(gv[nkv:] == sentinel)
+    ref = hstu_attention_backward(as_f64(q), as_f64(k), as_f64(v), as_f64(d_o), w.seq_offsets_q(),
+                                  w.seq_offsets_kv(), w.num_targets(), oracle_params(w))
+    for name, a, b in zip(("dq", "dk", "dv"), (gq[:nq], gk[:nkv], gv[:nkv]), ref):
+        assert_parity(_host(a), b, w.dtype, what=name)
+
+
+def test_backward_device_error_leaves_gradients_untouched():
+    w = W.CONFIGS["tiny"]()
+    q, k, v = w.tensors()
+    dq, dk, dv, off_q, off_kv, tg = device_inputs(w, q, k, v)
+    gq, gk, gv = (torch.full_like(x, 5.0) for x in (dq, dk, dv))
+    call = hstu.HstuBwdCall(dq, dk, dv, w.grad_output().cuda(), off_q, off_kv, tg, dq=gq, dk=gk, dv=gv,
+                            **call_kwargs(w, max_seqlen_q=10, max_seqlen_kv=10))
+    call.launch()
+    with pytest.raises(hstu.HstuError) as e:
+        call.check()
+    assert e.value.device_error & 8   # max_seqlen
+    assert torch.all(gq == 5.0) and torch.all(gk == 5.0) and torch.all(gv == 5.0)
+
+
+def test_backward_repeated_calls_are_identical():
+    w = W.random_small(7, hdim=128, softmax=True)
+    q, k, v = w.tensors()
+    d_o = w.grad_output()
+    a = gpu_backward(w, q, k, v, d_o)
+    b = gpu_backward(w, q, k, v, d_o)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+# ---------------------------------------------------------------- full size, sampled sequences
+@pytest.mark.parametrize("softmax", [False, True])
+def test_large_jagged_backward_sampled(softmax):
+    """The large jagged workload at full size through one backward call; the
+    oracle recomputes a few whole sequences (a sequence's gradients depend on
+    that sequence alone), with the attn_scale the full batch resolves to."""
+    w = W.large_jagged(hdim=128).with_(softmax=softmax)
+    q, k, v = w.tensors()
+    d_o = w.grad_output()
+    got = gpu_backward(w, q, k, v, d_o)
+    off = w.seq_offsets_q()
+    p = oracle_params(w)
+    scale = float(resolved_attn_scales(p, w.batch, off, w.num_targets())[0])
+    lens = w.lengths_q()
+    rng = np.random.default_rng(3)
+    for b in [int(np.argmin(lens)), int(rng.integers(0, w.batch))]:
+        s0, s1 = int(off[b]), int(off[b + 1])
+        sub = dataclasses.replace(p, attn_scale=[scale])
+        ref = hstu_attention_backward(as_f64(q[s0:s1]), as_f64(k[s0:s1]), as_f64(v[s0:s1]),
+                                      as_f64(d_o[s0:s1]), np.array([0, s1 - s0]), None,
+                                      np.array([w.targets[b]]), sub)
+        for name, a, r in zip(("dq", "dk", "dv"), got, ref):
+            assert_parity(a[s0:s1], r, w.dtype, what=f"b{b} {name}")
