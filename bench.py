@@ -5,7 +5,8 @@
 One step = one forward (scheduler + persistent tcgen05 kernel [+ combine]) over
 the large jagged workload: B=64 sequences, nhead 4, bf16, UIH lengths
 U_int[1024, 4096], targets U_int[1, 32], context 6, full causal, hdim 128
-(repeated at hdim 256 in the same run), synthetic N(0,1) inputs, seed 7.
+(repeated at hdim 256, 96 and 96/64 in the same run, and the backward of the
+hdim 128 case under "backward"), synthetic N(0,1) inputs, seed 7.
 Prints one JSON line (rank 0).  Metric: useful TFLOP/s = 2 (hdim_qk + hdim_v)
 x allowed (i, j) pairs / step time.
 
@@ -291,6 +292,55 @@ def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float)
     return out
 
 
+def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, peak: float):
+    """The backward over the same large jagged workload (hdim 128; SiLU, and
+    softmax fed the forward's own o and lse): one step = one hstu_attn_bwd call
+    (scheduler [+ row sums] + dQ kernel + dK/dV kernel), inputs and dO resident
+    (larger than L2).  Useful FLOPs per allowed pair: 2 (3 hdim_qk + 2 hdim_v),
+    the five products (S, dP, dV, dK, dQ) counted once; the two kernels
+    recompute S and dP, so the executed count is 2 (5 hdim_qk + 4 hdim_v)."""
+    from recommender_attention_gb300.hstu import HstuBwdCall
+    out = {}
+    for softmax in (False, True):
+        w = rank_workload(rank, 128).with_(softmax=softmax)
+        q, k, v = w.tensors()
+        call, (dq, dk, dv, off_q, tg) = device_call(w, q, k, v, device)
+        st = call.stats(stream)
+        call.launch(stream)
+        call.check(stream)
+        d_o = w.grad_output().to(device)
+        bw = HstuBwdCall(dq, dk, dv, d_o, off_q, None, tg, o=call.o, lse=call.lse, alpha=w.alpha,
+                         attn_scale=list(w.attn_scale), causal=w.causal, local_len=list(w.local_len),
+                         context_len=list(w.context_len), minfull_len=list(w.minfull_len),
+                         max_uih_len=list(w.max_uih_len), num_groups=w.num_groups, softmax=w.softmax,
+                         max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()))
+        for _ in range(warmup):
+            bw.launch(stream)
+        bw.check(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            bw.launch(stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        bw.check(stream)
+        ms = reduce_max(a.elapsed_time(b) / steps, world, device)
+        useful = 2.0 * (3 * w.hdim_qk + 2 * w.hdim_v) * st["allowed_pairs"]
+        executed = 2.0 * 128 * 128 * (5 * w.hdim_qk + 4 * w.hdim_v) * st["executed_tiles"]
+        tot = reduce_sum(useful, world, device)
+        tf = tot / (ms * 1e-3) / 1e12
+        out["softmax" if softmax else "silu"] = {
+            "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "pct_of_bf16_peak": 100.0 * tf / world / peak,
+            "executed_tflops": reduce_sum(executed, world, device) / (ms * 1e-3) / 1e12,
+            "launches_per_step": 3 + (1 if softmax else 0)}
+        del bw, call, dq, dk, dv, d_o, q, k, v
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_e2e_steps(call, host, dev, steps, warmup, world, stream):
     """Public-API round trip per step: pinned host q/k/v/offsets/targets -> device,
     forward, device o -> pinned host."""
@@ -372,6 +422,11 @@ def run_cuda(args):
                           "fwd_kernel_ms": fw2, "fwd_kernel_tflops": f2 / (fw2 * 1e-3) / 1e12}
             del call2, dev2, q2, k2, v2
             torch.cuda.empty_cache()
+
+    if args.hdim == 128 and not args.no_bwd:
+        peaks_b, _ = load_peaks()
+        extra["backward"] = backward_lines(rank, device, stream, args.steps, args.warmup, world,
+                                           float(peaks_b.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
 
     if rank == 0 and not args.no_configs:
         peaks0, _ = load_peaks()
@@ -507,6 +562,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--hdim", type=int, default=128, choices=[64, 128, 256])
     ap.add_argument("--no-d256", action="store_true", help="skip the hdim 256, 96 and 96/64 repeats")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other scope workloads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
