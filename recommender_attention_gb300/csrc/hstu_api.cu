@@ -207,8 +207,8 @@ PrepParams make_prep(const hstu_fwd_args* a, const Plan& pl) {
 // softmax mode, the row sums delta [H, total_q].
 struct BwdPlan {
   Plan fwd;
-  int q_tiles, max_kv_units;
-  size_t off_qbase, off_qtiles, off_kvunits, off_delta, total;
+  int q_tiles, max_kv_units, max_mask_words;
+  size_t off_qbase, off_qtiles, off_kvunits, off_maskbase, off_mask, off_delta, total;
 };
 
 hstu_fwd_args bwd_fwd_view(const hstu_bwd_args* a) {
@@ -248,6 +248,15 @@ BwdPlan make_bwd_plan(const hstu_bwd_args* a, int sms) {
   off = align256(off + static_cast<size_t>(bp.q_tiles) * kQTileInts * sizeof(int));
   bp.off_kvunits = off;
   off = align256(off + static_cast<size_t>(bp.max_kv_units) * sizeof(int4));
+  // member masks: (key tiles) x ceil(query tiles of the longest sequence / 32) words
+  const long long words_per_tile = ((bp.fwd.max_seq_q + kBlockM - 1) / kBlockM + 31) / 32;
+  long long mask_words = static_cast<long long>(bp.max_kv_units / f.nhead) * (words_per_tile > 0 ? words_per_tile : 1);
+  if (mask_words > (1LL << 30)) mask_words = 1LL << 30;
+  bp.max_mask_words = static_cast<int>(mask_words);
+  bp.off_maskbase = off;
+  off = align256(off + (static_cast<size_t>(f.batch) + 1) * sizeof(int));
+  bp.off_mask = off;
+  off = align256(off + static_cast<size_t>(bp.max_mask_words) * sizeof(unsigned));
   bp.off_delta = 0;
   if (f.softmax) {
     bp.off_delta = off;
@@ -473,6 +482,9 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   pp.qtiles = reinterpret_cast<int*>(ws + bp.off_qtiles);
   pp.kv_units = reinterpret_cast<int4*>(ws + bp.off_kvunits);
   pp.max_kv_units = bp.max_kv_units;
+  pp.kv_mask = reinterpret_cast<unsigned*>(ws + bp.off_mask);
+  pp.kv_mask_base = reinterpret_cast<int*>(ws + bp.off_maskbase);
+  pp.max_mask_words = bp.max_mask_words;
   if (launch_prep(pp, stream) != cudaSuccess) return HSTU_ERR_CUDA;
 
   float* delta = f.softmax ? reinterpret_cast<float*>(ws + bp.off_delta) : nullptr;
@@ -494,6 +506,8 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   bw.kv_units = pp.kv_units;
   bw.qtile_base = pp.qtile_base;
   bw.qtiles = pp.qtiles;
+  bw.kv_mask = pp.kv_mask;
+  bw.kv_mask_base = pp.kv_mask_base;
   bw.ws_header = pp.ws_header;
   bw.group_scale = pp.group_scale;
   bw.dq_stride = packed_or(a->dq_row_stride, w);

@@ -10,22 +10,29 @@
 //             dS = p . (c g V^T - delta),  delta = rowsum(g . O)
 //   both:     dQ = alpha dS K,  dK = alpha dS^T Q
 //
-// Two persistent kernels, each a static round-robin over its work units, with
-// one warp of TMA loads, one MMA warp (the whole warp runs the loop, one
-// elected lane issues) and two elementwise warpgroups that split each score
-// row's 128 columns:
+// Two persistent kernels with one warp of TMA loads (which also claims work
+// units from a global counter, longest first, and publishes them to the other
+// roles through a two-slot ring), one MMA warp (the whole warp runs the loop,
+// one elected lane issues) and two elementwise warpgroups.  Work goes in half
+// tiles of 64 columns with two TMEM buffers, so the tensor core computes the
+// next half tile's score products while the elementwise warps process the
+// current one:
 //   dQ kernel, one unit per (sequence, head, query tile): for every key tile of
-//     the tile's set, S = Q K^T and dP = dO V^T into TMEM, dS (16-bit, packed
-//     over S) back into TMEM, dQ += dS K with K read MN-major from its tile;
-//     the elementwise warps then scale dQ by alpha and store it.
+//     the tile's set and each half of it, S = Q K_h^T and dP = dO V_h^T (N = 64)
+//     into buffer (t & 1), dS (16-bit) packed over S, dQ += dS K_h with K read
+//     MN-major from its tile; the elementwise warps then scale dQ by alpha.
 //   dK/dV kernel, one unit per (sequence, head, key tile): for every query tile
-//     whose key-tile set holds this key tile, S^T = K Q^T and dP^T = V dO^T,
-//     P^T and dS^T (packed over S^T and dP^T), dV += P^T dO and dK += dS^T Q
-//     with dO and Q read MN-major; then dV * attn_scale and dK * alpha.
-// Query tiles follow the forward's layout (q_layout): context rows may sit on
-// the top lanes of a sequence's last query tile, and that tile's Q and dO then
-// arrive as 8-row TMA boxes.  Every wait is bounded (2 s); a timeout sets the
-// device error word and every role stops.
+//     whose key-tile set holds this key tile (a bit word per 32 query tiles,
+//     written by the scheduler) and each half of it, S^T = K Q_h^T and
+//     dP^T = V dO_h^T, P^T and dS^T packed over them, dV += P^T dO_h and
+//     dK += dS^T Q_h with dO and Q read MN-major; then dV * attn_scale and
+//     dK * alpha.
+// TMEM: buffer b at columns [128 b, 128 b + 128) (scores, then the score
+// gradients at +64), accumulators from column 256.  Query tiles follow the
+// forward's layout (q_layout): context rows may sit on the top lanes of a
+// sequence's last query tile, and that tile's Q and dO then arrive as 8-row
+// TMA boxes.  Every wait is bounded (2 s); a timeout sets the device error word
+// and every role stops.
 #pragma once
 #include "hstu_fwd_kernel.cuh"
 #include "hstu_launch.h"
@@ -33,6 +40,8 @@
 namespace hstu {
 
 constexpr int kBwdThreads = 320;   // producer, MMA, two elementwise warpgroups
+constexpr int kHalf = 64;          // columns of a half tile
+constexpr int kHalfBytes = kHalf * 128;   // rows of a half tile inside a 128-row swizzled chunk
 
 template <int D, int DV>
 struct BwdCfg {
@@ -44,16 +53,26 @@ struct BwdCfg {
   static constexpr int STAGES = 2;
   static constexpr int SMEM_BYTES = (TQ + TV) * (1 + STAGES) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(D % 16 == 0 && DV % 32 == 0 && 256 + D + DV <= TMEM_COLS, "backward head dimensions");
+  static constexpr uint32_t ACC = 256;          // first accumulator column
+  static_assert(D % 32 == 0 && DV % 32 == 0 && ACC + D + DV <= TMEM_COLS, "backward head dimensions");
 };
 
+constexpr int kBwdEwWarps = 8;
+
 struct BwdCtl {
-  uint64_t one_full, one_empty;        // dQ kernel: Q + dO of the unit; dK/dV kernel: K + V
+  uint64_t one_full, one_empty;           // dQ kernel: Q + dO of the unit; dK/dV kernel: K + V
   uint64_t ring_full[2], ring_empty[2];   // dQ kernel: K + V per key tile; dK/dV kernel: Q + dO
-  uint64_t s_full, p_full;             // both score products ready / the 16-bit operands written
-  uint64_t acc_full, acc_empty;        // accumulators complete / read out
+  uint64_t s_full[2], p_full[2];          // per TMEM buffer: score products ready / 16-bit operands written
+  uint64_t acc_full, acc_empty;           // accumulators complete / read out
+  uint64_t sched_full[2], sched_empty[2];   // claimed units: published by the producer / taken by all
+  int sched[2];                             // unit index, or -1 after the last
   uint32_t tmem_base;
   volatile int abort_flag;
+  // dK/dV elementwise warps: per warp, its 32 query columns' softmax
+  // statistics (lse in log2 units, delta / attn_scale) and allowed key
+  // intervals (lo, hi, diagonal key), read back as broadcasts
+  int4 col_rng[kBwdEwWarps][32];
+  alignas(16) float2 col_stat[kBwdEwWarps][32];   // read two columns at a time as float4
 };
 
 __device__ __forceinline__ bool bwd_wait(BwdCtl& ctl, const BwdParams& p, uint64_t* bar, uint32_t parity) {
@@ -90,22 +109,58 @@ __device__ __forceinline__ BwdUnit decode_bwd_unit(const BwdParams& p, int4 w) {
   return u;
 }
 
-// The query-tile record the scheduler wrote for tile m of sequence b.
-struct QTileRec {
-  TileSet ts;
-  TileBounds tb;
-};
-__device__ __forceinline__ QTileRec load_qtile(const BwdParams& p, int b, int m) {
-  const int4* r = reinterpret_cast<const int4*>(p.qtiles + static_cast<long long>(p.qtile_base[b] + m) * kQTileInts);
-  const int4 a = r[0], c = r[1], d = r[2];
-  QTileRec q;
-  q.ts.lo0 = a.x; q.ts.hi0 = a.y; q.ts.lo1 = a.z; q.ts.hi1 = a.w;
-  q.ts.lo2 = c.x; q.ts.hi2 = c.y; q.ts.count = c.z;
-  q.tb.LO = c.w; q.tb.HI = d.x; q.tb.maxLO = d.y; q.tb.minHI = d.z;
-  return q;
+// Producer: claims the next unit from the global counter and publishes its
+// index (-1 once the queue is drained) into the ring.
+__device__ __forceinline__ bool sched_publish(BwdCtl& ctl, const BwdParams& p, int* counter, int n_units,
+                                              int& s_it, int& ui) {
+  const int slot = s_it & 1;
+  if (!bwd_wait(ctl, p, &ctl.sched_empty[slot], ((s_it >> 1) & 1) ^ 1)) return false;
+  const int x = atomicAdd(counter, 1);
+  ui = x < n_units ? x : -1;
+  ctl.sched[slot] = ui;
+  ptx::mbar_arrive(&ctl.sched_full[slot]);
+  ++s_it;
+  return true;
 }
-__device__ __forceinline__ bool tileset_has(const TileSet& ts, int n) {
-  return (n >= ts.lo0 && n < ts.hi0) | (n >= ts.lo1 && n < ts.hi1) | (n >= ts.lo2 && n < ts.hi2);
+// MMA and elementwise warps: the next published unit (-1: none left).
+__device__ __forceinline__ bool sched_take(BwdCtl& ctl, const BwdParams& p, int lane, int& s_it, int& ui) {
+  const int slot = s_it & 1;
+  if (!bwd_warp_wait(ctl, p, &ctl.sched_full[slot], (s_it >> 1) & 1)) return false;
+  ui = *reinterpret_cast<volatile int*>(&ctl.sched[slot]);
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(&ctl.sched_empty[slot]);
+  ++s_it;
+  return true;
+}
+
+// Member words of a key-tile unit: bit m % 32 of word m / 32 is query tile m.
+struct MemberWords {
+  const unsigned* w;
+  int n;   // words
+};
+__device__ __forceinline__ MemberWords member_words(const BwdParams& p, const BwdUnit& u) {
+  MemberWords mw;
+  mw.n = (u.L.nq + 31) / 32;
+  mw.w = p.kv_mask + p.kv_mask_base[u.b] + static_cast<long long>(u.t) * mw.n;
+  return mw;
+}
+__device__ __forceinline__ int member_count(const MemberWords& mw) {
+  int c = 0;
+  for (int i = 0; i < mw.n; ++i) c += __popc(mw.w[i]);
+  return c;
+}
+
+// Full-tile bounds of query tile m of sequence b, as the scheduler recorded them.
+__device__ __forceinline__ TileBounds load_qtile_bounds(const BwdParams& p, int b, int m) {
+  const int* r = p.qtiles + static_cast<long long>(p.qtile_base[b] + m) * kQTileInts;
+  const int4 c = *reinterpret_cast<const int4*>(r + 4);
+  const int4 d = *reinterpret_cast<const int4*>(r + 8);
+  TileBounds tb;
+  tb.LO = c.w;
+  tb.HI = d.x;
+  tb.maxLO = d.y;
+  tb.minHI = d.z;
+  return tb;
 }
 
 // TMA of a query-side tile (Q or dO) of query tile m in the forward's lane layout.
@@ -125,30 +180,75 @@ __device__ __forceinline__ void load_query_tile(const CUtensorMap* m128, const C
   }
 }
 
-// C[tmem] (+)= A B^T, both K-major 128-row tiles in shared memory, KS k-steps.
+// C[tmem] = A B^T over KS k-steps: A a 128-row tile, B 64 rows starting at
+// b_base (a half of a 128-row tile), both K-major 128-byte-swizzled chunks.
 template <int KS>
-__device__ __forceinline__ void mma_ss_kmajor(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
+__device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
   const uint64_t ad0 = ptx::sdesc_sw128(a_base, 16, 1024), bd0 = ptx::sdesc_sw128(b_base, 16, 1024);
+  auto off = [](int ks) { return static_cast<uint64_t>(((ks >> 2) * (kBlockN * 128) + (ks & 3) * 32) >> 4); };
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    const uint64_t off = static_cast<uint64_t>(((ks >> 2) * (kBlockN * 128) + (ks & 3) * 32) >> 4);
-    ptx::umma_ss(d_tmem, ad0 + off, bd0 + off, idesc, ks > 0 ? 1u : 0u);
+  for (int g = 0; g + 8 <= KS; g += 8) {
+    uint64_t ad[8], bd[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { ad[j] = ad0 + off(g + j); bd[j] = bd0 + off(g + j); }
+    ptx::umma_ss_x8(d_tmem, ad, bd, idesc, g > 0 ? 1u : 0u);
+  }
+  if constexpr (KS % 8 != 0) {
+    static_assert(KS % 8 == 4, "k-steps");
+    constexpr int g = KS / 8 * 8;
+    uint64_t ad[4], bd[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { ad[j] = ad0 + off(g + j); bd[j] = bd0 + off(g + j); }
+    ptx::umma_ss_x4(d_tmem, ad, bd, idesc, g > 0 ? 1u : 0u);
   }
 }
-// C[tmem] (+)= A B with A (128 x 128, 16-bit) packed in TMEM at a_tmem the way
-// the elementwise warps write it, and B a 128-row tile in shared memory read
-// MN-major (K = its rows, N = its columns).
-__device__ __forceinline__ void mma_ts_mnmajor(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, uint32_t idesc,
-                                               bool accumulate) {
+// C[tmem] (+)= A B over one half tile: A (128 x 64, 16-bit) packed in TMEM by
+// the elementwise warps (warpgroup w's 32 columns at a_tmem + 32 w, 16 columns
+// each), B 64 rows of a tile from b_base read MN-major (K = its rows).
+__device__ __forceinline__ void mma_half_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, uint32_t idesc,
+                                            bool accumulate) {
   const uint64_t bd0 = ptx::sdesc_sw128(b_base, kBlockN * 128, 1024);
-  uint32_t pa[8];
-  uint64_t vd[8];
+  uint32_t pa[4];
+  uint64_t bd[4];
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    pa[kk] = a_tmem + (kk >> 2) * 64 + (kk & 3) * 8;
-    vd[kk] = bd0 + static_cast<uint64_t>((kk * 2048) >> 4);
+  for (int kk = 0; kk < 4; ++kk) {
+    pa[kk] = a_tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+    bd[kk] = bd0 + static_cast<uint64_t>((kk * 2048) >> 4);
   }
-  ptx::umma_ts_x8(d_tmem, pa, vd, idesc, accumulate ? 1u : 0u);
+  ptx::umma_ts_x4(d_tmem, pa, bd, idesc, accumulate ? 1u : 0u);
+}
+
+// SiLU and its derivative for the 32 scores of one row, on packed bf16 pairs
+// (the forward's SiLU arithmetic): with h = alpha s / 2, t = tanh(h),
+// sig = (1 + t) / 2, SiLU(x) = h (1 + t) and SiLU'(x) = sig + SiLU(x) (1 - sig).
+// pa receives SiLU(x) (when WANT_A), pr receives dp * SiLU'(x); pairs whose bit
+// in `allow` is clear give 0 (MASKED).
+template <bool WANT_A, bool MASKED>
+__device__ __forceinline__ void silu_bwd_bf16(const uint32_t (&sv)[32], const uint32_t (&dv)[32], uint32_t ha2,
+                                              uint32_t allow, uint32_t (&pa)[16], uint32_t (&pr)[16]) {
+  constexpr uint32_t kHalf2 = 0x3F003F00u, kNegHalf2 = 0xBF00BF00u;   // bf16 pairs (0.5, 0.5), (-0.5, -0.5)
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    uint32_t h, t, sg, a, om, d, g, r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "r"(sv[2 * k + 1]), "r"(sv[2 * k]));
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h) : "r"(ha2));
+    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t) : "r"(h));
+    asm("fma.rn.bf16x2 %0, %1, %2, %2;" : "=r"(sg) : "r"(t), "r"(kHalf2));
+    asm("fma.rn.bf16x2 %0, %1, %2, %1;" : "=r"(a) : "r"(h), "r"(t));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(om) : "r"(t), "r"(kNegHalf2), "r"(kHalf2));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(om), "r"(sg));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(g) : "r"(dv[2 * k + 1]), "r"(dv[2 * k]));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(g), "r"(d));
+    if constexpr (MASKED) {
+      const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(allow << (31 - 2 * k)) >> 31);
+      const uint32_t hi = static_cast<uint32_t>(static_cast<int32_t>(allow << (30 - 2 * k)) >> 31);
+      const uint32_t keep = (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
+      a &= keep;
+      r &= keep;
+    }
+    if constexpr (WANT_A) pa[k] = a;
+    pr[k] = r;
+  }
 }
 
 __device__ __forceinline__ float tanh_approx(float x) {
@@ -156,6 +256,55 @@ __device__ __forceinline__ float tanh_approx(float x) {
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// Teardown shared by both kernels: after an abort let copies and MMAs in
+// flight land, then free TMEM.
+__device__ __forceinline__ void bwd_teardown(BwdCtl& ctl, int tid, int warp, uint32_t tmem, uint32_t cols) {
+  if (ctl.abort_flag && tid == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, cols);
+  }
+}
+
+__device__ __forceinline__ void bwd_init(BwdCtl& ctl, int tid, int warp) {
+  if (tid == 0) {
+    ptx::mbar_init(&ctl.one_full, 1);
+    ptx::mbar_init(&ctl.one_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&ctl.ring_full[i], 1);
+      ptx::mbar_init(&ctl.ring_empty[i], 1);
+      ptx::mbar_init(&ctl.s_full[i], 1);
+      ptx::mbar_init(&ctl.p_full[i], kEwThreads);
+    }
+    ptx::mbar_init(&ctl.acc_full, 1);
+    ptx::mbar_init(&ctl.acc_empty, kEwThreads);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&ctl.sched_full[i], 1);
+      ptx::mbar_init(&ctl.sched_empty[i], 1 + kBwdEwWarps);   // the MMA warp and the elementwise warps
+    }
+    ctl.abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl.tmem_base, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+}
+
+}  // namespace hstu
+
+namespace hstu {
 
 // ---------------------------------------------------------------------------------- dQ
 template <int D, int DV, bool BF16, bool SOFTMAX>
@@ -173,131 +322,145 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sDO = smem + Cfg::TQ;
   uint8_t* sKV = sDO + Cfg::TV;          // ring: K then V of a key tile per stage
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    ptx::mbar_init(&ctl.one_full, 1);
-    ptx::mbar_init(&ctl.one_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&ctl.ring_full[i], 1);
-      ptx::mbar_init(&ctl.ring_empty[i], 1);
-    }
-    ptx::mbar_init(&ctl.s_full, 1);
-    ptx::mbar_init(&ctl.p_full, kEwThreads);
-    ptx::mbar_init(&ctl.acc_full, 1);
-    ptx::mbar_init(&ctl.acc_empty, kEwThreads);
-    ctl.abort_flag = 0;
-    ptx::fence_barrier_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(&ctl.tmem_base, Cfg::TMEM_COLS);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem = ctl.tmem_base;   // S [0,128), dP [128,256), dQ [256, 256 + D)
+  bwd_init(ctl, tid, warp);
+  const uint32_t tmem = ctl.tmem_base;   // buffers [0, 256), dQ [256, 256 + D)
   ptx::grid_dependency_wait();
   const int n_units = p.ws_header[kWsUnits];
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer + unit claims
     if (lane == 0) {
-      int one_it = 0, kv_it = 0;
-      bool ok = true;
-      for (int ui = blockIdx.x; ui < n_units && ok && !ctl.abort_flag; ui += gridDim.x) {
-        const BwdUnit u = decode_bwd_unit(p, p.units[ui]);
+      int s_it = 0, one_it = 0, kv_it = 0, ui = -1;
+      bool ok = sched_publish(ctl, p, p.ws_header + kWsCounter, n_units, s_it, ui);
+      BwdUnit u;
+      if (ok && ui >= 0) u = decode_bwd_unit(p, p.units[ui]);
+      while (ok && ui >= 0 && !ctl.abort_flag) {
         const TileSet ts = query_tile_kv_tiles(u.s, u.L, u.t);
-        if (ts.count == 0) continue;
-        if (!bwd_wait(ctl, p, &ctl.one_empty, (one_it & 1) ^ 1)) break;
-        ptx::mbar_arrive_expect_tx(&ctl.one_full, Cfg::TQ + Cfg::TV);
-        load_query_tile(&tm_q, &tm_q8, sQ, &ctl.one_full, u.s, u.L, u.t, u.h * D, Cfg::KCH);
-        load_query_tile(&tm_do, &tm_do8, sDO, &ctl.one_full, u.s, u.L, u.t, u.h * DV, Cfg::VCH);
-        ++one_it;
-        for (int k = 0; k < ts.count; ++k) {
-          const int st = kv_it & 1;
-          if (!bwd_wait(ctl, p, &ctl.ring_empty[st], ((kv_it >> 1) & 1) ^ 1)) { ok = false; break; }
-          const int krow = u.s.kv0 + tileset_at(ts, k) * kBlockN;
-          uint8_t* dst = sKV + st * (Cfg::TQ + Cfg::TV);
-          ptx::mbar_arrive_expect_tx(&ctl.ring_full[st], Cfg::TQ + Cfg::TV);
-          for (int kc = 0; kc < Cfg::KCH; ++kc)
-            ptx::tma_load_2d(dst + kc * Cfg::CHUNK, &tm_k, &ctl.ring_full[st], u.h * D + kc * 64, krow);
-          for (int kc = 0; kc < Cfg::VCH; ++kc)
-            ptx::tma_load_2d(dst + Cfg::TQ + kc * Cfg::CHUNK, &tm_v, &ctl.ring_full[st], u.h * DV + kc * 64, krow);
-          ++kv_it;
+        if (ts.count > 0) {
+          if (!bwd_wait(ctl, p, &ctl.one_empty, (one_it & 1) ^ 1)) break;
+          ptx::mbar_arrive_expect_tx(&ctl.one_full, Cfg::TQ + Cfg::TV);
+          load_query_tile(&tm_q, &tm_q8, sQ, &ctl.one_full, u.s, u.L, u.t, u.h * D, Cfg::KCH);
+          load_query_tile(&tm_do, &tm_do8, sDO, &ctl.one_full, u.s, u.L, u.t, u.h * DV, Cfg::VCH);
+          ++one_it;
+          for (int k = 0; k < ts.count; ++k) {
+            const int st = kv_it & 1;
+            if (!bwd_wait(ctl, p, &ctl.ring_empty[st], ((kv_it >> 1) & 1) ^ 1)) { ok = false; break; }
+            const int krow = u.s.kv0 + tileset_at(ts, k) * kBlockN;
+            uint8_t* dst = sKV + st * (Cfg::TQ + Cfg::TV);
+            ptx::mbar_arrive_expect_tx(&ctl.ring_full[st], Cfg::TQ + Cfg::TV);
+            for (int kc = 0; kc < Cfg::KCH; ++kc)
+              ptx::tma_load_2d(dst + kc * Cfg::CHUNK, &tm_k, &ctl.ring_full[st], u.h * D + kc * 64, krow);
+            for (int kc = 0; kc < Cfg::VCH; ++kc)
+              ptx::tma_load_2d(dst + Cfg::TQ + kc * Cfg::CHUNK, &tm_v, &ctl.ring_full[st], u.h * DV + kc * 64,
+                               krow);
+            ++kv_it;
+          }
+          if (!ok) break;
+        }
+        // the next unit: claimed now, its Q and dO prefetched into L2 while
+        // this unit's last tiles run
+        if (!sched_publish(ctl, p, p.ws_header + kWsCounter, n_units, s_it, ui)) break;
+        if (ui >= 0) {
+          u = decode_bwd_unit(p, p.units[ui]);
+          if (!(u.L.ctx_lane0 >= 0 && u.t == u.L.nq - 1)) {
+            for (int kc = 0; kc < Cfg::KCH; ++kc)
+              ptx::tma_prefetch_2d(&tm_q, u.h * D + kc * 64, u.s.q0 + u.t * kBlockM);
+            for (int kc = 0; kc < Cfg::VCH; ++kc)
+              ptx::tma_prefetch_2d(&tm_do, u.h * DV + kc * 64, u.s.q0 + u.t * kBlockM);
+          }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Half tile i of the unit (key tile i / 2, rows 64 (i % 2) of it) goes to
+    // buffer t & 1.  Its score products are issued before the dQ product of
+    // half tile i - 1, so the elementwise warps find the next scores ready.
     const bool leader = ptx::elect_one_sync();
-    constexpr uint32_t idesc_s = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
+    constexpr uint32_t idesc_s = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kHalf);
     constexpr uint32_t idesc_dq = ptx::idesc_f16_f32acc(BF16, true, kBlockM, D);
     const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sDO), kv_base = ptx::smem_u32(sKV);
-    int one_it = 0, kv_it = 0, t_it = 0, u_it = 0;
+    int s_it = 0, one_it = 0, kv_it = 0, t_it = 0, u_it = 0, ui = -1;
     bool ok = true;
-    for (int ui = blockIdx.x; ui < n_units && ok && !ctl.abort_flag; ui += gridDim.x) {
+    while (ok && !ctl.abort_flag) {
+      if (!sched_take(ctl, p, lane, s_it, ui) || ui < 0) break;
       const BwdUnit u = decode_bwd_unit(p, p.units[ui]);
       const int nt = query_tile_kv_tiles(u.s, u.L, u.t).count;
       if (nt == 0) continue;
       if (!bwd_warp_wait(ctl, p, &ctl.one_full, one_it & 1)) break;
       ptx::tc_fence_after();
-      for (int t = 0; t < nt; ++t) {
-        const int st = kv_it & 1;
-        if (!bwd_warp_wait(ctl, p, &ctl.ring_full[st], (kv_it >> 1) & 1)) { ok = false; break; }
+      const int n_sub = 2 * nt;
+      // dQ += dS K for half tile i (TMEM buffer of half tile t)
+      auto dq_step = [&](int i, int t) -> bool {
+        const int b = t & 1, kt = kv_it + (i >> 1), st = kt & 1, hh = i & 1;
+        if (!bwd_warp_wait(ctl, p, &ctl.p_full[b], (t >> 1) & 1)) return false;
         ptx::tc_fence_after();
-        const uint32_t k_base = kv_base + st * (Cfg::TQ + Cfg::TV);
-        if (leader) {
-          mma_ss_kmajor<D / 16>(tmem, q_base, k_base, idesc_s);                  // S = Q K^T
-          mma_ss_kmajor<DV / 16>(tmem + 128, do_base, k_base + Cfg::TQ, idesc_s);  // dP = dO V^T
-          ptx::umma_commit(&ctl.s_full);
-        }
-        __syncwarp();
-        if (!bwd_warp_wait(ctl, p, &ctl.p_full, t_it & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        if (t == 0) {
-          if (!bwd_warp_wait(ctl, p, &ctl.acc_empty, (u_it & 1) ^ 1)) { ok = false; break; }
+        if (i == 0) {
+          if (!bwd_warp_wait(ctl, p, &ctl.acc_empty, (u_it & 1) ^ 1)) return false;
           ptx::tc_fence_after();
         }
         if (leader) {
-          mma_ts_mnmajor(tmem + 256, tmem, k_base, idesc_dq, t > 0);   // dQ += dS K
-          ptx::umma_commit(&ctl.ring_empty[st]);
-          if (t == nt - 1) {
-            ptx::umma_commit(&ctl.one_empty);
-            ptx::umma_commit(&ctl.acc_full);
-          }
+          const uint32_t k_base = kv_base + st * (Cfg::TQ + Cfg::TV) + hh * kHalfBytes;
+          mma_half_ts(tmem + Cfg::ACC, tmem + 128 * b, k_base, idesc_dq, i > 0);
+          if (hh == 1) ptx::umma_commit(&ctl.ring_empty[st]);
         }
         __syncwarp();
-        ++kv_it;
-        ++t_it;
+        return true;
+      };
+      for (int i = 0; i < n_sub && ok; ++i) {
+        const int t = t_it + i, b = t & 1, kt = kv_it + (i >> 1), st = kt & 1, hh = i & 1;
+        if (hh == 0) {
+          if (!bwd_warp_wait(ctl, p, &ctl.ring_full[st], (kt >> 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+        }
+        if (leader) {
+          const uint32_t k_base = kv_base + st * (Cfg::TQ + Cfg::TV) + hh * kHalfBytes;
+          mma_scores<D / 16>(tmem + 128 * b, q_base, k_base, idesc_s);                 // S = Q K_h^T
+          mma_scores<DV / 16>(tmem + 128 * b + 64, do_base, k_base + Cfg::TQ, idesc_s);  // dP = dO V_h^T
+          if (i == n_sub - 1) ptx::umma_commit(&ctl.one_empty);   // Q and dO are no longer read
+          ptx::umma_commit(&ctl.s_full[b]);
+        }
+        __syncwarp();
+        if (i > 0 && !dq_step(i - 1, t - 1)) { ok = false; break; }
       }
+      if (!ok || !dq_step(n_sub - 1, t_it + n_sub - 1)) break;
+      if (leader) ptx::umma_commit(&ctl.acc_full);
+      __syncwarp();
+      t_it += n_sub;
+      kv_it += nt;
       ++one_it;
       ++u_it;
     }
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
+    // Warpgroup wg takes columns [32 wg, 32 wg + 32) of each half tile; lanes
+    // are query rows.  dS is kept without attn_scale (the epilogue applies
+    // alpha * attn_scale).
     const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int rloc = quarter * 32 + lane;
-    const int c0 = wg * 64;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float alpha = p.alpha;
+    const float half_alpha = 0.5f * p.alpha;
+    uint32_t ha2 = 0;
+    if constexpr (BF16) ha2 = pack2<true>(half_alpha, half_alpha);
     constexpr float kLog2e = 1.4426950408889634f;
-    int t_it = 0, u_it = 0;
+    int s_it = 0, t_it = 0, u_it = 0, ui = -1;
     bool ok = true;
-    for (int ui = blockIdx.x; ui < n_units && ok && !ctl.abort_flag; ui += gridDim.x) {
+    while (ok && !ctl.abort_flag) {
+      if (!sched_take(ctl, p, lane, s_it, ui) || ui < 0) break;
       const BwdUnit u = decode_bwd_unit(p, p.units[ui]);
       const TileSet ts = query_tile_kv_tiles(u.s, u.L, u.t);
-      const TileBounds tb = q_tile_bounds(u.s, u.L, u.t);
       const int nt = ts.count;
       const int qr = q_row(u.s, u.L, u.t, rloc);
       const bool valid = qr >= 0;
       const int row = valid ? qr : 0;
       const long long grow = static_cast<long long>(u.s.q0) + row;
-      uint16_t* dq_row = reinterpret_cast<uint16_t*>(p.dq) + grow * p.dq_stride + u.h * D;
+      uint16_t* dq_row = reinterpret_cast<uint16_t*>(p.dq) + grow * p.dq_stride + u.h * D + wg * (D / 2);
       if (nt == 0) {   // no key reaches this tile: dQ = 0
         if (valid) {
 #pragma unroll
-          for (int c = 0; c < D / 2; c += 8)
-            *reinterpret_cast<uint4*>(dq_row + wg * (D / 2) + c) = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < D / 2; c += 8) *reinterpret_cast<uint4*>(dq_row + c) = make_uint4(0u, 0u, 0u, 0u);
         }
         continue;
       }
@@ -306,14 +469,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int r_diag = row_diag_key(u.s, row);
       int r_ctx = u.s.c;
       if (!valid) { r_lo = r_hi = 0; r_diag = -1; r_ctx = 0; }
-      float lse2 = 0.f, dlt = 0.f;
+      float lse2 = 0.f, dlt = 0.f;   // softmax: lse (log2 units), delta / attn_scale
       if constexpr (SOFTMAX) {
         if (valid) {
           lse2 = p.lse[static_cast<long long>(u.h) * p.total_q + grow] * kLog2e;
-          dlt = p.delta[static_cast<long long>(u.h) * p.total_q + grow];
+          dlt = p.delta[static_cast<long long>(u.h) * p.total_q + grow] / u.scale;
         }
       }
-      const FullTiles ft = full_tile_ranges(u.s, tb);
+      const FullTiles ft = full_tile_ranges(u.s, q_tile_bounds(u.s, u.L, u.t));
       for (int idx = 0; idx < nt && ok; ++idx) {
         const int n = tileset_at(ts, idx);
         const bool full = n < ft.ctx_hi || (n >= ft.lo && n < ft.hi);
@@ -323,62 +486,66 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         rm.lo = r_lo - j0;
         rm.span = static_cast<uint32_t>(r_hi - r_lo);
         rm.diag = r_diag >= 0 ? r_diag - j0 : -1000000;
-        if (!bwd_warp_wait(ctl, p, &ctl.s_full, t_it & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t sv[32], dv[32];
-          ptx::tmem_ld32(tmem + lane_base + c0 + 32 * q, sv);
-          ptx::tmem_ld32(tmem + lane_base + 128 + c0 + 32 * q, dv);
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          const int t = t_it++, b = t & 1;
+          const uint32_t sb = tmem + lane_base + 128 * b + 32 * wg;
+          const uint32_t mb = full ? 0xFFFFFFFFu : rm.bits32(kHalf * hh + 32 * wg);
+          if (!bwd_warp_wait(ctl, p, &ctl.s_full[b], (t >> 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          uint32_t sv[32], dv[32], pk[16];
+          ptx::tmem_ld32(sb, sv);
+          ptx::tmem_ld32(sb + 64, dv);
           ptx::tmem_ld_wait(sv);
           ptx::tmem_ld_wait(dv);
-          const uint32_t mb = full ? 0xFFFFFFFFu : rm.bits32(c0 + 32 * q);
-          uint32_t pk[16];
+          if constexpr (BF16 && !SOFTMAX) {
+            if (full) silu_bwd_bf16<false, false>(sv, dv, ha2, mb, pk, pk);
+            else silu_bwd_bf16<false, true>(sv, dv, ha2, mb, pk, pk);
+          } else {
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            float ds[2];
+            for (int k = 0; k < 32; k += 2) {
+              float ds[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float s = __uint_as_float(sv[k + e]);
-              const float dp = __uint_as_float(dv[k + e]);
-              float r;
-              if constexpr (SOFTMAX) {
-                const float pr = ex2_approx(fmaf(s, alpha * kLog2e, -lse2));
-                r = pr * fmaf(dp, u.scale, -dlt);
-              } else {
-                const float x = alpha * s;
-                const float sig = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-                r = dp * u.scale * sig * fmaf(x, 1.f - sig, 1.f);
+              for (int e = 0; e < 2; ++e) {
+                const float s = __uint_as_float(sv[k + e]);
+                const float g = __uint_as_float(dv[k + e]);
+                float r;
+                if constexpr (SOFTMAX) {
+                  r = ex2_approx(fmaf(s, alpha * kLog2e, -lse2)) * (g - dlt);
+                } else {
+                  const float sig = fmaf(0.5f, tanh_approx(s * half_alpha), 0.5f);
+                  const float xs = s * alpha * sig;
+                  r = g * (sig + fmaf(-xs, sig, xs));
+                }
+                ds[e] = ((mb >> (k + e)) & 1u) ? r : 0.f;
               }
-              ds[e] = ((mb >> (k + e)) & 1u) ? r : 0.f;
+              pk[k >> 1] = pack2<BF16>(ds[0], ds[1]);
             }
-            pk[k >> 1] = pack2<BF16>(ds[0], ds[1]);
           }
-          ptx::tmem_st16(tmem + lane_base + c0 + 16 * q, pk);
+          ptx::tmem_st16(sb, pk);
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&ctl.p_full[b]);
         }
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.p_full);
-        ++t_it;
       }
       if (!ok) break;
-      // dQ * alpha out of TMEM: this warpgroup's half of the D columns
+      // dQ * alpha * attn_scale out of TMEM: this warpgroup's half of the D columns
       if (!bwd_warp_wait(ctl, p, &ctl.acc_full, u_it & 1)) break;
       ptx::tc_fence_after();
+      const float mul = alpha * u.scale;
 #pragma unroll 1
       for (int c = 0; c < D / 2; c += 32) {
         uint32_t o[32];
-        ptx::tmem_ld32(tmem + lane_base + 256 + wg * (D / 2) + c, o);
+        ptx::tmem_ld32(tmem + lane_base + Cfg::ACC + wg * (D / 2) + c, o);
         ptx::tmem_ld_wait(o);
         if (valid) {
-          uint32_t pk[16];
+          uint32_t q2[16];
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
-            pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * alpha, __uint_as_float(o[k + 1]) * alpha);
+            q2[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
 #pragma unroll
           for (int k = 0; k < 16; k += 4)
-            *reinterpret_cast<uint4*>(dq_row + wg * (D / 2) + c + 2 * k) =
-                make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
+            *reinterpret_cast<uint4*>(dq_row + c + 2 * k) = make_uint4(q2[k], q2[k + 1], q2[k + 2], q2[k + 3]);
         }
       }
       ptx::tc_fence_before();
@@ -386,20 +553,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++u_it;
     }
   }
-
-  if (ctl.abort_flag && tid == 0) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (ptx::globaltimer_ns() - t0 < 1000000ull) {
-    }
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
-  }
+  bwd_teardown(ctl, tid, warp, tmem, Cfg::TMEM_COLS);
 }
+
+}  // namespace hstu
+
+namespace hstu {
 
 // ---------------------------------------------------------------------------------- dK, dV
 template <int D, int DV, bool BF16, bool SOFTMAX>
@@ -415,228 +574,267 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sK = smem;                    // K then V of the unit's key tile
   uint8_t* sV = smem + Cfg::TQ;
-  uint8_t* sQD = sV + Cfg::TV;           // ring: Q then dO of a query tile per stage
+  uint8_t* sQD = sV + Cfg::TV;           // ring: Q then dO of a member query tile per stage
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    ptx::mbar_init(&ctl.one_full, 1);
-    ptx::mbar_init(&ctl.one_empty, 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&ctl.ring_full[i], 1);
-      ptx::mbar_init(&ctl.ring_empty[i], 1);
-    }
-    ptx::mbar_init(&ctl.s_full, 1);
-    ptx::mbar_init(&ctl.p_full, kEwThreads);
-    ptx::mbar_init(&ctl.acc_full, 1);
-    ptx::mbar_init(&ctl.acc_empty, kEwThreads);
-    ctl.abort_flag = 0;
-    ptx::fence_barrier_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(&ctl.tmem_base, Cfg::TMEM_COLS);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  // S^T [0,128), dP^T [128,256), dV [256, 256 + DV), dK [256 + DV, 256 + DV + D)
+  bwd_init(ctl, tid, warp);
+  // buffers [0, 256), dV [256, 256 + DV), dK [256 + DV, 256 + DV + D)
   const uint32_t tmem = ctl.tmem_base;
   ptx::grid_dependency_wait();
   const int n_units = p.ws_header[kWsKvUnits];
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer + unit claims
     if (lane == 0) {
-      int u_it = 0, q_it = 0;
-      bool ok = true;
-      for (int ui = blockIdx.x; ui < n_units && ok && !ctl.abort_flag; ui += gridDim.x) {
-        const BwdUnit u = decode_bwd_unit(p, p.kv_units[ui]);
-        if (!bwd_wait(ctl, p, &ctl.one_empty, (u_it & 1) ^ 1)) break;
-        ptx::mbar_arrive_expect_tx(&ctl.one_full, Cfg::TQ + Cfg::TV);
-        const int krow = u.s.kv0 + u.t * kBlockN;
-        for (int kc = 0; kc < Cfg::KCH; ++kc)
-          ptx::tma_load_2d(sK + kc * Cfg::CHUNK, &tm_k, &ctl.one_full, u.h * D + kc * 64, krow);
-        for (int kc = 0; kc < Cfg::VCH; ++kc)
-          ptx::tma_load_2d(sV + kc * Cfg::CHUNK, &tm_v, &ctl.one_full, u.h * DV + kc * 64, krow);
-        ++u_it;
-        for (int m = 0; m < u.L.nq; ++m) {
-          if (!tileset_has(load_qtile(p, u.b, m).ts, u.t)) continue;
-          const int st = q_it & 1;
-          if (!bwd_wait(ctl, p, &ctl.ring_empty[st], ((q_it >> 1) & 1) ^ 1)) { ok = false; break; }
-          uint8_t* dst = sQD + st * (Cfg::TQ + Cfg::TV);
-          ptx::mbar_arrive_expect_tx(&ctl.ring_full[st], Cfg::TQ + Cfg::TV);
-          load_query_tile(&tm_q, &tm_q8, dst, &ctl.ring_full[st], u.s, u.L, m, u.h * D, Cfg::KCH);
-          load_query_tile(&tm_do, &tm_do8, dst + Cfg::TQ, &ctl.ring_full[st], u.s, u.L, m, u.h * DV, Cfg::VCH);
-          ++q_it;
+      int s_it = 0, u_it = 0, q_it = 0, ui = -1;
+      bool ok = sched_publish(ctl, p, p.ws_header + kWsKvCounter, n_units, s_it, ui);
+      BwdUnit u;
+      if (ok && ui >= 0) u = decode_bwd_unit(p, p.kv_units[ui]);
+      while (ok && ui >= 0 && !ctl.abort_flag) {
+        const MemberWords mw = member_words(p, u);
+        if (member_count(mw) > 0) {
+          if (!bwd_wait(ctl, p, &ctl.one_empty, (u_it & 1) ^ 1)) break;
+          ptx::mbar_arrive_expect_tx(&ctl.one_full, Cfg::TQ + Cfg::TV);
+          const int krow = u.s.kv0 + u.t * kBlockN;
+          for (int kc = 0; kc < Cfg::KCH; ++kc)
+            ptx::tma_load_2d(sK + kc * Cfg::CHUNK, &tm_k, &ctl.one_full, u.h * D + kc * 64, krow);
+          for (int kc = 0; kc < Cfg::VCH; ++kc)
+            ptx::tma_load_2d(sV + kc * Cfg::CHUNK, &tm_v, &ctl.one_full, u.h * DV + kc * 64, krow);
+          ++u_it;
+          for (int w = 0; w < mw.n && ok; ++w) {
+            unsigned bits = mw.w[w];
+            while (bits != 0u) {
+              const int m = w * 32 + __ffs(bits) - 1;
+              bits &= bits - 1u;
+              const int st = q_it & 1;
+              if (!bwd_wait(ctl, p, &ctl.ring_empty[st], ((q_it >> 1) & 1) ^ 1)) { ok = false; break; }
+              uint8_t* dst = sQD + st * (Cfg::TQ + Cfg::TV);
+              ptx::mbar_arrive_expect_tx(&ctl.ring_full[st], Cfg::TQ + Cfg::TV);
+              load_query_tile(&tm_q, &tm_q8, dst, &ctl.ring_full[st], u.s, u.L, m, u.h * D, Cfg::KCH);
+              load_query_tile(&tm_do, &tm_do8, dst + Cfg::TQ, &ctl.ring_full[st], u.s, u.L, m, u.h * DV,
+                              Cfg::VCH);
+              ++q_it;
+            }
+          }
+          if (!ok) break;
+        }
+        // the next unit: claimed now, its K and V prefetched into L2
+        if (!sched_publish(ctl, p, p.ws_header + kWsKvCounter, n_units, s_it, ui)) break;
+        if (ui >= 0) {
+          u = decode_bwd_unit(p, p.kv_units[ui]);
+          for (int kc = 0; kc < Cfg::KCH; ++kc)
+            ptx::tma_prefetch_2d(&tm_k, u.h * D + kc * 64, u.s.kv0 + u.t * kBlockN);
+          for (int kc = 0; kc < Cfg::VCH; ++kc)
+            ptx::tma_prefetch_2d(&tm_v, u.h * DV + kc * 64, u.s.kv0 + u.t * kBlockN);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Half tile i of the unit (member query tile i / 2, rows 64 (i % 2) of it)
+    // goes to buffer t & 1; its score products are issued before the gradient
+    // products of half tile i - 1.
     const bool leader = ptx::elect_one_sync();
-    constexpr uint32_t idesc_s = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
+    constexpr uint32_t idesc_s = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kHalf);
     constexpr uint32_t idesc_dv = ptx::idesc_f16_f32acc(BF16, true, kBlockM, DV);
     constexpr uint32_t idesc_dk = ptx::idesc_f16_f32acc(BF16, true, kBlockM, D);
     const uint32_t k_base = ptx::smem_u32(sK), v_base = ptx::smem_u32(sV), qd_base = ptx::smem_u32(sQD);
-    int u_it = 0, q_it = 0, t_it = 0, a_it = 0;
+    int s_it = 0, u_it = 0, q_it = 0, t_it = 0, ui = -1;
     bool ok = true;
-    for (int ui = blockIdx.x; ui < n_units && ok && !ctl.abort_flag; ui += gridDim.x) {
+    while (ok && !ctl.abort_flag) {
+      if (!sched_take(ctl, p, lane, s_it, ui) || ui < 0) break;
       const BwdUnit u = decode_bwd_unit(p, p.kv_units[ui]);
+      const int nm = member_count(member_words(p, u));
+      if (nm == 0) continue;
       if (!bwd_warp_wait(ctl, p, &ctl.one_full, u_it & 1)) break;
       ptx::tc_fence_after();
-      int nm = 0;
-      for (int m = 0; m < u.L.nq; ++m) {
-        if (!tileset_has(load_qtile(p, u.b, m).ts, u.t)) continue;
-        const int st = q_it & 1;
-        if (!bwd_warp_wait(ctl, p, &ctl.ring_full[st], (q_it >> 1) & 1)) { ok = false; break; }
+      const int n_sub = 2 * nm;
+      // dV += P^T dO_h and dK += dS^T Q_h for half tile i (buffer of half tile t)
+      auto grad_step = [&](int i, int t) -> bool {
+        const int b = t & 1, qt = q_it + (i >> 1), st = qt & 1, hh = i & 1;
+        if (!bwd_warp_wait(ctl, p, &ctl.p_full[b], (t >> 1) & 1)) return false;
         ptx::tc_fence_after();
-        const uint32_t q_b = qd_base + st * (Cfg::TQ + Cfg::TV);
-        if (leader) {
-          mma_ss_kmajor<D / 16>(tmem, k_base, q_b, idesc_s);                    // S^T = K Q^T
-          mma_ss_kmajor<DV / 16>(tmem + 128, v_base, q_b + Cfg::TQ, idesc_s);   // dP^T = V dO^T
-          ptx::umma_commit(&ctl.s_full);
-        }
-        __syncwarp();
-        if (!bwd_warp_wait(ctl, p, &ctl.p_full, t_it & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        if (nm == 0) {
-          if (!bwd_warp_wait(ctl, p, &ctl.acc_empty, (a_it & 1) ^ 1)) { ok = false; break; }
+        if (i == 0) {
+          if (!bwd_warp_wait(ctl, p, &ctl.acc_empty, (u_it & 1) ^ 1)) return false;
           ptx::tc_fence_after();
         }
         if (leader) {
-          mma_ts_mnmajor(tmem + 256, tmem, q_b + Cfg::TQ, idesc_dv, nm > 0);         // dV += P^T dO
-          mma_ts_mnmajor(tmem + 256 + DV, tmem + 128, q_b, idesc_dk, nm > 0);       // dK += dS^T Q
-          ptx::umma_commit(&ctl.ring_empty[st]);
+          const uint32_t q_b = qd_base + st * (Cfg::TQ + Cfg::TV) + hh * kHalfBytes;
+          mma_half_ts(tmem + Cfg::ACC, tmem + 128 * b, q_b + Cfg::TQ, idesc_dv, i > 0);
+          mma_half_ts(tmem + Cfg::ACC + DV, tmem + 128 * b + 64, q_b, idesc_dk, i > 0);
+          if (hh == 1) ptx::umma_commit(&ctl.ring_empty[st]);
         }
         __syncwarp();
-        ++q_it;
-        ++t_it;
-        ++nm;
+        return true;
+      };
+      for (int i = 0; i < n_sub && ok; ++i) {
+        const int t = t_it + i, b = t & 1, qt = q_it + (i >> 1), st = qt & 1, hh = i & 1;
+        if (hh == 0) {
+          if (!bwd_warp_wait(ctl, p, &ctl.ring_full[st], (qt >> 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+        }
+        if (leader) {
+          const uint32_t q_b = qd_base + st * (Cfg::TQ + Cfg::TV) + hh * kHalfBytes;
+          mma_scores<D / 16>(tmem + 128 * b, k_base, q_b, idesc_s);                    // S^T = K Q_h^T
+          mma_scores<DV / 16>(tmem + 128 * b + 64, v_base, q_b + Cfg::TQ, idesc_s);     // dP^T = V dO_h^T
+          if (i == n_sub - 1) ptx::umma_commit(&ctl.one_empty);   // K and V are no longer read
+          ptx::umma_commit(&ctl.s_full[b]);
+        }
+        __syncwarp();
+        if (i > 0 && !grad_step(i - 1, t - 1)) { ok = false; break; }
       }
-      if (!ok) break;
-      if (leader) {
-        ptx::umma_commit(&ctl.one_empty);
-        if (nm > 0) ptx::umma_commit(&ctl.acc_full);
-      }
+      if (!ok || !grad_step(n_sub - 1, t_it + n_sub - 1)) break;
+      if (leader) ptx::umma_commit(&ctl.acc_full);
       __syncwarp();
-      if (nm > 0) ++a_it;
+      t_it += n_sub;
+      q_it += nm;
       ++u_it;
     }
   } else {
     // ------------------------------------------------------------ elementwise warpgroups
+    // Lanes are key rows; warpgroup wg takes query columns [32 wg, 32 wg + 32)
+    // of each half tile.  Lane l works out column l's row, validity, allowed
+    // key interval (partial tiles) and softmax statistics into this warp's
+    // slots of ctl.col_*, which every lane then reads as broadcasts.  dS^T is
+    // kept without attn_scale (the epilogue applies alpha * attn_scale).
     const int wg = (warp - 2) >> 2;
+    const int ew = warp - 2;
     const int quarter = warp & 3;
     const int rloc = quarter * 32 + lane;
-    const int c0 = wg * 64;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float alpha = p.alpha;
+    const float half_alpha = 0.5f * p.alpha;
+    uint32_t ha2 = 0;
+    if constexpr (BF16) ha2 = pack2<true>(half_alpha, half_alpha);
     constexpr float kLog2e = 1.4426950408889634f;
-    int t_it = 0, a_it = 0;
+    const float4* stat4 = reinterpret_cast<const float4*>(&ctl.col_stat[ew][0]);
+    int s_it = 0, t_it = 0, a_it = 0, ui = -1;
     bool ok = true;
-    for (int ui = blockIdx.x; ui < n_units && ok && !ctl.abort_flag; ui += gridDim.x) {
+    while (ok && !ctl.abort_flag) {
+      if (!sched_take(ctl, p, lane, s_it, ui) || ui < 0) break;
       const BwdUnit u = decode_bwd_unit(p, p.kv_units[ui]);
+      const MemberWords mw = member_words(p, u);
+      const int nm = member_count(mw);
       const int j = u.t * kBlockN + rloc;   // this lane's key row
       const bool kvalid = j < u.s.Lkv;
       const long long krow = static_cast<long long>(u.s.kv0) + j;
-      uint16_t* dv_row = reinterpret_cast<uint16_t*>(p.dv) + krow * p.dv_stride + u.h * DV;
-      uint16_t* dk_row = reinterpret_cast<uint16_t*>(p.dk) + krow * p.dk_stride + u.h * D;
-      int nm = 0;
-      for (int m = 0; m < u.L.nq && ok; ++m) {
-        const QTileRec rec = load_qtile(p, u.b, m);
-        if (!tileset_has(rec.ts, u.t)) continue;
-        const FullTiles ft = full_tile_ranges(u.s, rec.tb);
-        const bool full = u.t < ft.ctx_hi || (u.t >= ft.lo && u.t < ft.hi);
-        if (!bwd_warp_wait(ctl, p, &ctl.s_full, t_it & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-#pragma unroll 1
-        for (int q = 0; q < 2; ++q) {
-          // column (query) of this lane: its row, validity and, for a partial
-          // block, its allowed key interval, shared with the other lanes
-          const int col = c0 + 32 * q + lane;
-          const int qi = q_row(u.s, u.L, m, col);
-          const uint32_t cvalid = __ballot_sync(0xffffffffu, qi >= 0);
-          int c_lo = 0, c_hi = 0, c_dg = -1;
-          if (!full && qi >= 0) {
-            row_uih_keys(u.s, qi, c_lo, c_hi);
-            c_dg = row_diag_key(u.s, qi);
-          }
-          float c_lse2 = 0.f, c_dlt = 0.f;
-          if constexpr (SOFTMAX) {
-            if (qi >= 0) {
-              const long long gq = static_cast<long long>(u.h) * p.total_q + u.s.q0 + qi;
-              c_lse2 = p.lse[gq] * kLog2e;
-              c_dlt = p.delta[gq];
-            }
-          }
-          uint32_t sv[32], dv[32];
-          ptx::tmem_ld32(tmem + lane_base + c0 + 32 * q, sv);
-          ptx::tmem_ld32(tmem + lane_base + 128 + c0 + 32 * q, dv);
-          ptx::tmem_ld_wait(sv);
-          ptx::tmem_ld_wait(dv);
-          uint32_t pp[16], pd[16];
+      uint16_t* dv_row = reinterpret_cast<uint16_t*>(p.dv) + krow * p.dv_stride + u.h * DV + wg * (DV / 2);
+      uint16_t* dk_row = reinterpret_cast<uint16_t*>(p.dk) + krow * p.dk_stride + u.h * D + wg * (D / 2);
+      if (nm == 0) {   // no query sees this key tile: dK = dV = 0
+        if (kvalid) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            float pv[2], ds[2];
+          for (int c = 0; c < DV / 2; c += 8) *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int kk = k + e;
-              bool allowed = (cvalid >> kk) & 1u;
-              if (!full) {
-                const int lo = __shfl_sync(0xffffffffu, c_lo, kk);
-                const int hi = __shfl_sync(0xffffffffu, c_hi, kk);
-                const int dg = __shfl_sync(0xffffffffu, c_dg, kk);
-                allowed = allowed && (j < u.s.c || (j >= lo && j < hi) || j == dg);
-              }
-              const float s = __uint_as_float(sv[kk]);
-              const float dp = __uint_as_float(dv[kk]);
-              float a, r;
-              if constexpr (SOFTMAX) {
-                const float l2 = __shfl_sync(0xffffffffu, c_lse2, kk);
-                const float dl = __shfl_sync(0xffffffffu, c_dlt, kk);
-                a = ex2_approx(fmaf(s, alpha * kLog2e, -l2));
-                r = a * fmaf(dp, u.scale, -dl);
-              } else {
-                const float x = alpha * s;
-                const float sig = fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-                a = x * sig;
-                r = dp * u.scale * sig * fmaf(x, 1.f - sig, 1.f);
-              }
-              pv[e] = allowed ? a : 0.f;
-              ds[e] = allowed ? r : 0.f;
-            }
-            pp[k >> 1] = pack2<BF16>(pv[0], pv[1]);
-            pd[k >> 1] = pack2<BF16>(ds[0], ds[1]);
-          }
-          ptx::tmem_st16(tmem + lane_base + c0 + 16 * q, pp);
-          ptx::tmem_st16(tmem + lane_base + 128 + c0 + 16 * q, pd);
+          for (int c = 0; c < D / 2; c += 8) *reinterpret_cast<uint4*>(dk_row + c) = make_uint4(0u, 0u, 0u, 0u);
         }
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.p_full);
-        ++t_it;
-        ++nm;
+        continue;
+      }
+      const bool ctx_key = j < u.s.c;   // context keys are seen by every query row
+      for (int w = 0; w < mw.n && ok; ++w) {
+        unsigned bits = mw.w[w];
+        while (bits != 0u && ok) {
+          const int m = w * 32 + __ffs(bits) - 1;
+          bits &= bits - 1u;
+          const FullTiles ft = full_tile_ranges(u.s, load_qtile_bounds(p, u.b, m));
+          const bool full = u.t < ft.ctx_hi || (u.t >= ft.lo && u.t < ft.hi);
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {
+            const int t = t_it++, b = t & 1;
+            const uint32_t sb = tmem + lane_base + 128 * b + 32 * wg;
+            // this lane's column: row, validity, interval, statistics
+            const int qi = q_row(u.s, u.L, m, kHalf * hh + 32 * wg + lane);
+            const uint32_t cvalid = __ballot_sync(0xffffffffu, qi >= 0);
+            __syncwarp();   // the previous half tile's broadcasts are all read
+            if (!full) {
+              int lo = 0, hi = 0, dg = -1;
+              if (qi >= 0) {
+                row_uih_keys(u.s, qi, lo, hi);
+                dg = row_diag_key(u.s, qi);
+              }
+              ctl.col_rng[ew][lane] = make_int4(lo, hi, dg, 0);
+            }
+            if constexpr (SOFTMAX) {
+              float l2 = 0.f, dl = 0.f;
+              if (qi >= 0) {
+                const long long gq = static_cast<long long>(u.h) * p.total_q + u.s.q0 + qi;
+                l2 = p.lse[gq] * kLog2e;
+                dl = p.delta[gq] / u.scale;
+              }
+              ctl.col_stat[ew][lane] = make_float2(l2, dl);
+            }
+            __syncwarp();
+            uint32_t allow = cvalid;
+            if (!full && !ctx_key) {
+              uint32_t seen = 0u;
+#pragma unroll
+              for (int kk = 0; kk < 32; ++kk) {
+                const int4 r = ctl.col_rng[ew][kk];
+                seen |= static_cast<uint32_t>((j >= r.x && j < r.y) || j == r.z) << kk;
+              }
+              allow &= seen;
+            }
+            const bool masked = !full || cvalid != 0xFFFFFFFFu;   // warp-uniform
+            if (!bwd_warp_wait(ctl, p, &ctl.s_full[b], (t >> 1) & 1)) { ok = false; break; }
+            ptx::tc_fence_after();
+            uint32_t sv[32], dv[32], pp[16], pd[16];
+            ptx::tmem_ld32(sb, sv);
+            ptx::tmem_ld32(sb + 64, dv);
+            ptx::tmem_ld_wait(sv);
+            ptx::tmem_ld_wait(dv);
+            if constexpr (BF16 && !SOFTMAX) {
+              if (masked) silu_bwd_bf16<true, true>(sv, dv, ha2, allow, pp, pd);
+              else silu_bwd_bf16<true, false>(sv, dv, ha2, allow, pp, pd);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; k += 2) {
+                float pv[2], ds[2];
+                float4 st4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (SOFTMAX) st4 = stat4[k >> 1];   // columns k, k + 1
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const float s = __uint_as_float(sv[k + e]);
+                  const float g = __uint_as_float(dv[k + e]);
+                  float a, r;
+                  if constexpr (SOFTMAX) {
+                    const float l2 = e ? st4.z : st4.x;
+                    const float dl = e ? st4.w : st4.y;
+                    a = ex2_approx(fmaf(s, alpha * kLog2e, -l2));
+                    r = a * (g - dl);
+                  } else {
+                    const float sig = fmaf(0.5f, tanh_approx(s * half_alpha), 0.5f);
+                    a = s * alpha * sig;                   // SiLU(x)
+                    r = g * (sig + fmaf(-a, sig, a));      // SiLU'(x) = sig + x sig (1 - sig)
+                  }
+                  const bool al = (allow >> (k + e)) & 1u;
+                  pv[e] = al ? a : 0.f;
+                  ds[e] = al ? r : 0.f;
+                }
+                pp[k >> 1] = pack2<BF16>(pv[0], pv[1]);
+                pd[k >> 1] = pack2<BF16>(ds[0], ds[1]);
+              }
+            }
+            ptx::tmem_st16(sb, pp);
+            ptx::tmem_st16(sb + 64, pd);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&ctl.p_full[b]);
+          }
+        }
       }
       if (!ok) break;
-      // dV * attn_scale and dK * alpha: this warpgroup's half of each
-      if (nm > 0) {
-        if (!bwd_warp_wait(ctl, p, &ctl.acc_full, a_it & 1)) break;
-        ptx::tc_fence_after();
-      }
+      // dV * attn_scale and dK * alpha * attn_scale: this warpgroup's half of each
+      if (!bwd_warp_wait(ctl, p, &ctl.acc_full, a_it & 1)) break;
+      ptx::tc_fence_after();
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {
         const int W = part == 0 ? DV : D;
-        const float mul = part == 0 ? u.scale : alpha;
-        const uint32_t col0 = 256 + (part == 0 ? 0 : DV) + wg * (W / 2);
-        uint16_t* dst = (part == 0 ? dv_row : dk_row) + wg * (W / 2);
+        const float mul = part == 0 ? u.scale : alpha * u.scale;
+        const uint32_t col0 = Cfg::ACC + (part == 0 ? 0 : DV) + wg * (W / 2);
+        uint16_t* dst = part == 0 ? dv_row : dk_row;
 #pragma unroll 1
         for (int c = 0; c < W / 2; c += 32) {
           uint32_t o[32];
-          if (nm > 0) {
-            ptx::tmem_ld32(tmem + lane_base + col0 + c, o);
-            ptx::tmem_ld_wait(o);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = 0u;
-          }
+          ptx::tmem_ld32(tmem + lane_base + col0 + c, o);
+          ptx::tmem_ld_wait(o);
           if (kvalid) {
             uint32_t pk[16];
 #pragma unroll
@@ -648,31 +846,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
-      if (nm > 0) {
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.acc_empty);
-        ++a_it;
-      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ctl.acc_empty);
+      ++a_it;
     }
   }
-
-  if (ctl.abort_flag && tid == 0) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (ptx::globaltimer_ns() - t0 < 1000000ull) {
-    }
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
-  }
+  bwd_teardown(ctl, tid, warp, tmem, Cfg::TMEM_COLS);
 }
-
-}  // namespace hstu
-
-namespace hstu {
 
 // Host side: both backward kernels of one head dimension, the dQ kernel first.
 template <int D, bool BF16, bool SOFTMAX>

@@ -52,6 +52,7 @@ enum : int {
   kWsTilesLo = 4,    // executed (b, h, q-tile, kv-tile) blocks, int64 in slots 4-5
   kWsPairsLo = 6,    // allowed (b, h, i, j) pairs, int64 in slots 6-7 (stats only)
   kWsKvUnits = 8,    // backward: number of key-tile work units
+  kWsKvCounter = 9,  // backward: dynamic work counter of the dK/dV kernel
   kWsHeaderInts = 64,
 };
 
@@ -353,6 +354,9 @@ struct PrepParams {
   int* qtiles;
   int4* kv_units;
   int max_kv_units;
+  unsigned* kv_mask;       // member query tiles of every (sequence, key tile), as bit words
+  int* kv_mask_base;       // [batch + 1] first word of each sequence
+  int max_mask_words;
   int batch, nhead, num_groups, batch_per_group, splits;
   int total_q, total_kv, max_seqlen_q, max_seqlen_kv, max_units;
   int causal, self_attn, kv_targets;
@@ -374,6 +378,8 @@ struct BwdParams {
   const int4* kv_units;    // dK/dV units {b, n, h, 0}
   const int* qtile_base;   // [batch + 1] first query tile of each sequence
   const int* qtiles;       // [query tiles][kQTileInts]
+  const unsigned* kv_mask;       // member query tiles per (sequence, key tile) as bit words
+  const int* kv_mask_base;       // [batch + 1] first word of each sequence
   int* ws_header;
   const float* group_scale;
   long long dq_stride, dk_stride, dv_stride;

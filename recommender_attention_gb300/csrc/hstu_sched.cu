@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
       p.ws_header[kWsUnits] = 0;
       p.ws_header[kWsKvUnits] = 0;
       p.ws_header[kWsCounter] = 0;
+      p.ws_header[kWsKvCounter] = 0;
       reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
     }
     return;
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
       p.ws_header[kWsUnits] = 0;
       p.ws_header[kWsKvUnits] = 0;
       p.ws_header[kWsCounter] = 0;
+      p.ws_header[kWsKvCounter] = 0;
       reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
     }
     return;
@@ -228,6 +230,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
         p.ws_header[kWsUnits] = 0;
         p.ws_header[kWsKvUnits] = 0;
         p.ws_header[kWsCounter] = 0;
+        p.ws_header[kWsKvCounter] = 0;
         reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
       }
       return;
@@ -238,6 +241,44 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
       const int per_h = (kbase[pos + 1] - kbase[pos]) / p.nhead;
       const int local = u - kbase[pos];
       p.kv_units[u] = make_int4(b, local % per_h, local / per_h, 0);
+    }
+    // member masks: bit (m % 32) of word kv_mask_base[b] + n * words_b + m / 32
+    // is set when query tile m of sequence b runs key tile n (words_b =
+    // ceil(query tiles / 32)); the dK/dV kernel walks these words instead of
+    // testing every query tile's record
+    int* mb = p.kv_mask_base;
+    for (int b = tid; b < B; b += nth) {
+      const int k0 = p.self_attn ? p.off_q[b] : p.off_kv[b];
+      const int k1 = p.self_attn ? p.off_q[b + 1] : p.off_kv[b + 1];
+      mb[b] = ((k1 - k0 + kBlockN - 1) / kBlockN) * ((tbase[b + 1] - tbase[b] + 31) / 32);
+    }
+    __syncthreads();
+    const int total_words = block_exclusive_scan(mb, B, s_wsum);
+    if (total_words > p.max_mask_words) {
+      if (tid == 0) {
+        p.ws_header[kWsError] = kErrMaxSeqlen;
+        p.ws_header[kWsUnits] = 0;
+        p.ws_header[kWsKvUnits] = 0;
+        p.ws_header[kWsCounter] = 0;
+        p.ws_header[kWsKvCounter] = 0;
+        reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = 0;
+      }
+      return;
+    }
+    for (int i = tid; i < total_words; i += nth) p.kv_mask[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n_items; i += nth) {
+      const int b = find_segment(tbase, B, i);
+      const int m = i - tbase[b];
+      const int words = (tbase[b + 1] - tbase[b] + 31) / 32;
+      const int nk = words > 0 ? (mb[b + 1] - mb[b]) / words : 0;
+      const int* r = p.qtiles + static_cast<long long>(i) * kQTileInts;
+      unsigned* base = p.kv_mask + mb[b] + m / 32;
+      const unsigned bit = 1u << (m & 31);
+      for (int k = 0; k < 3; ++k) {
+        const int lo = r[2 * k], hi = r[2 * k + 1] < nk ? r[2 * k + 1] : nk;
+        for (int n = lo; n < hi; ++n) atomicOr(base + static_cast<long long>(n) * words, bit);
+      }
     }
   }
 
@@ -256,6 +297,7 @@ __global__ void __launch_bounds__(kPrepThreads) hstu_prep_kernel(const __grid_co
     p.ws_header[kWsUnits] = total;
     p.ws_header[kWsKvUnits] = total_kv_units;
     p.ws_header[kWsCounter] = 0;
+    p.ws_header[kWsKvCounter] = 0;
     reinterpret_cast<long long*>(p.ws_header + kWsTilesLo)[0] = static_cast<long long>(s_tiles);
   }
 }

@@ -195,6 +195,19 @@ __device__ __forceinline__ void umma_ts_x8(uint32_t d_tmem, const uint32_t (&a)[
       "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four MMAs with A in TMEM (columns a[k]) and B in shared memory (descriptors b[k]).
+__device__ __forceinline__ void umma_ts_x4(uint32_t d_tmem, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, Q;\n\tsetp.ne.b32 P, %10, 0;\n\tsetp.eq.b32 Q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, P;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, Q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, Q;\n\t"
+      "}\n" ::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every tcgen05 async op issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
