@@ -48,6 +48,20 @@ used (each one a named constant or a commented branch):
     the batch's group; a group whose largest UIH length is 0 uses 1.0.
   * groups are consecutive blocks of batch/num_groups batches.
 
+Relative attention bias ("From transformer parallelism to HSTU", sections
+2.4 and 3.5; the rab term of the HSTU layer's spatial aggregation), when the
+parameters carry one: s[i, j] gains, before the nonlinearity and the mask,
+
+    rab[i, j] = rab_time[h, bucket(|ts_i - ts_j|)] + rab_pos[h, min(|pos_i - j|, P - 1)]
+
+with the section 3.5 bucket edges (seconds) 0, 1, 5, 30, 60, 300, 1800, 3600,
+86400, 604800, 2.6e6 (bucket k holds [edge_k, edge_k+1), bucket 10 everything
+from 2.6e6 up), one learned scalar per head and bucket.  The pages name a
+positional half without defining it; the reading here is one scalar per head
+and clamped distance, pos_i being query row i's position in key coordinates
+(i for a context row, i + (u_kv - u) otherwise: the mask's bottom-right
+alignment, and a target row's own key at distance 0).
+
 The backward (``hstu_attention_backward``) is the exact gradient of that
 forward (the README's training mode keeps the softmax LSE for it); it is
 pinned against central finite differences of the forward.
@@ -183,9 +197,48 @@ def silu(s: np.ndarray) -> np.ndarray:
         return s / (1.0 + np.exp(-s))
 
 
-def _head_forward(q, k, v, allowed, alpha, attn_scale, softmax):
-    """One (sequence, head): q [n, Dqk], k [L_kv, Dqk], v [L_kv, Dv], allowed [n, L_kv]."""
+# ----------------------------------------------------------------------------
+# Relative attention bias ("From transformer parallelism to HSTU", section 3.5)
+# ----------------------------------------------------------------------------
+# Lower edges of the time-gap buckets, in seconds (the section's table).
+TIME_BUCKET_EDGES = (0.0, 1.0, 5.0, 30.0, 60.0, 300.0, 1800.0, 3600.0, 86400.0, 604800.0, 2.6e6)
+
+
+def time_gap_bucket(gap) -> np.ndarray:
+    """Bucket of a time gap >= 0 (seconds): the largest k with gap >= edge_k."""
+    gap = np.asarray(gap, dtype=np.float64)
+    return np.searchsorted(np.asarray(TIME_BUCKET_EDGES), gap, side="right") - 1
+
+
+def query_key_positions(p: "SeqMaskParams", rows: np.ndarray) -> np.ndarray:
+    """Position of each query row in key coordinates: a context row keeps its
+    index; UIH and target rows shift by u_kv - u (bottom-right alignment)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    return np.where(rows < p.context, rows, rows + (p.uih_kv - p.uih_q))
+
+
+def rab_rows(p: "SeqMaskParams", rows, h: int, ts_q, ts_kv, rab_time, rab_pos) -> np.ndarray:
+    """rab[i, j] for the given query rows of one sequence and head; ts_q / ts_kv
+    are the sequence's timestamps (None: no temporal term)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    bias = np.zeros((rows.shape[0], p.L_kv), dtype=np.float64)
+    if rab_time is not None and ts_q is not None:
+        gap = np.abs(np.asarray(ts_q, dtype=np.float64)[rows][:, None] -
+                     np.asarray(ts_kv, dtype=np.float64)[None, :])
+        bias += np.asarray(rab_time, dtype=np.float64)[h][time_gap_bucket(gap)]
+    if rab_pos is not None:
+        table = np.asarray(rab_pos, dtype=np.float64)[h]
+        d = np.abs(query_key_positions(p, rows)[:, None] - np.arange(p.L_kv)[None, :])
+        bias += table[np.minimum(d, table.shape[0] - 1)]
+    return bias
+
+
+def _head_forward(q, k, v, allowed, alpha, attn_scale, softmax, bias=None):
+    """One (sequence, head): q [n, Dqk], k [L_kv, Dqk], v [L_kv, Dv], allowed [n, L_kv],
+    bias [n, L_kv] (relative attention bias) or None."""
     s = alpha * (q @ k.T)
+    if bias is not None:
+        s = s + bias
     if not softmax:
         p = np.where(allowed, silu(s), 0.0)
         return attn_scale * (p @ v), None
@@ -219,6 +272,28 @@ class HstuParams:
     causal: bool = True
     softmax: bool = False
     kv_targets: bool = False               # cross-attention keys end with the targets' own keys
+    # relative attention bias (None: none): per-token timestamps in seconds
+    # ([total_q]; [total_kv] for cross-attention), rab_time [H, 11], rab_pos [H, P]
+    timestamps_q: Optional[np.ndarray] = None
+    timestamps_kv: Optional[np.ndarray] = None
+    rab_time: Optional[np.ndarray] = None
+    rab_pos: Optional[np.ndarray] = None
+
+    @property
+    def has_rab(self) -> bool:
+        return (self.rab_time is not None and self.timestamps_q is not None) or self.rab_pos is not None
+
+
+def _seq_bias(params: HstuParams, sp, q0: int, kv0: int, h: int, rows) -> Optional[np.ndarray]:
+    """rab rows of one sequence and head, or None when the call has no bias."""
+    if not params.has_rab:
+        return None
+    ts_q = ts_kv = None
+    if params.timestamps_q is not None:
+        ts_q = np.asarray(params.timestamps_q)[q0:q0 + sp.L_q]
+        tkv = params.timestamps_kv if sp.cross else params.timestamps_q
+        ts_kv = np.asarray(tkv)[kv0:kv0 + sp.L_kv]
+    return rab_rows(sp, rows, h, ts_q, ts_kv, params.rab_time, params.rab_pos)
 
 
 def _seq_params(params: HstuParams, b: int, batch: int, off_q, off_kv, targets):
@@ -285,9 +360,10 @@ def hstu_attention_forward(q, k, v, seq_offsets_q, seq_offsets_kv, num_targets,
         q0 = off_q[b]
         kv0 = off_kv[b] if off_kv is not None else q0
         for h in range(H):
+            bias = _seq_bias(params, sp, q0, kv0, h, np.arange(sp.L_q))
             ob, lb = _head_forward(q[q0:q0 + sp.L_q, h], k[kv0:kv0 + sp.L_kv, h],
                                    v[kv0:kv0 + sp.L_kv, h], allowed, alpha, scales[g],
-                                   params.softmax)
+                                   params.softmax, bias)
             o[q0:q0 + sp.L_q, h] = ob
             if lse is not None:
                 lse[h, q0:q0 + sp.L_q] = lb
@@ -313,7 +389,8 @@ def hstu_attention_forward_rows(q, k, v, seq_offsets_q, seq_offsets_kv, num_targ
     qb = np.asarray(q[q0 + rows, h], dtype=np.float64)
     kb = np.asarray(k[kv0:kv0 + sp.L_kv, h], dtype=np.float64)
     vb = np.asarray(v[kv0:kv0 + sp.L_kv, h], dtype=np.float64)
-    return _head_forward(qb, kb, vb, mask_rows(sp, rows), alpha, scales[g], params.softmax)
+    bias = _seq_bias(params, sp, q0, kv0, h, rows)
+    return _head_forward(qb, kb, vb, mask_rows(sp, rows), alpha, scales[g], params.softmax, bias)
 
 
 def allowed_pair_count(seq_offsets_q, seq_offsets_kv, num_targets, params: HstuParams,
@@ -361,7 +438,7 @@ def silu_grad(s: np.ndarray) -> np.ndarray:
     return sig * (1.0 + s * (1.0 - sig))
 
 
-def _head_backward(q, k, v, g, allowed, alpha, attn_scale, softmax):
+def _head_backward(q, k, v, g, allowed, alpha, attn_scale, softmax, bias=None):
     """One (sequence, head): the gradients of _head_forward's o with respect to q,
     k and v for the output gradient g [n, Dv].
 
@@ -369,8 +446,11 @@ def _head_backward(q, k, v, g, allowed, alpha, attn_scale, softmax):
              dv = c a^T g,  da = c g v^T,  ds = M . da . SiLU'(s)
     softmax: o = c * p v,   p = M . exp(s - lse) (row-normalised over allowed keys)
              dv = c p^T g,  dp = c g v^T,  ds = p . (dp - rowsum(p . dp))
-    both:    dq = alpha ds k,  dk = alpha ds^T q."""
+    both:    dq = alpha ds k,  dk = alpha ds^T q.
+    A relative attention bias enters s, and through it every derivative."""
     s = alpha * (q @ k.T)
+    if bias is not None:
+        s = s + bias
     if not softmax:
         a = np.where(allowed, silu(s), 0.0)
         dv = attn_scale * (a.T @ g)
@@ -413,9 +493,10 @@ def hstu_attention_backward(q, k, v, d_o, seq_offsets_q, seq_offsets_kv, num_tar
         q0 = off_q[b]
         kv0 = off_kv[b] if off_kv is not None else q0
         for h in range(H):
+            bias = _seq_bias(params, sp, q0, kv0, h, np.arange(sp.L_q))
             a, bk, c = _head_backward(q[q0:q0 + sp.L_q, h], k[kv0:kv0 + sp.L_kv, h],
                                       v[kv0:kv0 + sp.L_kv, h], d_o[q0:q0 + sp.L_q, h], allowed,
-                                      alpha, scales[g_], params.softmax)
+                                      alpha, scales[g_], params.softmax, bias)
             dq[q0:q0 + sp.L_q, h] += a
             dk[kv0:kv0 + sp.L_kv, h] += bk
             dv[kv0:kv0 + sp.L_kv, h] += c

@@ -283,10 +283,12 @@ def _pins_pass():
     return True
 
 
-def _mfalcon_case(rng, softmax):
+def _mfalcon_case(rng, softmax, rab=False):
     """One random request: the full self-attention over [context | history |
     candidates] and the same candidates as an M-FALCON cross-attention call
-    over the cached [context | history] keys plus the candidates' own keys."""
+    over the cached [context | history] keys plus the candidates' own keys
+    (with rab: a relative attention bias from per-token timestamps and both
+    tables)."""
     c = int(rng.choice([0, 2, 5]))
     hist = int(rng.integers(0, 150))
     t = int(rng.integers(1, 20))
@@ -298,10 +300,18 @@ def _mfalcon_case(rng, softmax):
     kw = dict(context_len=[c], local_len=[int(rng.choice([0, 3, 40]))],
               minfull_len=[int(rng.choice([0, 4, 30]))], attn_scale=[0.25], alpha=0.5,
               causal=bool(rng.integers(0, 2)), softmax=softmax)
-    full = hstu_attention_forward(q, k, v, np.array([0, L]), None, np.array([t]), HstuParams(**kw))
     rows = np.r_[0:c, c + hist:L]
+    extra_full, extra_mf = {}, {}
+    if rab:
+        ts = np.sort(rng.integers(0, 4_000_000, size=L))
+        tables = dict(rab_time=rng.standard_normal((H, 11)),
+                      rab_pos=rng.standard_normal((H, int(rng.integers(1, 60)))))
+        extra_full = dict(timestamps_q=ts, **tables)
+        extra_mf = dict(timestamps_q=ts[rows], timestamps_kv=ts, **tables)
+    full = hstu_attention_forward(q, k, v, np.array([0, L]), None, np.array([t]),
+                                  HstuParams(**kw, **extra_full))
     mf = hstu_attention_forward(q[rows], k, v, np.array([0, c + t]), np.array([0, L]), np.array([t]),
-                                HstuParams(kv_targets=True, **kw))
+                                HstuParams(kv_targets=True, **kw, **extra_mf))
     return full, mf, rows
 
 
@@ -322,6 +332,22 @@ def test_mfalcon_equals_target_rows_of_full_sequence():
                 np.testing.assert_allclose(lse_mf[fin], lse_full[:, rows][fin], rtol=1e-12)
 
 
+def test_mfalcon_with_rab_equals_target_rows_of_full_sequence():
+    """The same equality with a relative attention bias: a candidate's time gaps
+    and distances to the history keys and to its own key are those of its
+    target row in the whole sequence.  Pins the bias's pairing of query and key
+    timestamps and the cross-attention position alignment against the
+    self-attention case."""
+    rng = np.random.default_rng(15)
+    for softmax in (False, True):
+        for _ in range(30):
+            (o_full, lse_full), (o_mf, lse_mf), rows = _mfalcon_case(rng, softmax, rab=True)
+            np.testing.assert_allclose(o_mf, o_full[rows], rtol=1e-11, atol=1e-11)
+            if softmax:
+                fin = np.isfinite(lse_mf)
+                np.testing.assert_allclose(lse_mf[fin], lse_full[:, rows][fin], rtol=1e-11)
+
+
 def test_mfalcon_candidates_see_only_their_own_key():
     for c, u_kv, t in [(0, 5, 3), (2, 9, 4), (3, 0, 2)]:
         p = SeqMaskParams(L_q=c + t, L_kv=c + u_kv + t, context=c, targets=t, causal=True,
@@ -333,6 +359,95 @@ def test_mfalcon_candidates_see_only_their_own_key():
         assert not m[:c, c + u_kv:].any()         # context rows never see candidate keys
         assert m[:, :c].all()                     # context keys: everyone
         assert m[c:, c:c + u_kv].all()            # causal: candidates sit after the whole history
+
+
+# ---------------------------------------------------------------- relative attention bias
+def _read_rab_fixtures():
+    edges, gaps = {}, []
+    for line in open(os.path.join(GOLDEN, "rab_time_buckets.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        kind, a, b = line.split()
+        if kind == "edge":
+            edges[int(a)] = float(b)
+        else:
+            gaps.append((float(a), int(b)))
+    ex = {"tbucket": [], "pbucket": []}
+    for line in open(os.path.join(GOLDEN, "rab_example.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        kind, *vals = line.split()
+        if kind == "ts":
+            ex["ts"] = np.array([int(x) for x in vals])
+        else:
+            ex[kind].append([int(x) for x in vals])
+    return edges, gaps, ex
+
+
+def test_rab_time_buckets_match_the_table():
+    """The bucket edges and a gap at, and just below, every edge ("From
+    transformer parallelism to HSTU", section 3.5)."""
+    edges, gaps, _ = _read_rab_fixtures()
+    assert tuple(edges[k] for k in range(11)) == orc.TIME_BUCKET_EDGES
+    for gap, bucket in gaps:
+        assert int(orc.time_gap_bucket(gap)) == bucket, gap
+
+
+def test_rab_worked_example():
+    """A hand-derived 5-token example: each (i, j) takes the scalar of its own
+    time-gap bucket and of its clamped distance, per head."""
+    _, _, ex = _read_rab_fixtures()
+    H = 2
+    rab_time = np.arange(11)[None, :] * 1.0 + 100.0 * np.arange(H)[:, None]
+    rab_pos = np.array([[10.0, 20.0, 30.0], [40.0, 50.0, 60.0]])
+    p = SeqMaskParams(L_q=5, L_kv=5, context=0, targets=0, causal=False, local=0, minfull=0, cross=False)
+    for h in range(H):
+        t_only = orc.rab_rows(p, np.arange(5), h, ex["ts"], ex["ts"], rab_time, None)
+        np.testing.assert_array_equal(t_only, rab_time[h][np.array(ex["tbucket"])])
+        p_only = orc.rab_rows(p, np.arange(5), h, None, None, None, rab_pos)
+        np.testing.assert_array_equal(p_only, rab_pos[h][np.array(ex["pbucket"])])
+
+
+def test_rab_closed_form_silu_of_two():
+    """q = 0 leaves s = rab: a single token whose own time-gap bucket (0) holds
+    2.0 gets o = attn_scale * SiLU(2) * v = 2 sigma(2) v, with sigma(2) from
+    section 3.4's worked example."""
+    sigma2 = None
+    for line in open(os.path.join(GOLDEN, "silu_mass.txt")):
+        if line.startswith("sigma2"):
+            sigma2 = float(line.split()[1])
+    q = np.zeros((1, 1, 8))
+    v = np.ones((1, 1, 8))
+    rab_time = np.zeros((1, 11))
+    rab_time[0, 0] = 2.0
+    p = HstuParams(attn_scale=[1.0], alpha=1.0, timestamps_q=np.array([12345]), rab_time=rab_time)
+    o, _ = hstu_attention_forward(q, q, v, [0, 1], None, None, p)
+    assert round(o[0, 0, 0] / 2.0, 4) == sigma2
+
+
+def test_rab_constant_per_head_leaves_softmax_unchanged():
+    """Softmax is invariant to a constant added to every score of a row: a bias
+    whose tables are constant per head leaves o unchanged and shifts the LSE
+    by exactly that constant."""
+    rng = np.random.default_rng(8)
+    for _ in range(10):
+        w = W.random_small(int(rng.integers(0, 1000)), softmax=True, hdim=64, max_uih=40)
+        q, k, v = w.tensors()
+        base = oracle_params(w)
+        const_t = rng.standard_normal(w.nhead)
+        const_p = rng.standard_normal(w.nhead)
+        ts_q = rng.integers(0, 10 ** 7, size=w.total_q)
+        ts_kv = rng.integers(0, 10 ** 7, size=w.total_kv) if w.cross else None
+        p = HstuParams(**{**base.__dict__, "timestamps_q": ts_q, "timestamps_kv": ts_kv,
+                          "rab_time": np.repeat(const_t[:, None], 11, axis=1),
+                          "rab_pos": np.repeat(const_p[:, None], 7, axis=1)})
+        args = (as_f64(q), as_f64(k), as_f64(v), w.seq_offsets_q(), w.seq_offsets_kv(), w.num_targets())
+        o0, l0 = hstu_attention_forward(*args, base)
+        o1, l1 = hstu_attention_forward(*args, p)
+        np.testing.assert_allclose(o1, o0, rtol=1e-10, atol=1e-12)
+        fin = np.isfinite(l0)
+        np.testing.assert_array_equal(fin, np.isfinite(l1))
+        np.testing.assert_allclose(l1[fin], (l0 + (const_t + const_p)[:, None])[fin], rtol=1e-12, atol=1e-12)
 
 
 def _fd_case(rng, softmax, cross=False, kv_targets=False):
@@ -391,6 +506,20 @@ def test_backward_matches_finite_differences():
                 _fd_check(*_fd_case(rng, softmax, cross, kvt), rng)
 
 
+def test_backward_with_rab_matches_finite_differences():
+    """The same with a relative attention bias in the scores."""
+    rng = np.random.default_rng(12)
+    for softmax in (False, True):
+        for cross, kvt in ((False, False), (True, True)):
+            for _ in range(3):
+                q, k, v, g, off_q, off_kv, t, p = _fd_case(rng, softmax, cross, kvt)
+                p.timestamps_q = rng.integers(0, 10 ** 6, size=q.shape[0])
+                p.timestamps_kv = rng.integers(0, 10 ** 6, size=k.shape[0]) if cross else None
+                p.rab_time = rng.standard_normal((q.shape[1], 11))
+                p.rab_pos = rng.standard_normal((q.shape[1], 5))
+                _fd_check(q, k, v, g, off_q, off_kv, t, p, rng)
+
+
 def test_backward_silu_grad_closed_form():
     s = np.linspace(-12, 12, 97)
     h = 1e-6
@@ -441,7 +570,7 @@ def test_planted_mistakes_are_caught(monkeypatch):
     # 4. K transposed against Q in the head product (Q K instead of Q K^T)
     real_head = orc._head_forward
     monkeypatch.setattr(orc, "_head_forward",
-                        lambda q, k, v, a, al, sc, sm: real_head(q, k[::-1].copy(), v, a, al, sc, sm))
+                        lambda q, k, v, a, al, sc, sm, *bias: real_head(q, k[::-1].copy(), v, a, al, sc, sm, *bias))
     assert not _pins_pass()
     monkeypatch.undo()
     # 5. M-FALCON candidates that see one another's keys
@@ -461,4 +590,24 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(orc, "silu_grad", lambda s: 1.0 / (1.0 + np.exp(-s)))
     assert not _backward_pin_passes()
     monkeypatch.undo()
-    assert _pins_pass() and _mfalcon_pin_passes() and _backward_pin_passes()
+    # 7. time-gap buckets that put a gap equal to an edge in the bucket below
+    def rab_pins_pass():
+        try:
+            test_rab_time_buckets_match_the_table()
+            test_rab_worked_example()
+            test_mfalcon_with_rab_equals_target_rows_of_full_sequence()
+        except AssertionError:
+            return False
+        return True
+
+    assert rab_pins_pass()
+    monkeypatch.setattr(orc, "time_gap_bucket",
+                        lambda g: np.maximum(np.searchsorted(np.asarray(orc.TIME_BUCKET_EDGES),
+                                                             np.asarray(g, dtype=np.float64), side="left") - 1, 0))
+    assert not rab_pins_pass()
+    monkeypatch.undo()
+    # 8. query positions without the cross-attention alignment
+    monkeypatch.setattr(orc, "query_key_positions", lambda p, rows: np.asarray(rows, dtype=np.int64))
+    assert not rab_pins_pass()
+    monkeypatch.undo()
+    assert _pins_pass() and _mfalcon_pin_passes() and _backward_pin_passes() and rab_pins_pass()
