@@ -5,8 +5,9 @@
 One step = one forward (scheduler + persistent tcgen05 kernel [+ combine]) over
 the large jagged workload: B=64 sequences, nhead 4, bf16, UIH lengths
 U_int[1024, 4096], targets U_int[1, 32], context 6, full causal, hdim 128
-(repeated at hdim 256, 96 and 96/64 in the same run, and the backward of the
-hdim 128 case under "backward"), synthetic N(0,1) inputs, seed 7.
+(repeated at hdim 256, 96 and 96/64 in the same run; with a relative
+attention bias under "rab"; and the backward of the hdim 128 case under
+"backward"), synthetic N(0,1) inputs, seed 7.
 Prints one JSON line (rank 0).  Metric: useful TFLOP/s = 2 (hdim_qk + hdim_v)
 x allowed (i, j) pairs / step time.
 
@@ -292,6 +293,40 @@ def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float)
     return out
 
 
+def rab_lines(rank, device, stream, steps: int, warmup: int, world: int):
+    """The forward of the same large jagged workload (hdim 128) with a relative
+    attention bias (per-token timestamps, an 11-bucket time table and a
+    128-entry positional table per head; Workload.rab_inputs), SiLU and softmax.
+    Useful FLOPs as the headline's (the bias adds no GEMM work)."""
+    from recommender_attention_gb300.hstu import HstuCall
+    out = {}
+    for softmax in (False, True):
+        w = rank_workload(rank, 128).with_(softmax=softmax, rab_pos_buckets=128)
+        q, k, v = w.tensors()
+        ts_q, _, rab_time, rab_pos = w.rab_inputs()
+        dq, dk, dv = q.to(device), k.to(device), v.to(device)
+        off_q = torch.from_numpy(w.seq_offsets_q()).to(device)
+        tg = torch.from_numpy(w.num_targets()).to(device)
+        call = HstuCall(dq, dk, dv, off_q, None, tg, alpha=w.alpha, attn_scale=list(w.attn_scale),
+                        causal=w.causal, local_len=list(w.local_len), context_len=list(w.context_len),
+                        minfull_len=list(w.minfull_len), max_uih_len=list(w.max_uih_len),
+                        num_groups=w.num_groups, softmax=w.softmax,
+                        max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()),
+                        timestamps_q=torch.from_numpy(ts_q).to(device),
+                        rab_time=torch.from_numpy(rab_time).to(device), rab_pos=torch.from_numpy(rab_pos).to(device))
+        st = call.stats(stream)
+        step_ms, fwd_ms = time_device_steps(call, steps, warmup, world, stream)
+        step_ms = reduce_max(step_ms, world, device)
+        flops = 2.0 * (w.hdim_qk + w.hdim_v) * st["allowed_pairs"]
+        tot = reduce_sum(flops, world, device)
+        out["softmax" if softmax else "silu"] = {
+            "value": tot / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": step_ms,
+            "fwd_kernel_ms": fwd_ms, "fwd_kernel_tflops": flops / (fwd_ms * 1e-3) / 1e12}
+        del call, dq, dk, dv
+        torch.cuda.empty_cache()
+    return out
+
+
 def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, peak: float):
     """The backward over the same large jagged workload (hdim 128; SiLU, and
     softmax fed the forward's own o and lse): one step = one hstu_attn_bwd call
@@ -422,6 +457,9 @@ def run_cuda(args):
                           "fwd_kernel_ms": fw2, "fwd_kernel_tflops": f2 / (fw2 * 1e-3) / 1e12}
             del call2, dev2, q2, k2, v2
             torch.cuda.empty_cache()
+
+    if args.hdim == 128 and not args.no_rab:
+        extra["rab"] = rab_lines(rank, device, stream, args.steps, args.warmup, world)
 
     if args.hdim == 128 and not args.no_bwd:
         peaks_b, _ = load_peaks()
@@ -563,6 +601,7 @@ def main(argv=None):
     ap.add_argument("--hdim", type=int, default=128, choices=[64, 128, 256])
     ap.add_argument("--no-d256", action="store_true", help="skip the hdim 256, 96 and 96/64 repeats")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward lines")
+    ap.add_argument("--no-rab", action="store_true", help="skip the relative attention bias lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other scope workloads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

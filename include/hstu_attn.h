@@ -43,9 +43,11 @@
 extern "C" {
 #endif
 
-#define HSTU_ABI_VERSION 3
+#define HSTU_ABI_VERSION 4
 #define HSTU_MAX_GROUPS 256
 #define HSTU_MAX_SPLITS 16
+#define HSTU_RAB_TIME_BUCKETS 11
+#define HSTU_RAB_MAX_POS 256
 
 typedef enum hstu_status {
   HSTU_OK = 0,
@@ -118,6 +120,22 @@ typedef struct hstu_fwd_args {
    * sequence, the targets' own keys; target r of the queries sees target key r
    * of the keys and no other target key.  0 = [context | UIH_kv]. */
   int32_t kv_targets;
+  /* Relative attention bias ("From transformer parallelism to HSTU", sections
+   * 2.4 and 3.5), added to alpha * <q, k> before SiLU / softmax:
+   *   rab[i,j] = rab_time[h, bucket(|ts_i - ts_j|)] + rab_pos[h, min(|pos_i - j|, P - 1)]
+   * Time-gap buckets by lower edge in seconds: 0, 1, 5, 30, 60, 300, 1800,
+   * 3600, 86400, 604800, 2.6e6 (the last open-ended).  pos_i is query row i's
+   * position in key coordinates: i for a context row, i + (uih_kv - uih_q)
+   * for UIH and target rows (the mask's bottom-right alignment).  Gaps are
+   * exact unless the 128 keys of one key tile span 2^29 s (17 years) or
+   * more.  With a bias, hdim_qk ==
+   * hdim_v == 64 or 128; everything NULL / 0 = no bias. */
+  const int64_t* timestamps_q;    /* [dev] [total_q] seconds; required with rab_time */
+  const int64_t* timestamps_kv;   /* [dev] [total_kv]; cross-attention with rab_time (NULL for
+                                     self-attention, which uses timestamps_q) */
+  const float* rab_time;          /* [dev] [H, HSTU_RAB_TIME_BUCKETS] one scalar per head and bucket */
+  const float* rab_pos;           /* [dev] [H, rab_pos_buckets] one scalar per head and clamped distance */
+  int32_t rab_pos_buckets;        /* P: 1..HSTU_RAB_MAX_POS with rab_pos, else ignored */
 } hstu_fwd_args;
 
 /* Counters of one call's schedule (hstu_attn_fwd_stats). */
@@ -226,7 +244,8 @@ hstu_status hstu_attn_bwd_workspace_size(const hstu_bwd_args* args, size_t* byte
  *   SiLU:    a = SiLU(s) masked       dv = c a^T g,  ds = (c g v^T) . SiLU'(s) masked
  *   softmax: p = exp(s - lse) masked  dv = c p^T g,  ds = p . (c g v^T - rowsum(g . o))
  *   both:    dq = alpha ds k,  dk = alpha ds^T q
- * Head dimensions: hdim_qk == hdim_v, 64 or 128 (others HSTU_ERR_UNSUPPORTED).
+ * Head dimensions: hdim_qk == hdim_v, 64 or 128; no relative attention bias
+ * (other calls return HSTU_ERR_UNSUPPORTED).
  * Launches on `stream` the scheduler, in softmax mode a row-sum kernel, then
  * one persistent tcgen05 kernel per query tile (dq) and one per key tile (dk,
  * dv); returns without synchronising.  Every row of every sequence gets its

@@ -65,6 +65,14 @@ hstu_status validate(const hstu_fwd_args* a) {
   if (a->seq_offsets_kv == nullptr && a->total_kv != a->total_q) return HSTU_ERR_INVALID_ARG;
   if (a->kv_targets != 0 && a->kv_targets != 1) return HSTU_ERR_INVALID_ARG;
   if (a->kv_targets && a->seq_offsets_kv == nullptr) return HSTU_ERR_INVALID_ARG;
+  if (a->rab_time != nullptr || a->rab_pos != nullptr) {
+    if (a->hdim_v != a->hdim_qk || (a->hdim_qk != 64 && a->hdim_qk != 128)) return HSTU_ERR_UNSUPPORTED;
+    if (a->rab_time != nullptr &&
+        (a->timestamps_q == nullptr || (a->seq_offsets_kv != nullptr && a->timestamps_kv == nullptr)))
+      return HSTU_ERR_INVALID_ARG;
+    if (a->rab_pos != nullptr && (a->rab_pos_buckets < 1 || a->rab_pos_buckets > HSTU_RAB_MAX_POS))
+      return HSTU_ERR_INVALID_ARG;
+  }
   const int64_t wq = static_cast<int64_t>(a->nhead) * a->hdim_qk;
   const int64_t wv = static_cast<int64_t>(a->nhead) * a->hdim_v;
   const int64_t qs = packed_or(a->q_row_stride, wq), ks = packed_or(a->k_row_stride, wq);
@@ -86,6 +94,10 @@ hstu_status validate_pointers(const hstu_fwd_args* a) {
   const uintptr_t mis = reinterpret_cast<uintptr_t>(a->q) | reinterpret_cast<uintptr_t>(a->k) |
                         reinterpret_cast<uintptr_t>(a->v) | reinterpret_cast<uintptr_t>(a->o);
   if (mis & 15) return HSTU_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->timestamps_q) | reinterpret_cast<uintptr_t>(a->timestamps_kv)) & 7)
+    return HSTU_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->rab_time) | reinterpret_cast<uintptr_t>(a->rab_pos)) & 3)
+    return HSTU_ERR_INVALID_ARG;
   if (a->workspace == nullptr || (reinterpret_cast<uintptr_t>(a->workspace) & 255))
     return HSTU_ERR_WORKSPACE;
   return HSTU_OK;
@@ -223,6 +235,7 @@ hstu_status validate_bwd(const hstu_bwd_args* a) {
   const hstu_status st = validate(&f);
   if (st != HSTU_OK) return st;
   if (f.hdim_v != f.hdim_qk || (f.hdim_qk != 64 && f.hdim_qk != 128)) return HSTU_ERR_UNSUPPORTED;
+  if (f.rab_time != nullptr || f.rab_pos != nullptr) return HSTU_ERR_UNSUPPORTED;   // backward without a bias
   const int64_t w = static_cast<int64_t>(f.nhead) * f.hdim_qk;
   const int64_t strides[4] = {packed_or(a->do_row_stride, w), packed_or(a->dq_row_stride, w),
                               packed_or(a->dk_row_stride, w), packed_or(a->dv_row_stride, w)};
@@ -355,13 +368,24 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   fp.kv_targets = a->kv_targets;
   fp.splits = pl.splits;
   fp.alpha = a->alpha != 0.f ? a->alpha : 1.f / std::sqrt(static_cast<float>(a->hdim_qk));
+  const bool rab = a->rab_time != nullptr || a->rab_pos != nullptr;
+  if (rab) {
+    fp.ts_q = a->rab_time != nullptr ? reinterpret_cast<const long long*>(a->timestamps_q) : nullptr;
+    fp.ts_kv = fp.ts_q == nullptr ? nullptr
+               : reinterpret_cast<const long long*>(a->seq_offsets_kv ? a->timestamps_kv : a->timestamps_q);
+    fp.rab_time = a->rab_time;
+    fp.rab_pos = a->rab_pos;
+    fp.rab_np = a->rab_pos != nullptr ? a->rab_pos_buckets : 1;
+  }
   fill_group_params(a, fp.ctx, fp.loc, fp.mf);
   const int grid = pl.max_units < sms ? (pl.max_units > 0 ? pl.max_units : 1) : sms;
   if (a->event_fwd_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_begin), stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
   cudaError_t e;
-  if (D == 64) e = launch_fwd_d64(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
+  if (rab) e = D == 64 ? launch_fwd_rab_d64(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream)
+                       : launch_fwd_rab_d128(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
+  else if (D == 64) e = launch_fwd_d64(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
   else if (D == 96) e = launch_fwd_d96(tq, tk, tv, tq8, fp, a->hdim_v, bf16, a->softmax != 0, grid, stream);
   else if (D == 128) e = launch_fwd_d128(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
   else e = launch_fwd_d256(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);

@@ -331,6 +331,14 @@ struct FwdParams {
   int batch, nhead, num_groups, batch_per_group;
   int causal, self_attn, kv_targets, splits;
   float alpha;             // resolved QK scale
+  // relative attention bias (the kernels built with it only): per-token
+  // timestamps (seconds; ts_kv == ts_q for self-attention; null = no temporal
+  // term), per-head tables [nhead, 11] and [nhead, rab_np] (null = zero term)
+  const long long* ts_q;
+  const long long* ts_kv;
+  const float* rab_time;
+  const float* rab_pos;
+  int rab_np;
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
 };
 

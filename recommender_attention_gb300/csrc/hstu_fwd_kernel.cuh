@@ -45,6 +45,7 @@
 #include <cuda_fp16.h>
 
 #include "hstu_common.cuh"
+#include "hstu_rab.cuh"
 #include "ptx.cuh"
 
 namespace hstu {
@@ -56,7 +57,7 @@ struct SoftmaxScratch {
   float rs_l[2][2][128];      // [O buffer][warpgroup][row] row sum over the warpgroup's columns
 };
 
-template <int D, int DV, bool SOFTMAX>
+template <int D, int DV, bool SOFTMAX, bool RAB = false>
 struct FwdCfg {
   static constexpr int KCH = (D + 63) / 64;           // 128-byte column chunks per Q / K row
   static constexpr int VCH = (DV + 63) / 64;          // ... per V row
@@ -65,11 +66,13 @@ struct FwdCfg {
   static constexpr int VTILE_BYTES = VCH * CHUNK_BYTES;   // one V tile
   // Q is double-buffered where it fits so the next unit's Q streams in early.
   static constexpr int QBUF = D <= 128 ? 2 : 1;
-  static constexpr int KSTAGES = D == 64 ? 4 : (D <= 128 ? (SOFTMAX ? 2 : 3) : 1);   // K ring depth
+  // K ring depth (one stage less with a relative attention bias, whose tables take its room)
+  static constexpr int KSTAGES = D == 64 ? 4 : (D <= 128 ? ((SOFTMAX || RAB) ? 2 : 3) : 1);
   static constexpr int VSTAGES = D == 64 ? 4 : (D <= 128 ? 2 : 1);                   // V ring depth
   static constexpr int TILES_BYTES = (QBUF + KSTAGES) * TILE_BYTES + VSTAGES * VTILE_BYTES;
-  static constexpr int SMEM_BYTES =
-      TILES_BYTES + (SOFTMAX ? static_cast<int>(sizeof(SoftmaxScratch)) : 0) + 1024;
+  static constexpr int SOFTMAX_BYTES = SOFTMAX ? static_cast<int>(sizeof(SoftmaxScratch)) : 0;
+  static constexpr int RAB_BYTES = RAB ? static_cast<int>(sizeof(RabWarp)) * 8 : 0;   // one per elementwise warp
+  static constexpr int SMEM_BYTES = TILES_BYTES + SOFTMAX_BYTES + RAB_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
   static constexpr int O_BUFS = DV <= 128 ? 2 : 1;
@@ -194,7 +197,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
 // SiLU of the 64 scores of key columns [c0, c0+64) of one row (fp32 bit
 // patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.  Each
 // 16-pair chunk runs stage by stage so the pairs' latencies overlap.
-template <bool BF16, bool MASKED>
+template <bool BF16, bool MASKED, bool PRESCALED = false>
 __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tmem, uint32_t ha,
                                           const RowMask& rm, int c0) {
 #pragma unroll
@@ -204,14 +207,16 @@ __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tm
 #pragma unroll
       for (int k = 0; k < 16; ++k)
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "r"(r[32 * q + 2 * k + 1]), "r"(r[32 * q + 2 * k]));
+      if constexpr (!PRESCALED) {   // else r already holds alpha s / 2 (plus the halved bias)
 #pragma unroll
-      for (int k = 0; k < 16; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
+        for (int k = 0; k < 16; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
+      }
 #pragma unroll
       for (int k = 0; k < 16; ++k) asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
 #pragma unroll
       for (int k = 0; k < 16; ++k) asm("fma.rn.bf16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
     } else {
-      const float haf = __uint_as_float(ha);
+      const float haf = PRESCALED ? 1.0f : __uint_as_float(ha);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const float h0 = __uint_as_float(r[32 * q + 2 * k]) * haf;
@@ -237,12 +242,12 @@ __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tm
   }
 }
 
-template <int D, int DV, bool BF16, bool SOFTMAX>
+template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q8,
                     const __grid_constant__ FwdParams p) {
-  using Cfg = FwdCfg<D, DV, SOFTMAX>;
+  using Cfg = FwdCfg<D, DV, SOFTMAX, RAB>;
   constexpr int KCH = Cfg::KCH;
   constexpr int VCH = Cfg::VCH;
   constexpr int KST = Cfg::KSTAGES;
@@ -257,6 +262,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint8_t* sK = smem + QB * Cfg::TILE_BYTES;
   uint8_t* sV = sK + KST * Cfg::TILE_BYTES;
   SoftmaxScratch* sx = reinterpret_cast<SoftmaxScratch*>(smem + Cfg::TILES_BYTES);   // softmax only
+  RabWarp* rabw = reinterpret_cast<RabWarp*>(smem + Cfg::TILES_BYTES + Cfg::SOFTMAX_BYTES);   // bias only
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -713,6 +719,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int r_diag = row_diag_key(u.s, row);
       int r_ctx = u.s.c;
       if (!valid) { r_lo = r_hi = 0; r_diag = -1; r_ctx = 0; }
+      // relative attention bias: this warp's tables for the unit's head, and the
+      // row's timestamp (relative to the sequence's first key) and position
+      RabRow rrow{0, 0};
+      long long ts_row = 0;   // the row's timestamp; made relative to each key tile's first key
+      if constexpr (RAB) {
+        RabWarp& rw = rabw[warp - 2 - kEpiWarps];
+        __syncwarp();   // the previous unit's lookups are done
+        rab_build(rw, p.ts_q != nullptr ? p.rab_time : nullptr, p.rab_pos, p.rab_np, u.h,
+                  SOFTMAX ? 1.4426950408889634f : 0.5f, lane);
+        __syncwarp();
+        if (p.ts_q != nullptr) ts_row = p.ts_q[u.s.q0 + row];
+        rrow.pos = row < u.s.c ? row : row + (u.s.ukv - u.s.u);
+      }
       const int ob = q_it % OB;
       const uint32_t o_tmem = tmem + lane_base + Cfg::O_COL + ob * DV;   // softmax rescale:
                                                                         // 32-column chunks wg, wg+2, ...
@@ -738,6 +757,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       const FullTiles ft = full_tile_ranges(u.s, u.tb);
+      // bias: raw timestamps of this warpgroup's 64 keys of the next tile, one
+      // per lane and chunk (keys past the sequence repeat its last one), loaded
+      // a tile ahead so their latency hides behind the current tile
+      long long nk0 = 0, nk1 = 0;
+      auto load_keys = [&](int jt0) {
+        if constexpr (RAB) {
+          if (p.ts_q != nullptr) {
+            nk0 = p.ts_kv[u.s.kv0 + min(jt0 + c0 + lane, u.s.Lkv - 1)];
+            nk1 = p.ts_kv[u.s.kv0 + min(jt0 + c0 + 32 + lane, u.s.Lkv - 1)];
+          }
+        }
+      };
+      if (nt > 0) load_keys(n * kBlockN);
       for (int idx = 0; idx < nt; ++idx) {
         const bool full = n < ft.ctx_hi || (n >= ft.lo && n < ft.hi);
         const int j0 = n * kBlockN;
@@ -745,22 +777,44 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           n = n_lo1; n_end = n_hi1;
           n_lo1 = n_lo2; n_hi1 = n_hi2;
         }
+        const long long ck0 = nk0, ck1 = nk1;
+        if (idx + 1 < nt) load_keys(n * kBlockN);
         RowMask rm;
         rm.ctx = r_ctx - j0;
         rm.lo = r_lo - j0;
         rm.span = static_cast<uint32_t>(r_hi - r_lo);
         rm.diag = r_diag >= 0 ? r_diag - j0 : -1000000;
         const int si = s_it + idx;
+        // bias: the keys' timestamps (loaded a tile ahead) and the row's, relative
+        // to the warpgroup's first key of the tile
+        int tsk0 = 0, tsk1 = 0;
+        if constexpr (RAB) {
+          if (p.ts_q != nullptr) {
+            const long long base = __shfl_sync(0xffffffffu, ck0, 0);
+            tsk0 = rab_rel_ts(ck0, base);
+            tsk1 = rab_rel_ts(ck1, base);
+            rrow.ts = rab_rel_ts(ts_row, base);
+          }
+        }
         if (!warp_wait_or_abort(ctl, p, &ctl.s_full[si & 1], (si >> 1) & 1)) { ok = false; break; }
         ptx::tc_fence_after();
         const uint32_t s_tmem = tmem + lane_base + (si & 1) * 128 + c0;
         uint32_t r[64];
         ptx::tmem_ld64(s_tmem, r);
         ptx::tmem_ld_wait(r);
+        if constexpr (RAB) {
+          // r becomes alpha s + rab, scaled for the arithmetic below (SiLU: / 2;
+          // softmax: * log2 e)
+          const RabWarp& rw = rabw[warp - 2 - kEpiWarps];
+          const float mul = SOFTMAX ? scale_log2 : 0.5f * p.alpha;
+          const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
+          rab_apply32(r, mul, rw, p.rab_np, has_time, rrow, rab_chunk(tsk0, j0 + c0, lane));
+          rab_apply32(r + 32, mul, rw, p.rab_np, has_time, rrow, rab_chunk(tsk1, j0 + c0 + 32, lane));
+        }
         if constexpr (!SOFTMAX) {
           // P is packed over this warpgroup's S columns (already in registers)
-          if (full) silu_half<BF16, false>(r, s_tmem, ha2, rm, c0);
-          else silu_half<BF16, true>(r, s_tmem, ha2, rm, c0);
+          if (full) silu_half<BF16, false, RAB>(r, s_tmem, ha2, rm, c0);
+          else silu_half<BF16, true, RAB>(r, s_tmem, ha2, rm, c0);
         } else {
           float mx = -INFINITY;
           if (full) {
@@ -780,7 +834,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           sx->xmax[si & 1][wg][rloc] = mx;
           ptx::mbar_arrive(&ctl.xch[si & 1]);
           if (!warp_wait_or_abort(ctl, p, &ctl.xch[si & 1], (si >> 1) & 1)) { ok = false; break; }
-          mx = fmaxf(mx, sx->xmax[si & 1][wg ^ 1][rloc]) * scale_log2;
+          mx = fmaxf(mx, sx->xmax[si & 1][wg ^ 1][rloc]);
+          if constexpr (!RAB) mx *= scale_log2;   // with a bias the scores are already in log2 units
           // PV of the tile before last must be complete before this tile; keeps the
           // parity tracking of pv_done unambiguous.
           if (si >= 2) {
@@ -818,7 +873,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           // stage by stage so the exponentials of the 64 scores overlap
 #pragma unroll
           for (int k = 0; k < 64; ++k)   // masked scores are -inf and give 0
-            r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), scale_log2, nm));
+            r[k] = __float_as_uint(RAB ? __uint_as_float(r[k]) + nm : fmaf(__uint_as_float(r[k]), scale_log2, nm));
 #pragma unroll
           for (int k = 0; k < 64; ++k) r[k] = __float_as_uint(ex2_approx(__uint_as_float(r[k])));
 #pragma unroll

@@ -17,6 +17,13 @@ cudaError_t launch_fwd_d128(const CUtensorMap& q, const CUtensorMap& k, const CU
 cudaError_t launch_fwd_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                            const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
                            cudaStream_t stream);
+// with a relative attention bias (FwdParams::ts_q / rab_time / rab_pos), hdim_qk == hdim_v
+cudaError_t launch_fwd_rab_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& q8, const FwdParams& p, bool bf16, bool softmax, int grid,
+                               cudaStream_t stream);
+cudaError_t launch_fwd_rab_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& q8, const FwdParams& p, bool bf16, bool softmax, int grid,
+                                cudaStream_t stream);
 cudaError_t launch_fwd_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
                             const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
 // Tensor maps of the backward: 128-row boxes, and 8-row boxes for query tiles

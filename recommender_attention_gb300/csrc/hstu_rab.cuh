@@ -1,0 +1,159 @@
+// Relative attention bias of the HSTU layer ("From transformer parallelism to
+// HSTU", sections 2.4 and 3.5): added to the scaled score of every (query row
+// i, key j) before the nonlinearity,
+//
+//   rab[i, j] = rab_time[h, bucket(|ts_i - ts_j|)] + rab_pos[h, min(|pos_i - j|, P - 1)]
+//
+// with the section's time-gap buckets (lower edges 0, 1, 5, 30, 60, 300, 1800,
+// 3600, 86400, 604800, 2.6e6 seconds; the last bucket open-ended) and pos_i the
+// query row's position in key coordinates (i for a context row, i + (u_kv - u)
+// for UIH and target rows: the mask's bottom-right alignment).
+//
+// Device side, per elementwise warp:
+//   * once per unit, a 33-entry table indexed by clz(gap): a gap's leading bit
+//     fixes its power-of-two octave, and no octave holds more than one bucket
+//     edge, so an entry packs the bucket at the octave's low end (bits 27-30)
+//     and the edge inside it (bits 0-26; all ones when there is none, which
+//     only gaps of 2^27 s and more reach, and those are in the last bucket,
+//     whose weight is repeated one slot further); the head's 11 time weights
+//     and its positional table, all fp32;
+//   * per key tile, the warpgroup's 64 keys' timestamps, loaded one tile ahead,
+//     and the row's, relative to the first of those keys and clamped to
+//     +-2^30 s so every gap fits 32 bits (a row clamped there is at least
+//     2^29 s from every key of a tile spanning less than 2^29 s: the last
+//     bucket either way), the keys' in two registers per lane, read by the
+//     other lanes with shuffles;
+//   * per 32-key chunk and row, the bias is one constant when the chunk's
+//     timestamps are sorted, the row's timestamp lies outside their range and
+//     both ends fall in the same bucket, and when every key of the chunk is at
+//     least P - 1 away; otherwise it is looked up key by key.
+// Weights are stored pre-multiplied by the factor the caller's arithmetic
+// wants (1/2 for the SiLU half-argument, log2 e for the softmax exponent).
+#pragma once
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "hstu_common.cuh"
+
+namespace hstu {
+
+constexpr int kRabTimeBuckets = 11;
+constexpr int kRabMaxPos = 256;               // largest positional table per head
+constexpr int kRabTsClamp = 1 << 30;          // relative timestamps are clamped to +-2^30 s
+constexpr int kRabNoEdge = (1 << 27) - 1;
+
+// Lower edges of the time-gap buckets in seconds ("From transformer parallelism
+// to HSTU", section 3.5).
+__host__ __device__ constexpr int rab_time_edge(int k) {
+  return k == 0 ? 0 : k == 1 ? 1 : k == 2 ? 5 : k == 3 ? 30 : k == 4 ? 60 : k == 5 ? 300
+       : k == 6 ? 1800 : k == 7 ? 3600 : k == 8 ? 86400 : k == 9 ? 604800 : 2600000;
+}
+// Bucket of a gap >= 0: the last bucket whose lower edge it reaches.
+__host__ __device__ inline int rab_time_bucket(long long gap) {
+  int b = 0;
+  for (int k = 1; k < kRabTimeBuckets; ++k) b += gap >= rab_time_edge(k) ? 1 : 0;
+  return b;
+}
+
+// Per elementwise warp.
+struct RabWarp {
+  int tab[33];                       // by clz(gap): bucket at the octave's low end << 27 | edge inside it
+  float wt[kRabTimeBuckets + 1];     // time weights (pre-scaled); the last repeated
+  float pos[kRabMaxPos];             // positional weights (pre-scaled)
+};
+
+__device__ __forceinline__ int rab_rel_ts(long long t, long long base) {
+  long long d = t - base;
+  d = d < -static_cast<long long>(kRabTsClamp - 1) ? -static_cast<long long>(kRabTsClamp - 1) : d;
+  d = d > static_cast<long long>(kRabTsClamp - 1) ? static_cast<long long>(kRabTsClamp - 1) : d;
+  return static_cast<int>(d);
+}
+
+// Builds the warp's tables for head h (all lanes call it); `scale` multiplies
+// every weight.  Null tables give zero terms.
+__device__ __forceinline__ void rab_build(RabWarp& w, const float* rab_time, const float* rab_pos, int np, int h,
+                                          float scale, int lane) {
+  for (int idx = lane; idx <= 32; idx += 32) {
+    // octave of clz == idx: gaps [2^(31 - idx), 2^(32 - idx)); idx 32: gap 0
+    const long long lo = idx == 32 ? 0 : (1LL << (31 - idx));
+    const long long hi = idx == 32 ? 1 : (1LL << (32 - idx));
+    const int b = rab_time_bucket(lo);
+    int edge = kRabNoEdge;
+    if (b + 1 < kRabTimeBuckets && rab_time_edge(b + 1) < hi) edge = rab_time_edge(b + 1);
+    w.tab[idx] = (b << 27) | edge;
+  }
+  if (lane < kRabTimeBuckets + 1) {
+    const int b = lane < kRabTimeBuckets ? lane : kRabTimeBuckets - 1;
+    w.wt[lane] = rab_time != nullptr ? rab_time[h * kRabTimeBuckets + b] * scale : 0.f;
+  }
+  for (int d = lane; d < np; d += 32) w.pos[d] = rab_pos != nullptr ? rab_pos[h * np + d] * scale : 0.f;
+}
+
+// Bucket slot of one gap (0 <= gap < 2^31); slot 11 stands for bucket 10.
+__device__ __forceinline__ int rab_time_slot(const RabWarp& w, int gap) {
+  const int e = w.tab[__clz(gap)];
+  return (e >> 27) + (gap >= (e & kRabNoEdge) ? 1 : 0);
+}
+// Temporal weight of one gap.
+__device__ __forceinline__ float rab_time_weight(const RabWarp& w, int gap) { return w.wt[rab_time_slot(w, gap)]; }
+
+// This lane's row: relative timestamp and key-coordinate position.
+struct RabRow {
+  int ts, pos;
+};
+
+// Keys of one 32-column chunk of a tile: lane l holds key (jb + l)'s relative
+// timestamp in `tsk`; `sorted`, `tmin`, `tmax` describe the chunk.
+struct RabChunk {
+  int tsk;
+  int jb;
+  bool sorted;
+  int tmin, tmax;
+};
+__device__ __forceinline__ RabChunk rab_chunk(int tsk, int jb, int lane) {
+  RabChunk c;
+  c.tsk = tsk;
+  c.jb = jb;
+  const int next = __shfl_down_sync(0xffffffffu, tsk, 1);
+  c.sorted = __all_sync(0xffffffffu, lane == 31 || tsk <= next);
+  c.tmin = __shfl_sync(0xffffffffu, tsk, 0);
+  c.tmax = __shfl_sync(0xffffffffu, tsk, 31);
+  return c;
+}
+
+// r[k] (a raw score, fp32 bits) becomes fma(s, mul, scaled bias) for the 32
+// keys of the chunk.  Warp-collective (shuffles): every lane calls it, and the
+// choice between the constant and the key-by-key form is made for the whole
+// warp, so no lane leaves the shuffles early.
+__device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWarp& w, int np, bool has_time,
+                                            const RabRow& row, const RabChunk& c) {
+  // positional term constant over the chunk?
+  const int dmin = row.pos <= c.jb ? c.jb - row.pos : (row.pos >= c.jb + 31 ? row.pos - (c.jb + 31) : 0);
+  const bool pos_const = dmin >= np - 1;
+  // temporal term constant over the chunk?
+  bool time_const = !has_time;
+  float wt_const = 0.f;
+  if (has_time && c.sorted && (row.ts >= c.tmax || row.ts <= c.tmin)) {
+    const int g0 = abs(row.ts - c.tmin), g1 = abs(row.ts - c.tmax);
+    const int s0 = rab_time_slot(w, g0), s1 = rab_time_slot(w, g1);
+    time_const = s0 == s1 || (s0 >= kRabTimeBuckets - 1 && s1 >= kRabTimeBuckets - 1);
+    wt_const = w.wt[s0];
+  }
+  if (__all_sync(0xffffffffu, pos_const && time_const)) {
+    const float b = w.pos[np - 1] + wt_const;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const int tk = __shfl_sync(0xffffffffu, c.tsk, k);
+    float b = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
+    int d = abs(row.pos - (c.jb + k));
+    d = d < np - 1 ? d : np - 1;
+    b += w.pos[d];
+    r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));
+  }
+}
+
+}  // namespace hstu

@@ -54,6 +54,8 @@ class FwdArgs(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("event_fwd_begin", ctypes.c_void_p), ("event_fwd_end", ctypes.c_void_p),
         ("kv_targets", ctypes.c_int32),
+        ("timestamps_q", ctypes.c_void_p), ("timestamps_kv", ctypes.c_void_p),
+        ("rab_time", ctypes.c_void_p), ("rab_pos", ctypes.c_void_p), ("rab_pos_buckets", ctypes.c_int32),
     ]
 
 
@@ -141,7 +143,9 @@ class HstuCall:
                  max_seqlen_kv: int = 0, num_splits: int = 0,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                  save_lse: bool = True, workspace: Optional[torch.Tensor] = None,
-                 static_workspace: bool = False, kv_targets: bool = False):
+                 static_workspace: bool = False, kv_targets: bool = False,
+                 timestamps_q: Optional[torch.Tensor] = None, timestamps_kv: Optional[torch.Tensor] = None,
+                 rab_time: Optional[torch.Tensor] = None, rab_pos: Optional[torch.Tensor] = None):
         self.lib = load_library()
         if q.dtype not in DTYPE_CODES or k.dtype != q.dtype or v.dtype != q.dtype:
             raise TypeError("q, k, v must share a dtype, fp16 or bf16")
@@ -158,7 +162,12 @@ class HstuCall:
         self._groups = [_per_group(local_len, g, ctypes.c_int32), _per_group(context_len, g, ctypes.c_int32),
                         _per_group(minfull_len, g, ctypes.c_int32), _per_group(max_uih_len, g, ctypes.c_int32),
                         _per_group(attn_scale, g, ctypes.c_float)]
-        self._keep = [q, k, v, seq_offsets_q, seq_offsets_kv, num_targets]
+        self._keep = [q, k, v, seq_offsets_q, seq_offsets_kv, num_targets,
+                      timestamps_q, timestamps_kv, rab_time, rab_pos]
+        for t, dt in ((timestamps_q, torch.int64), (timestamps_kv, torch.int64),
+                      (rab_time, torch.float32), (rab_pos, torch.float32)):
+            if t is not None and (t.dtype != dt or not t.is_contiguous()):
+                raise TypeError("timestamps must be contiguous int64, rab tables contiguous float32")
         a = FwdArgs()
         a.dtype = DTYPE_CODES[q.dtype]
         a.batch, a.nhead, a.hdim_qk, a.hdim_v = batch, nhead, dqk, dv
@@ -167,6 +176,9 @@ class HstuCall:
         a.causal, a.softmax = int(bool(causal)), int(bool(softmax))
         a.num_groups, a.num_splits, a.alpha = g, num_splits, alpha
         a.kv_targets = int(bool(kv_targets))
+        a.timestamps_q, a.timestamps_kv = _ptr(timestamps_q), _ptr(timestamps_kv)
+        a.rab_time, a.rab_pos = _ptr(rab_time), _ptr(rab_pos)
+        a.rab_pos_buckets = 0 if rab_pos is None else rab_pos.shape[-1]
         a.q_row_stride, a.k_row_stride = q.stride(0), k.stride(0)
         a.v_row_stride, a.o_row_stride = v.stride(0), out.stride(0)
         for t in (q, k, v, out):

@@ -56,6 +56,7 @@ class Workload:
     seed: int = 0
     has_targets: bool = True         # False: pass no num_targets array (all zero)
     kv_targets: bool = False         # cross-attention: the key side ends with the targets' keys
+    rab_pos_buckets: int = 0         # > 0: a relative attention bias (timestamps, both tables)
 
     # ----------------------------------------------------------- layout
     @property
@@ -118,6 +119,46 @@ class Workload:
                 x = vrng.uniform(-1.0, 1.0, size=shp).astype(np.float32)
             out.append(torch.from_numpy(x).to(DTYPES[self.dtype]))
         return tuple(out)
+
+    def rab_inputs(self):
+        """Relative attention bias inputs (numpy): (timestamps_q int64 [total_q],
+        timestamps_kv int64 [total_kv] or None for self-attention, rab_time
+        float32 [nhead, 11], rab_pos float32 [nhead, rab_pos_buckets]).
+
+        Per sequence the key timestamps (seconds) start near 1.7e9 and grow by
+        gaps that are 0 one time in ten and otherwise log-uniform on [1 s,
+        ~37 days], so every time-gap bucket occurs.  Query rows take the
+        timestamp of the key at their key-coordinate position (context row i:
+        key i; UIH and target rows: key i + u_kv - u); rows past the last key
+        continue it by the same gap law.  The tables are N(0, 1)."""
+        rng = np.random.default_rng([self.seed, 3])
+        okv = self.seq_offsets_kv() if self.cross else self.seq_offsets_q()
+        oq = self.seq_offsets_q()
+        ts_kv = np.zeros(int(okv[-1]), dtype=np.int64)
+        ts_q = np.zeros(int(oq[-1]), dtype=np.int64)
+
+        def gaps(n):
+            g = np.floor(10.0 ** rng.uniform(0.0, 6.5, size=n)).astype(np.int64)
+            g[rng.uniform(size=n) < 0.1] = 0
+            return g
+
+        for b in range(self.batch):
+            lkv = int(okv[b + 1] - okv[b])
+            lq = int(oq[b + 1] - oq[b])
+            start = 1_700_000_000 + int(rng.integers(0, 10 ** 7))
+            keys = start + np.concatenate([[0], np.cumsum(gaps(max(lkv - 1, 0)))])[:lkv]
+            ts_kv[okv[b]:okv[b] + lkv] = keys
+            c = self.context_len[self.group(b)]
+            u = self.uih_q[b]
+            ukv = self.uih_kv[b] if self.cross else u
+            last = int(keys[-1]) if lkv else start
+            extra = last + np.cumsum(gaps(lq))
+            for i in range(lq):
+                pos = i if i < c else i + (ukv - u)
+                ts_q[oq[b] + i] = keys[min(max(pos, 0), lkv - 1)] if 0 <= pos < lkv else int(extra[i])
+        rab_time = rng.standard_normal((self.nhead, 11)).astype(np.float32)
+        rab_pos = rng.standard_normal((self.nhead, max(self.rab_pos_buckets, 1))).astype(np.float32)
+        return ts_q, (ts_kv if self.cross else None), rab_time, rab_pos
 
     def grad_output(self):
         """An output gradient dO [total_q, nhead, hdim_v] (CPU, storage dtype)

@@ -33,6 +33,19 @@ def call_kwargs(w, **over):
     return kw
 
 
+def rab_kwargs(rab, use_time=True, use_pos=True, device="cuda"):
+    """HstuCall keyword arguments of w.rab_inputs() (numpy) as device tensors."""
+    ts_q, ts_kv, rab_time, rab_pos = rab
+    kw = {}
+    if use_time:
+        kw["timestamps_q"] = torch.from_numpy(ts_q).to(device)
+        kw["timestamps_kv"] = None if ts_kv is None else torch.from_numpy(ts_kv).to(device)
+        kw["rab_time"] = torch.from_numpy(rab_time).to(device)
+    if use_pos:
+        kw["rab_pos"] = torch.from_numpy(rab_pos).to(device)
+    return kw
+
+
 def gpu_forward(w, q, k, v, **over):
     dq, dk, dv, off_q, off_kv, tg = device_inputs(w, q, k, v)
     o, lse = hstu_attn_fwd(dq, dk, dv, off_q, off_kv, tg, check=True, **call_kwargs(w, **over))

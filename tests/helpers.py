@@ -6,22 +6,32 @@ import numpy as np
 from oracle.hstu_oracle import HstuParams
 
 
-def oracle_params(w) -> HstuParams:
-    return HstuParams(num_groups=w.num_groups, context_len=list(w.context_len),
-                      local_len=list(w.local_len), minfull_len=list(w.minfull_len),
-                      max_uih_len=list(w.max_uih_len), attn_scale=list(w.attn_scale),
-                      alpha=w.alpha, causal=w.causal, softmax=w.softmax,
-                      kv_targets=w.kv_targets)
+def oracle_params(w, rab=None, use_time=True, use_pos=True) -> HstuParams:
+    """The oracle's parameters of workload w; rab = w.rab_inputs() adds the
+    relative attention bias (use_time / use_pos keep one term only)."""
+    p = HstuParams(num_groups=w.num_groups, context_len=list(w.context_len),
+                   local_len=list(w.local_len), minfull_len=list(w.minfull_len),
+                   max_uih_len=list(w.max_uih_len), attn_scale=list(w.attn_scale),
+                   alpha=w.alpha, causal=w.causal, softmax=w.softmax,
+                   kv_targets=w.kv_targets)
+    if rab is not None:
+        ts_q, ts_kv, rab_time, rab_pos = rab
+        if use_time:
+            p.timestamps_q, p.timestamps_kv, p.rab_time = ts_q, ts_kv, rab_time
+        if use_pos:
+            p.rab_pos = rab_pos
+    return p
 
 
 def as_f64(t) -> np.ndarray:
     return t.float().numpy().astype(np.float64)
 
 
-def oracle_forward(w, q, k, v):
+def oracle_forward(w, q, k, v, rab=None, use_time=True, use_pos=True):
     from oracle.hstu_oracle import hstu_attention_forward
     return hstu_attention_forward(as_f64(q), as_f64(k), as_f64(v), w.seq_offsets_q(),
-                                  w.seq_offsets_kv(), w.num_targets(), oracle_params(w))
+                                  w.seq_offsets_kv(), w.num_targets(),
+                                  oracle_params(w, rab, use_time, use_pos))
 
 
 def read_mask_fixture(path):

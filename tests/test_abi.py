@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_strings_and_struct_layout(lib):
-    assert lib.hstu_abi_version() == 3
+    assert lib.hstu_abi_version() == 4
     for s in range(6):
         assert lib.hstu_status_string(s)
     assert lib.hstu_status_string(99) == b"unknown status"
@@ -104,6 +104,28 @@ def test_forward_rejects_before_launch(lib):
     a.q = 4096 + 2
     a.workspace = 8192
     assert lib.hstu_attn_fwd(ctypes.byref(a), None) == 1
+
+
+def test_rab_host_validation(lib):
+    t = (ctypes.c_float * 8)()
+    ok = _args(rab_pos=ctypes.cast(t, ctypes.c_void_p), rab_pos_buckets=4)
+    assert _ws(lib, ok)[0] == 0
+    assert _ws(lib, _args(rab_pos=ctypes.cast(t, ctypes.c_void_p), rab_pos_buckets=0))[0] == 1
+    assert _ws(lib, _args(rab_pos=ctypes.cast(t, ctypes.c_void_p), rab_pos_buckets=257))[0] == 1
+    # the time term needs timestamps (and key timestamps for cross-attention)
+    assert _ws(lib, _args(rab_time=ctypes.cast(t, ctypes.c_void_p)))[0] == 1
+    assert _ws(lib, _args(rab_time=ctypes.cast(t, ctypes.c_void_p), timestamps_q=4096))[0] == 0
+    assert _ws(lib, _args(rab_time=ctypes.cast(t, ctypes.c_void_p), timestamps_q=4096,
+                          seq_offsets_kv=4096))[0] == 1
+    # bias kernels: hdim 64 and 128 with hdim_v == hdim_qk
+    for dqk, dv in ((96, 96), (96, 64), (256, 256)):
+        assert _ws(lib, _args(hdim_qk=dqk, hdim_v=dv, rab_pos=ctypes.cast(t, ctypes.c_void_p),
+                              rab_pos_buckets=4))[0] == 2
+    # no backward with a bias yet
+    b = _bwd()
+    b.fwd.rab_pos = ctypes.cast(t, ctypes.c_void_p)
+    b.fwd.rab_pos_buckets = 4
+    assert _bwd_ws(lib, b)[0] == 2
 
 
 def _bwd(**kw):
