@@ -139,20 +139,37 @@ __device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWar
     time_const = s0 == s1 || (s0 >= kRabTimeBuckets - 1 && s1 >= kRabTimeBuckets - 1);
     wt_const = w.wt[s0];
   }
-  if (__all_sync(0xffffffffu, pos_const && time_const)) {
+  const bool all_pos = __all_sync(0xffffffffu, pos_const);
+  const bool all_time = __all_sync(0xffffffffu, time_const);
+  if (all_pos && all_time) {
     const float b = w.pos[np - 1] + wt_const;
 #pragma unroll
     for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));
-    return;
-  }
+  } else if (all_time) {   // the distance varies over the chunk, the time bucket does not
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const int tk = __shfl_sync(0xffffffffu, c.tsk, k);
-    float b = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
-    int d = abs(row.pos - (c.jb + k));
-    d = d < np - 1 ? d : np - 1;
-    b += w.pos[d];
-    r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));
+    for (int k = 0; k < 32; ++k) {
+      int d = abs(row.pos - (c.jb + k));
+      d = d < np - 1 ? d : np - 1;
+      r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, w.pos[d] + wt_const));
+    }
+  } else if (all_pos) {    // the time bucket varies, the distance term does not
+    const float bp = w.pos[np - 1];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int tk = __shfl_sync(0xffffffffu, c.tsk, k);
+      const float wt = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
+      r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, bp + wt));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int tk = __shfl_sync(0xffffffffu, c.tsk, k);
+      float b = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
+      int d = abs(row.pos - (c.jb + k));
+      d = d < np - 1 ? d : np - 1;
+      b += w.pos[d];
+      r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));
+    }
   }
 }
 
