@@ -293,7 +293,7 @@ def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float)
     return out
 
 
-def rab_lines(rank, device, stream, steps: int, warmup: int, world: int):
+def rab_lines(rank, device, stream, steps: int, warmup: int, world: int, peak: float, cpu: bool):
     """The forward of the same large jagged workload (hdim 128) with a relative
     attention bias (per-token timestamps, an 11-bucket time table and a
     128-entry positional table per head; Workload.rab_inputs), SiLU and softmax.
@@ -319,15 +319,20 @@ def rab_lines(rank, device, stream, steps: int, warmup: int, world: int):
         step_ms = reduce_max(step_ms, world, device)
         flops = 2.0 * (w.hdim_qk + w.hdim_v) * st["allowed_pairs"]
         tot = reduce_sum(flops, world, device)
+        kt = flops / (fwd_ms * 1e-3) / 1e12
         out["softmax" if softmax else "silu"] = {
             "value": tot / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": step_ms,
-            "fwd_kernel_ms": fwd_ms, "fwd_kernel_tflops": flops / (fwd_ms * 1e-3) / 1e12}
+            "fwd_kernel_ms": fwd_ms, "fwd_kernel_tflops": kt,
+            "roofline": {"bound": "tensor", "achieved": kt, "peak": peak, "unit": "TFLOP/s", "frac": kt / peak,
+                         "traffic": None, "kernel": "hstu_fwd_kernel<128,bf16,bias>"},
+            "cpu_baseline": (cpu_baseline_rab(w, q, k, v, (ts_q, None, rab_time, rab_pos))
+                             if cpu and rank == 0 else None)}
         del call, dq, dk, dv
         torch.cuda.empty_cache()
     return out
 
 
-def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, peak: float):
+def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, peak: float, cpu: bool):
     """The backward over the same large jagged workload (hdim 128; SiLU, and
     softmax fed the forward's own o and lse): one step = one hstu_attn_bwd call
     (scheduler [+ row sums] + dQ kernel + dK/dV kernel), inputs and dO resident
@@ -367,10 +372,15 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
         executed = 2.0 * 128 * 128 * (5 * w.hdim_qk + 4 * w.hdim_v) * st["executed_tiles"]
         tot = reduce_sum(useful, world, device)
         tf = tot / (ms * 1e-3) / 1e12
+        per_gpu = useful / (ms * 1e-3) / 1e12
         out["softmax" if softmax else "silu"] = {
             "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "pct_of_bf16_peak": 100.0 * tf / world / peak,
             "executed_tflops": reduce_sum(executed, world, device) / (ms * 1e-3) / 1e12,
-            "launches_per_step": 3 + (1 if softmax else 0)}
+            "launches_per_step": 3 + (1 if softmax else 0),
+            "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s",
+                         "frac": per_gpu / peak, "traffic": None,
+                         "kernel": "dQ + dK/dV kernels (whole backward step, useful FLOPs)"},
+            "cpu_baseline": cpu_baseline_backward(w, q, k, v, w.grad_output(), 4.0) if cpu and rank == 0 else None}
         del bw, call, dq, dk, dv, d_o, q, k, v
         torch.cuda.empty_cache()
     return out
@@ -459,12 +469,16 @@ def run_cuda(args):
             torch.cuda.empty_cache()
 
     if args.hdim == 128 and not args.no_rab:
-        extra["rab"] = rab_lines(rank, device, stream, args.steps, args.warmup, world)
+        peaks_r, _ = load_peaks()
+        extra["rab"] = rab_lines(rank, device, stream, args.steps, args.warmup, world,
+                                 float(peaks_r.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                                 not args.no_cpu_baseline)
 
     if args.hdim == 128 and not args.no_bwd:
         peaks_b, _ = load_peaks()
         extra["backward"] = backward_lines(rank, device, stream, args.steps, args.warmup, world,
-                                           float(peaks_b.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
+                                           float(peaks_b.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                                           not args.no_cpu_baseline)
 
     if rank == 0 and not args.no_configs:
         peaks0, _ = load_peaks()
@@ -564,6 +578,71 @@ def cpu_baseline(w, q, k, v, budget_s: float = 12.0):
     return {"value": flops / el / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{done} whole (sequence, head) problems of the {w.batch}x{w.nhead}, "
                       f"longest first, fp64 numpy, {el:.1f} s"}
+
+
+def cpu_baseline_backward(w, q, k, v, d_o, budget_s: float = 6.0):
+    """The oracle's backward as it stands on a bounded sample: whole sequences
+    (all heads) of the workload, longest first, each with the attn_scale the
+    full batch resolves to.  Value: useful backward TFLOP/s (the bench line's
+    FLOP count)."""
+    import dataclasses
+    from oracle.hstu_oracle import (HstuParams, SeqMaskParams, dense_mask, hstu_attention_backward,
+                                    resolved_attn_scales)
+    p = HstuParams(num_groups=1, context_len=w.context_len, local_len=w.local_len, minfull_len=w.minfull_len,
+                   max_uih_len=w.max_uih_len, attn_scale=w.attn_scale, alpha=w.alpha, causal=w.causal,
+                   softmax=w.softmax)
+    off = w.seq_offsets_q()
+    tg = w.num_targets()
+    sub = dataclasses.replace(p, attn_scale=[float(resolved_attn_scales(p, w.batch, off, tg)[0])])
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    flops, done = 0.0, 0
+    t0 = time.perf_counter()
+    for b in list(np.argsort(-w.lengths_q())):
+        s0, s1 = int(off[b]), int(off[b + 1])
+        hstu_attention_backward(f64(q[s0:s1]), f64(k[s0:s1]), f64(v[s0:s1]), f64(d_o[s0:s1]),
+                                np.array([0, s1 - s0]), None, np.array([tg[b]]), sub)
+        sp = SeqMaskParams(L_q=s1 - s0, L_kv=s1 - s0, context=int(w.context_len[0]), targets=int(tg[b]),
+                           causal=w.causal, local=int(w.local_len[0]), minfull=int(w.minfull_len[0]), cross=False)
+        flops += 2.0 * (3 * w.hdim_qk + 2 * w.hdim_v) * float(dense_mask(sp).sum()) * w.nhead
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} whole sequences (all {w.nhead} heads) of the {w.batch}, longest first, "
+                      f"fp64 numpy backward, {el:.1f} s"}
+
+
+def cpu_baseline_rab(w, q, k, v, rab, budget_s: float = 6.0):
+    """The oracle's forward with the relative attention bias on a bounded
+    sample: whole (sequence, head) problems, longest first."""
+    from oracle.hstu_oracle import HstuParams, SeqMaskParams, dense_mask, hstu_attention_forward_rows
+    ts_q, _, rab_time, rab_pos = rab
+    p = HstuParams(num_groups=1, context_len=w.context_len, local_len=w.local_len, minfull_len=w.minfull_len,
+                   max_uih_len=w.max_uih_len, attn_scale=w.attn_scale, alpha=w.alpha, causal=w.causal,
+                   softmax=w.softmax, timestamps_q=ts_q, rab_time=rab_time, rab_pos=rab_pos)
+    off = w.seq_offsets_q()
+    tg = w.num_targets()
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    qd, kd, vd = f64(q), f64(k), f64(v)
+    flops, done = 0.0, 0
+    t0 = time.perf_counter()
+    for b in list(np.argsort(-w.lengths_q())):
+        L = int(off[b + 1] - off[b])
+        for h in range(w.nhead):
+            hstu_attention_forward_rows(qd, kd, vd, off, None, tg, p, int(b), h, np.arange(L))
+            sp = SeqMaskParams(L_q=L, L_kv=L, context=int(w.context_len[0]), targets=int(tg[b]),
+                               causal=w.causal, local=int(w.local_len[0]), minfull=int(w.minfull_len[0]),
+                               cross=False)
+            flops += 2.0 * (w.hdim_qk + w.hdim_v) * float(dense_mask(sp).sum())
+            done += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{done} whole (sequence, head) problems with the bias, longest first, fp64 numpy, {el:.1f} s"}
 
 
 def run_reference(args):
