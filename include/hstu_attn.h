@@ -244,8 +244,9 @@ hstu_status hstu_attn_bwd_workspace_size(const hstu_bwd_args* args, size_t* byte
  *   SiLU:    a = SiLU(s) masked       dv = c a^T g,  ds = (c g v^T) . SiLU'(s) masked
  *   softmax: p = exp(s - lse) masked  dv = c p^T g,  ds = p . (c g v^T - rowsum(g . o))
  *   both:    dq = alpha ds k,  dk = alpha ds^T q
- * Head dimensions: hdim_qk == hdim_v, 64 or 128; no relative attention bias
- * (other calls return HSTU_ERR_UNSUPPORTED).
+ * Head dimensions: hdim_qk == hdim_v, 64 or 128 (others HSTU_ERR_UNSUPPORTED).
+ * With a relative attention bias in fwd, s includes it and every gradient
+ * flows through it (the bias tables themselves get no gradient here).
  * Launches on `stream` the scheduler, in softmax mode a row-sum kernel, then
  * one persistent tcgen05 kernel per query tile (dq) and one per key tile (dk,
  * dv); returns without synchronising.  Every row of every sequence gets its

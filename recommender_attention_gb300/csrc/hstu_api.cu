@@ -235,7 +235,6 @@ hstu_status validate_bwd(const hstu_bwd_args* a) {
   const hstu_status st = validate(&f);
   if (st != HSTU_OK) return st;
   if (f.hdim_v != f.hdim_qk || (f.hdim_qk != 64 && f.hdim_qk != 128)) return HSTU_ERR_UNSUPPORTED;
-  if (f.rab_time != nullptr || f.rab_pos != nullptr) return HSTU_ERR_UNSUPPORTED;   // backward without a bias
   const int64_t w = static_cast<int64_t>(f.nhead) * f.hdim_qk;
   const int64_t strides[4] = {packed_or(a->do_row_stride, w), packed_or(a->dq_row_stride, w),
                               packed_or(a->dk_row_stride, w), packed_or(a->dv_row_stride, w)};
@@ -481,6 +480,10 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
                         reinterpret_cast<uintptr_t>(a->d_o) | reinterpret_cast<uintptr_t>(a->dq) |
                         reinterpret_cast<uintptr_t>(a->dk) | reinterpret_cast<uintptr_t>(a->dv);
   if (mis & 15) return HSTU_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(f.timestamps_q) | reinterpret_cast<uintptr_t>(f.timestamps_kv)) & 7)
+    return HSTU_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(f.rab_time) | reinterpret_cast<uintptr_t>(f.rab_pos)) & 3)
+    return HSTU_ERR_INVALID_ARG;
   if (f.workspace == nullptr || (reinterpret_cast<uintptr_t>(f.workspace) & 255)) return HSTU_ERR_WORKSPACE;
   const int sms = sm_count_current();
   if (sms <= 0) return HSTU_ERR_CUDA;
@@ -545,12 +548,24 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   bw.self_attn = f.seq_offsets_kv == nullptr;
   bw.kv_targets = f.kv_targets;
   bw.alpha = f.alpha != 0.f ? f.alpha : 1.f / std::sqrt(static_cast<float>(D));
+  const bool rab = f.rab_time != nullptr || f.rab_pos != nullptr;
+  if (rab) {
+    bw.ts_q = f.rab_time != nullptr ? reinterpret_cast<const long long*>(f.timestamps_q) : nullptr;
+    bw.ts_kv = bw.ts_q == nullptr ? nullptr
+               : reinterpret_cast<const long long*>(f.seq_offsets_kv ? f.timestamps_kv : f.timestamps_q);
+    bw.rab_time = f.rab_time;
+    bw.rab_pos = f.rab_pos;
+    bw.rab_np = f.rab_pos != nullptr ? f.rab_pos_buckets : 1;
+  }
   fill_group_params(&f, bw.ctx, bw.loc, bw.mf);
   const int mu = bp.fwd.max_units, mk = bp.max_kv_units;
   const int grid_q = mu < sms ? (mu > 0 ? mu : 1) : sms;
   const int grid_kv = mk < sms ? (mk > 0 ? mk : 1) : sms;
-  const cudaError_t e = D == 64 ? launch_bwd_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream)
-                                : launch_bwd_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
+  cudaError_t e;
+  if (rab) e = D == 64 ? launch_bwd_rab_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream)
+                       : launch_bwd_rab_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
+  else e = D == 64 ? launch_bwd_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream)
+                   : launch_bwd_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 

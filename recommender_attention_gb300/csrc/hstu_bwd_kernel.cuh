@@ -36,6 +36,7 @@
 #pragma once
 #include "hstu_fwd_kernel.cuh"
 #include "hstu_launch.h"
+#include "hstu_rab.cuh"
 
 namespace hstu {
 
@@ -43,7 +44,7 @@ constexpr int kBwdThreads = 320;   // producer, MMA, two elementwise warpgroups
 constexpr int kHalf = 64;          // columns of a half tile
 constexpr int kHalfBytes = kHalf * 128;   // rows of a half tile inside a 128-row swizzled chunk
 
-template <int D, int DV>
+template <int D, int DV, bool RAB = false>
 struct BwdCfg {
   static constexpr int KCH = (D + 63) / 64;
   static constexpr int VCH = (DV + 63) / 64;
@@ -51,7 +52,8 @@ struct BwdCfg {
   static constexpr int TQ = KCH * CHUNK;        // a Q or K tile
   static constexpr int TV = VCH * CHUNK;        // a V or dO tile
   static constexpr int STAGES = 2;
-  static constexpr int SMEM_BYTES = (TQ + TV) * (1 + STAGES) + 1024;
+  static constexpr int RAB_OFFSET = (TQ + TV) * (1 + STAGES);   // relative attention bias tables, per warp
+  static constexpr int SMEM_BYTES = RAB_OFFSET + (RAB ? 8 * static_cast<int>(sizeof(RabWarp)) : 0) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t ACC = 256;          // first accumulator column
   static_assert(D % 32 == 0 && DV % 32 == 0 && ACC + D + DV <= TMEM_COLS, "backward head dimensions");
@@ -222,8 +224,9 @@ __device__ __forceinline__ void mma_half_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 // (the forward's SiLU arithmetic): with h = alpha s / 2, t = tanh(h),
 // sig = (1 + t) / 2, SiLU(x) = h (1 + t) and SiLU'(x) = sig + SiLU(x) (1 - sig).
 // pa receives SiLU(x) (when WANT_A), pr receives dp * SiLU'(x); pairs whose bit
-// in `allow` is clear give 0 (MASKED).
-template <bool WANT_A, bool MASKED>
+// in `allow` is clear give 0 (MASKED).  PRESCALED: sv already holds h (with a
+// relative attention bias, alpha s / 2 + rab / 2).
+template <bool WANT_A, bool MASKED, bool PRESCALED = false>
 __device__ __forceinline__ void silu_bwd_bf16(const uint32_t (&sv)[32], const uint32_t (&dv)[32], uint32_t ha2,
                                               uint32_t allow, uint32_t (&pa)[16], uint32_t (&pr)[16]) {
   constexpr uint32_t kHalf2 = 0x3F003F00u, kNegHalf2 = 0xBF00BF00u;   // bf16 pairs (0.5, 0.5), (-0.5, -0.5)
@@ -231,7 +234,7 @@ __device__ __forceinline__ void silu_bwd_bf16(const uint32_t (&sv)[32], const ui
   for (int k = 0; k < 16; ++k) {
     uint32_t h, t, sg, a, om, d, g, r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "r"(sv[2 * k + 1]), "r"(sv[2 * k]));
-    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h) : "r"(ha2));
+    if constexpr (!PRESCALED) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h) : "r"(ha2));   // else sv holds h
     asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t) : "r"(h));
     asm("fma.rn.bf16x2 %0, %1, %2, %2;" : "=r"(sg) : "r"(t), "r"(kHalf2));
     asm("fma.rn.bf16x2 %0, %1, %2, %1;" : "=r"(a) : "r"(h), "r"(t));
@@ -307,13 +310,13 @@ __device__ __forceinline__ void bwd_init(BwdCtl& ctl, int tid, int warp) {
 namespace hstu {
 
 // ---------------------------------------------------------------------------------- dQ
-template <int D, int DV, bool BF16, bool SOFTMAX>
+template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     hstu_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_q8, const __grid_constant__ CUtensorMap tm_do8,
                        const __grid_constant__ BwdParams p) {
-  using Cfg = BwdCfg<D, DV>;
+  using Cfg = BwdCfg<D, DV, RAB>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -476,9 +479,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dlt = p.delta[static_cast<long long>(u.h) * p.total_q + grow] / u.scale;
         }
       }
+      // relative attention bias: this warp's tables, the row's timestamp and
+      // position, and each key tile's timestamps (one per lane and half) loaded
+      // a key tile ahead
+      RabWarp* rw = reinterpret_cast<RabWarp*>(smem + Cfg::RAB_OFFSET) + (warp - 2);
+      long long ts_row = 0, nk0 = 0, nk1 = 0;
+      int pos_row = 0;
+      auto load_keys = [&](int nn) {
+        if constexpr (RAB) {
+          if (p.ts_q != nullptr) {
+            nk0 = p.ts_kv[u.s.kv0 + min(nn * kBlockN + 32 * wg + lane, u.s.Lkv - 1)];
+            nk1 = p.ts_kv[u.s.kv0 + min(nn * kBlockN + kHalf + 32 * wg + lane, u.s.Lkv - 1)];
+          }
+        }
+      };
+      if constexpr (RAB) {
+        __syncwarp();   // the previous unit's lookups are done
+        rab_build(*rw, p.ts_q != nullptr ? p.rab_time : nullptr, p.rab_pos, p.rab_np, u.h,
+                  SOFTMAX ? kLog2e : 0.5f, lane);
+        __syncwarp();
+        if (p.ts_q != nullptr) ts_row = p.ts_q[u.s.q0 + row];
+        pos_row = row < u.s.c ? row : row + (u.s.ukv - u.s.u);
+        load_keys(tileset_at(ts, 0));
+      }
       const FullTiles ft = full_tile_ranges(u.s, q_tile_bounds(u.s, u.L, u.t));
       for (int idx = 0; idx < nt && ok; ++idx) {
         const int n = tileset_at(ts, idx);
+        const long long ck0 = nk0, ck1 = nk1;
+        if (RAB && idx + 1 < nt) load_keys(tileset_at(ts, idx + 1));
         const bool full = n < ft.ctx_hi || (n >= ft.lo && n < ft.hi);
         const int j0 = n * kBlockN;
         RowMask rm;
@@ -498,9 +526,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::tmem_ld32(sb + 64, dv);
           ptx::tmem_ld_wait(sv);
           ptx::tmem_ld_wait(dv);
+          if constexpr (RAB) {   // sv becomes alpha s + rab, scaled (SiLU: / 2, softmax: * log2 e)
+            const long long ck = hh ? ck1 : ck0;
+            const long long base = __shfl_sync(0xffffffffu, ck, 0);
+            const RabRow rr{p.ts_q != nullptr ? rab_rel_ts(ts_row, base) : 0, pos_row};
+            rab_apply32<true>(sv, SOFTMAX ? alpha * kLog2e : half_alpha, *rw, p.rab_np,
+                              p.ts_q != nullptr && p.rab_time != nullptr, rr,
+                              rab_cols(p.ts_q != nullptr ? rab_rel_ts(ck, base) : 0,
+                                       j0 + kHalf * hh + 32 * wg + lane, true));
+          }
           if constexpr (BF16 && !SOFTMAX) {
-            if (full) silu_bwd_bf16<false, false>(sv, dv, ha2, mb, pk, pk);
-            else silu_bwd_bf16<false, true>(sv, dv, ha2, mb, pk, pk);
+            if (full) silu_bwd_bf16<false, false, RAB>(sv, dv, ha2, mb, pk, pk);
+            else silu_bwd_bf16<false, true, RAB>(sv, dv, ha2, mb, pk, pk);
           } else {
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
@@ -511,10 +548,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const float g = __uint_as_float(dv[k + e]);
                 float r;
                 if constexpr (SOFTMAX) {
-                  r = ex2_approx(fmaf(s, alpha * kLog2e, -lse2)) * (g - dlt);
+                  r = ex2_approx((RAB ? s : s * (alpha * kLog2e)) - lse2) * (g - dlt);
                 } else {
-                  const float sig = fmaf(0.5f, tanh_approx(s * half_alpha), 0.5f);
-                  const float xs = s * alpha * sig;
+                  const float h = RAB ? s : s * half_alpha;   // x / 2
+                  const float sig = fmaf(0.5f, tanh_approx(h), 0.5f);
+                  const float xs = 2.0f * h * sig;
                   r = g * (sig + fmaf(-xs, sig, xs));
                 }
                 ds[e] = ((mb >> (k + e)) & 1u) ? r : 0.f;
@@ -561,13 +599,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 namespace hstu {
 
 // ---------------------------------------------------------------------------------- dK, dV
-template <int D, int DV, bool BF16, bool SOFTMAX>
+template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     hstu_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_q8, const __grid_constant__ CUtensorMap tm_do8,
                          const __grid_constant__ BwdParams p) {
-  using Cfg = BwdCfg<D, DV>;
+  using Cfg = BwdCfg<D, DV, RAB>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -729,6 +767,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         continue;
       }
       const bool ctx_key = j < u.s.c;   // context keys are seen by every query row
+      // relative attention bias: this warp's tables; the key row's timestamp,
+      // relative to the unit's first key, and position
+      RabWarp* rw = reinterpret_cast<RabWarp*>(smem + Cfg::RAB_OFFSET) + ew;
+      long long ts_base = 0;
+      RabRow krow_rab{0, j};
+      if constexpr (RAB) {
+        __syncwarp();   // the previous unit's lookups are done
+        rab_build(*rw, p.ts_q != nullptr ? p.rab_time : nullptr, p.rab_pos, p.rab_np, u.h,
+                  SOFTMAX ? kLog2e : 0.5f, lane);
+        __syncwarp();
+        if (p.ts_q != nullptr) {
+          ts_base = p.ts_kv[u.s.kv0 + u.t * kBlockN];
+          krow_rab.ts = rab_rel_ts(p.ts_kv[u.s.kv0 + min(j, u.s.Lkv - 1)], ts_base);
+        }
+      }
       for (int w = 0; w < mw.n && ok; ++w) {
         unsigned bits = mw.w[w];
         while (bits != 0u && ok) {
@@ -751,6 +804,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 dg = row_diag_key(u.s, qi);
               }
               ctl.col_rng[ew][lane] = make_int4(lo, hi, dg, 0);
+            }
+            int c_ts = 0;   // bias: this lane's column's timestamp
+            if constexpr (RAB) {
+              if (p.ts_q != nullptr && qi >= 0) c_ts = rab_rel_ts(p.ts_q[u.s.q0 + qi], ts_base);
             }
             if constexpr (SOFTMAX) {
               float l2 = 0.f, dl = 0.f;
@@ -780,9 +837,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             ptx::tmem_ld32(sb + 64, dv);
             ptx::tmem_ld_wait(sv);
             ptx::tmem_ld_wait(dv);
+            if constexpr (RAB) {   // sv becomes alpha s + rab, scaled (SiLU: / 2, softmax: * log2 e)
+              const int c_pos = qi < 0 ? 0 : (qi < u.s.c ? qi : qi + (u.s.ukv - u.s.u));
+              rab_apply32<false>(sv, SOFTMAX ? alpha * kLog2e : half_alpha, *rw, p.rab_np,
+                                 p.ts_q != nullptr && p.rab_time != nullptr, krow_rab,
+                                 rab_cols(c_ts, c_pos, qi >= 0));
+            }
             if constexpr (BF16 && !SOFTMAX) {
-              if (masked) silu_bwd_bf16<true, true>(sv, dv, ha2, allow, pp, pd);
-              else silu_bwd_bf16<true, false>(sv, dv, ha2, allow, pp, pd);
+              if (masked) silu_bwd_bf16<true, true, RAB>(sv, dv, ha2, allow, pp, pd);
+              else silu_bwd_bf16<true, false, RAB>(sv, dv, ha2, allow, pp, pd);
             } else {
 #pragma unroll
               for (int k = 0; k < 32; k += 2) {
@@ -797,11 +860,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   if constexpr (SOFTMAX) {
                     const float l2 = e ? st4.z : st4.x;
                     const float dl = e ? st4.w : st4.y;
-                    a = ex2_approx(fmaf(s, alpha * kLog2e, -l2));
+                    a = ex2_approx((RAB ? s : s * (alpha * kLog2e)) - l2);
                     r = a * (g - dl);
                   } else {
-                    const float sig = fmaf(0.5f, tanh_approx(s * half_alpha), 0.5f);
-                    a = s * alpha * sig;                   // SiLU(x)
+                    const float h = RAB ? s : s * half_alpha;   // x / 2
+                    const float sig = fmaf(0.5f, tanh_approx(h), 0.5f);
+                    a = 2.0f * h * sig;                    // SiLU(x)
                     r = g * (sig + fmaf(-a, sig, a));      // SiLU'(x) = sig + x sig (1 - sig)
                   }
                   const bool al = (allow >> (k + e)) & 1u;
@@ -855,11 +919,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // Host side: both backward kernels of one head dimension, the dQ kernel first.
-template <int D, bool BF16, bool SOFTMAX>
+template <int D, bool BF16, bool SOFTMAX, bool RAB>
 cudaError_t launch_bwd_pair(const BwdMaps& m, const BwdParams& p, int grid_q, int grid_kv, cudaStream_t stream) {
-  constexpr int smem = BwdCfg<D, D>::SMEM_BYTES;
-  auto kq = hstu_bwd_dq_kernel<D, D, BF16, SOFTMAX>;
-  auto kkv = hstu_bwd_dkdv_kernel<D, D, BF16, SOFTMAX>;
+  constexpr int smem = BwdCfg<D, D, RAB>::SMEM_BYTES;
+  auto kq = hstu_bwd_dq_kernel<D, D, BF16, SOFTMAX, RAB>;
+  auto kkv = hstu_bwd_dkdv_kernel<D, D, BF16, SOFTMAX, RAB>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -877,13 +941,13 @@ cudaError_t launch_bwd_pair(const BwdMaps& m, const BwdParams& p, int grid_q, in
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool RAB>
 cudaError_t launch_bwd_dispatch(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q,
                                 int grid_kv, cudaStream_t stream) {
-  if (bf16) return softmax ? launch_bwd_pair<D, true, true>(m, p, grid_q, grid_kv, stream)
-                           : launch_bwd_pair<D, true, false>(m, p, grid_q, grid_kv, stream);
-  return softmax ? launch_bwd_pair<D, false, true>(m, p, grid_q, grid_kv, stream)
-                 : launch_bwd_pair<D, false, false>(m, p, grid_q, grid_kv, stream);
+  if (bf16) return softmax ? launch_bwd_pair<D, true, true, RAB>(m, p, grid_q, grid_kv, stream)
+                           : launch_bwd_pair<D, true, false, RAB>(m, p, grid_q, grid_kv, stream);
+  return softmax ? launch_bwd_pair<D, false, true, RAB>(m, p, grid_q, grid_kv, stream)
+                 : launch_bwd_pair<D, false, false, RAB>(m, p, grid_q, grid_kv, stream);
 }
 
 }  // namespace hstu

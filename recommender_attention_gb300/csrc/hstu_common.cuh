@@ -393,6 +393,12 @@ struct BwdParams {
   long long dq_stride, dk_stride, dv_stride;
   int total_q, batch, nhead, batch_per_group, causal, self_attn, kv_targets;
   float alpha;
+  // relative attention bias (the kernels built with it only), as in FwdParams
+  const long long* ts_q;
+  const long long* ts_kv;
+  const float* rab_time;
+  const float* rab_pos;
+  int rab_np;
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
 };
 

@@ -808,8 +808,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const RabWarp& rw = rabw[warp - 2 - kEpiWarps];
           const float mul = SOFTMAX ? scale_log2 : 0.5f * p.alpha;
           const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
-          rab_apply32(r, mul, rw, p.rab_np, has_time, rrow, rab_chunk(tsk0, j0 + c0, lane));
-          rab_apply32(r + 32, mul, rw, p.rab_np, has_time, rrow, rab_chunk(tsk1, j0 + c0 + 32, lane));
+          // keys past the sequence repeat its last one: every column counts in the ranges
+          rab_apply32<true>(r, mul, rw, p.rab_np, has_time, rrow, rab_cols(tsk0, j0 + c0 + lane, true));
+          rab_apply32<true>(r + 32, mul, rw, p.rab_np, has_time, rrow, rab_cols(tsk1, j0 + c0 + 32 + lane, true));
         }
         if constexpr (!SOFTMAX) {
           // P is packed over this warpgroup's S columns (already in registers)

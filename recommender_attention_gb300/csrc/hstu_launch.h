@@ -36,6 +36,11 @@ cudaError_t launch_bwd_d64(const BwdMaps& m, const BwdParams& p, bool bf16, bool
                            cudaStream_t stream);
 cudaError_t launch_bwd_d128(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q, int grid_kv,
                             cudaStream_t stream);
+// with a relative attention bias (BwdParams::ts_q / rab_time / rab_pos)
+cudaError_t launch_bwd_rab_d64(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q,
+                               int grid_kv, cudaStream_t stream);
+cudaError_t launch_bwd_rab_d128(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q,
+                                int grid_kv, cudaStream_t stream);
 // delta[h, i] = sum_e dO[i, h, e] O[i, h, e] in fp32 over every row in [0, total_q).
 cudaError_t launch_bwd_delta(const void* o, long long o_stride, const void* d_o, long long do_stride, float* delta,
                              int total_q, int nhead, int hdim_v, bool bf16, cudaStream_t stream);

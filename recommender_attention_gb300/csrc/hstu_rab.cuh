@@ -23,10 +23,10 @@
 //     2^29 s from every key of a tile spanning less than 2^29 s: the last
 //     bucket either way), the keys' in two registers per lane, read by the
 //     other lanes with shuffles;
-//   * per 32-key chunk and row, the bias is one constant when the chunk's
-//     timestamps are sorted, the row's timestamp lies outside their range and
-//     both ends fall in the same bucket, and when every key of the chunk is at
-//     least P - 1 away; otherwise it is looked up key by key.
+//   * per 32-column chunk and row, each term is one constant when the row's
+//     timestamp lies outside the columns' range and both ends fall in the same
+//     bucket (the extreme gaps are at the range's ends), and when every column
+//     is at least P - 1 away; otherwise it is looked up column by column.
 // Weights are stored pre-multiplied by the factor the caller's arithmetic
 // wants (1/2 for the SiLU half-argument, log2 e for the softmax exponent).
 #pragma once
@@ -102,38 +102,41 @@ struct RabRow {
   int ts, pos;
 };
 
-// Keys of one 32-column chunk of a tile: lane l holds key (jb + l)'s relative
-// timestamp in `tsk`; `sorted`, `tmin`, `tmax` describe the chunk.
-struct RabChunk {
-  int tsk;
-  int jb;
-  bool sorted;
-  int tmin, tmax;
+// The 32 columns of a chunk, lane l describing column l: its relative
+// timestamp and key-coordinate position, and over the valid columns the
+// extremes of both (invalid columns are ignored there and their scores
+// masked later).
+struct RabCols {
+  int ts, pos;
+  int tmin, tmax, pmin, pmax;
 };
-__device__ __forceinline__ RabChunk rab_chunk(int tsk, int jb, int lane) {
-  RabChunk c;
-  c.tsk = tsk;
-  c.jb = jb;
-  const int next = __shfl_down_sync(0xffffffffu, tsk, 1);
-  c.sorted = __all_sync(0xffffffffu, lane == 31 || tsk <= next);
-  c.tmin = __shfl_sync(0xffffffffu, tsk, 0);
-  c.tmax = __shfl_sync(0xffffffffu, tsk, 31);
+__device__ __forceinline__ RabCols rab_cols(int ts, int pos, bool valid) {
+  RabCols c;
+  c.ts = ts;
+  c.pos = pos;
+  c.tmin = __reduce_min_sync(0xffffffffu, valid ? ts : 0x7fffffff);
+  c.tmax = __reduce_max_sync(0xffffffffu, valid ? ts : -0x7fffffff);
+  c.pmin = __reduce_min_sync(0xffffffffu, valid ? pos : 0x7fffffff);
+  c.pmax = __reduce_max_sync(0xffffffffu, valid ? pos : -0x7fffffff);
   return c;
 }
 
 // r[k] (a raw score, fp32 bits) becomes fma(s, mul, scaled bias) for the 32
-// keys of the chunk.  Warp-collective (shuffles): every lane calls it, and the
-// choice between the constant and the key-by-key form is made for the whole
-// warp, so no lane leaves the shuffles early.
+// columns of the chunk: bias(row, column k) = time weight of |row.ts - ts_k|
+// plus distance weight of min(|row.pos - pos_k|, np - 1).  CONTIG: column k's
+// position is c.pmin + k (keys of a tile), else it comes from lane k.  Each
+// term is one constant per row when the row's timestamp (position) lies
+// outside the columns' range and both ends fall in the same bucket (are at
+// least np - 1 away); the constant or key-by-key form is chosen per term for
+// the whole warp, so every lane runs the same shuffles.  Warp-collective.
+template <bool CONTIG>
 __device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWarp& w, int np, bool has_time,
-                                            const RabRow& row, const RabChunk& c) {
-  // positional term constant over the chunk?
-  const int dmin = row.pos <= c.jb ? c.jb - row.pos : (row.pos >= c.jb + 31 ? row.pos - (c.jb + 31) : 0);
+                                            const RabRow& row, const RabCols& c) {
+  const int dmin = row.pos <= c.pmin ? c.pmin - row.pos : (row.pos >= c.pmax ? row.pos - c.pmax : 0);
   const bool pos_const = dmin >= np - 1;
-  // temporal term constant over the chunk?
   bool time_const = !has_time;
   float wt_const = 0.f;
-  if (has_time && c.sorted && (row.ts >= c.tmax || row.ts <= c.tmin)) {
+  if (has_time && (row.ts >= c.tmax || row.ts <= c.tmin)) {
     const int g0 = abs(row.ts - c.tmin), g1 = abs(row.ts - c.tmax);
     const int s0 = rab_time_slot(w, g0), s1 = rab_time_slot(w, g1);
     time_const = s0 == s1 || (s0 >= kRabTimeBuckets - 1 && s1 >= kRabTimeBuckets - 1);
@@ -148,7 +151,8 @@ __device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWar
   } else if (all_time) {   // the distance varies over the chunk, the time bucket does not
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      int d = abs(row.pos - (c.jb + k));
+      const int pk = CONTIG ? c.pmin + k : __shfl_sync(0xffffffffu, c.pos, k);
+      int d = abs(row.pos - pk);
       d = d < np - 1 ? d : np - 1;
       r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, w.pos[d] + wt_const));
     }
@@ -156,16 +160,17 @@ __device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWar
     const float bp = w.pos[np - 1];
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      const int tk = __shfl_sync(0xffffffffu, c.tsk, k);
+      const int tk = __shfl_sync(0xffffffffu, c.ts, k);
       const float wt = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
       r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, bp + wt));
     }
   } else {
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-      const int tk = __shfl_sync(0xffffffffu, c.tsk, k);
+      const int tk = __shfl_sync(0xffffffffu, c.ts, k);
+      const int pk = CONTIG ? c.pmin + k : __shfl_sync(0xffffffffu, c.pos, k);
       float b = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
-      int d = abs(row.pos - (c.jb + k));
+      int d = abs(row.pos - pk);
       d = d < np - 1 ? d : np - 1;
       b += w.pos[d];
       r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));

@@ -121,11 +121,13 @@ def test_rab_host_validation(lib):
     for dqk, dv in ((96, 96), (96, 64), (256, 256)):
         assert _ws(lib, _args(hdim_qk=dqk, hdim_v=dv, rab_pos=ctypes.cast(t, ctypes.c_void_p),
                               rab_pos_buckets=4))[0] == 2
-    # no backward with a bias yet
+    # the backward takes the same bias fields and checks
     b = _bwd()
     b.fwd.rab_pos = ctypes.cast(t, ctypes.c_void_p)
     b.fwd.rab_pos_buckets = 4
-    assert _bwd_ws(lib, b)[0] == 2
+    assert _bwd_ws(lib, b)[0] == 0
+    b.fwd.rab_pos_buckets = 300
+    assert _bwd_ws(lib, b)[0] == 1
 
 
 def _bwd(**kw):

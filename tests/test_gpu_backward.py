@@ -16,7 +16,7 @@ import torch
 from oracle.hstu_oracle import hstu_attention_backward, resolved_attn_scales
 from recommender_attention_gb300 import hstu
 from recommender_attention_gb300 import workloads as W
-from tests.gpu_helpers import assert_parity, call_kwargs, device_inputs
+from tests.gpu_helpers import assert_parity, call_kwargs, device_inputs, rab_kwargs
 from tests.helpers import as_f64, oracle_params
 
 pytestmark = pytest.mark.gpu
@@ -44,12 +44,16 @@ def gpu_backward(w, q, k, v, d_o, **over):
     return tuple(_host(x) for x in g)
 
 
-def check_backward(w, **over):
+def check_backward(w, rab=False, **over):
+    """rab: with the workload's relative attention bias (Workload.rab_inputs)."""
     q, k, v = w.tensors()
     d_o = w.grad_output()
+    bias = w.rab_inputs() if rab else None
+    if rab:
+        over = {**over, **rab_kwargs(bias)}
     got = gpu_backward(w, q, k, v, d_o, **over)
     ref = hstu_attention_backward(as_f64(q), as_f64(k), as_f64(v), as_f64(d_o), w.seq_offsets_q(),
-                                  w.seq_offsets_kv(), w.num_targets(), oracle_params(w))
+                                  w.seq_offsets_kv(), w.num_targets(), oracle_params(w, bias))
     for name, a, b in zip(("dq", "dk", "dv"), got, ref):
         assert_parity(a, b, w.dtype, what=f"{w.name} {name}")
 
@@ -80,6 +84,26 @@ def test_fuzz_backward(seed, softmax):
     dtype = "bf16" if seed % 3 else "fp16"
     w = W.random_small(seed, dtype=dtype, hdim=hdim, softmax=softmax, kv_targets=seed % 5 == 4)
     check_backward(w)
+
+
+# ---------------------------------------------------------------- with a relative attention bias
+@pytest.mark.parametrize("cfg", ["tiny", "jagged"])
+@pytest.mark.parametrize("softmax", [False, True])
+def test_small_configs_backward_rab(cfg, softmax):
+    check_backward(W.CONFIGS[cfg]().with_(softmax=softmax, rab_pos_buckets=64), rab=True)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_backward_rab(seed):
+    w = W.random_small(100 + seed, hdim=[64, 128][seed % 2], softmax=seed % 4 >= 2,
+                       dtype="bf16" if seed % 3 else "fp16", kv_targets=seed % 4 == 3)
+    check_backward(w.with_(rab_pos_buckets=[1, 9, 64, 256][seed % 4]), rab=True)
+
+
+@pytest.mark.parametrize("softmax", [False, True])
+def test_mfalcon_backward_rab(softmax):
+    check_backward(W.mfalcon(batch=2, candidates=150, softmax=softmax, history=(300, 700)).with_(rab_pos_buckets=100),
+                   rab=True)
 
 
 # ---------------------------------------------------------------- edges
@@ -146,15 +170,17 @@ def test_backward_repeated_calls_are_identical():
 
 
 # ---------------------------------------------------------------- full size, sampled sequences
-@pytest.mark.parametrize("softmax", [False, True])
-def test_large_jagged_backward_sampled(softmax):
-    """The large jagged workload at full size through one backward call; the
-    oracle recomputes a few whole sequences (a sequence's gradients depend on
-    that sequence alone), with the attn_scale the full batch resolves to."""
-    w = W.large_jagged(hdim=128).with_(softmax=softmax)
+@pytest.mark.parametrize("softmax,rab", [(False, False), (True, False), (False, True)])
+def test_large_jagged_backward_sampled(softmax, rab):
+    """The large jagged workload at full size through one backward call (with
+    rab: plus the relative attention bias); the oracle recomputes a few whole
+    sequences (a sequence's gradients depend on that sequence alone), with the
+    attn_scale the full batch resolves to."""
+    w = W.large_jagged(hdim=128).with_(softmax=softmax, rab_pos_buckets=128 if rab else 0)
     q, k, v = w.tensors()
     d_o = w.grad_output()
-    got = gpu_backward(w, q, k, v, d_o)
+    bias = w.rab_inputs() if rab else None
+    got = gpu_backward(w, q, k, v, d_o, **(rab_kwargs(bias) if rab else {}))
     off = w.seq_offsets_q()
     p = oracle_params(w)
     scale = float(resolved_attn_scales(p, w.batch, off, w.num_targets())[0])
@@ -163,6 +189,8 @@ def test_large_jagged_backward_sampled(softmax):
     for b in [int(np.argmin(lens)), int(rng.integers(0, w.batch))]:
         s0, s1 = int(off[b]), int(off[b + 1])
         sub = dataclasses.replace(p, attn_scale=[scale])
+        if rab:
+            sub = dataclasses.replace(sub, timestamps_q=bias[0][s0:s1], rab_time=bias[2], rab_pos=bias[3])
         ref = hstu_attention_backward(as_f64(q[s0:s1]), as_f64(k[s0:s1]), as_f64(v[s0:s1]),
                                       as_f64(d_o[s0:s1]), np.array([0, s1 - s0]), None,
                                       np.array([w.targets[b]]), sub)
