@@ -341,10 +341,14 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
     recompute S and dP, so the executed count is 2 (5 hdim_qk + 4 hdim_v)."""
     from recommender_attention_gb300.hstu import HstuBwdCall
     out = {}
-    for softmax in (False, True):
-        w = rank_workload(rank, 128).with_(softmax=softmax)
+    for softmax, rab in ((False, False), (True, False), (False, True)):
+        w = rank_workload(rank, 128).with_(softmax=softmax, rab_pos_buckets=128 if rab else 0)
         q, k, v = w.tensors()
         call, (dq, dk, dv, off_q, tg) = device_call(w, q, k, v, device)
+        bias = w.rab_inputs() if rab else None
+        bias_kw = {} if not rab else dict(timestamps_q=torch.from_numpy(bias[0]).to(device),
+                                          rab_time=torch.from_numpy(bias[2]).to(device),
+                                          rab_pos=torch.from_numpy(bias[3]).to(device))
         st = call.stats(stream)
         call.launch(stream)
         call.check(stream)
@@ -353,7 +357,8 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
                          attn_scale=list(w.attn_scale), causal=w.causal, local_len=list(w.local_len),
                          context_len=list(w.context_len), minfull_len=list(w.minfull_len),
                          max_uih_len=list(w.max_uih_len), num_groups=w.num_groups, softmax=w.softmax,
-                         max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()))
+                         max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()),
+                         **bias_kw)
         for _ in range(warmup):
             bw.launch(stream)
         bw.check(stream)
@@ -373,14 +378,15 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
         tot = reduce_sum(useful, world, device)
         tf = tot / (ms * 1e-3) / 1e12
         per_gpu = useful / (ms * 1e-3) / 1e12
-        out["softmax" if softmax else "silu"] = {
+        out[("softmax" if softmax else "silu") + ("_rab" if rab else "")] = {
             "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "pct_of_bf16_peak": 100.0 * tf / world / peak,
             "executed_tflops": reduce_sum(executed, world, device) / (ms * 1e-3) / 1e12,
             "launches_per_step": 3 + (1 if softmax else 0),
             "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s",
                          "frac": per_gpu / peak, "traffic": None,
                          "kernel": "dQ + dK/dV kernels (whole backward step, useful FLOPs)"},
-            "cpu_baseline": cpu_baseline_backward(w, q, k, v, w.grad_output(), 4.0) if cpu and rank == 0 else None}
+            "cpu_baseline": (cpu_baseline_backward(w, q, k, v, w.grad_output(), 4.0, bias)
+                             if cpu and rank == 0 else None)}
         del bw, call, dq, dk, dv, d_o, q, k, v
         torch.cuda.empty_cache()
     return out
@@ -580,11 +586,12 @@ def cpu_baseline(w, q, k, v, budget_s: float = 12.0):
                       f"longest first, fp64 numpy, {el:.1f} s"}
 
 
-def cpu_baseline_backward(w, q, k, v, d_o, budget_s: float = 6.0):
+def cpu_baseline_backward(w, q, k, v, d_o, budget_s: float = 6.0, bias=None):
     """The oracle's backward as it stands on a bounded sample: whole sequences
-    (all heads) of the workload, longest first, each with the attn_scale the
-    full batch resolves to.  Value: useful backward TFLOP/s (the bench line's
-    FLOP count)."""
+    (all heads) of the workload, each with the attn_scale the full batch
+    resolves to; longest first, or shortest first with a relative attention
+    bias (whose dense per-pair arrays make the oracle much slower).  Value:
+    useful backward TFLOP/s (the bench line's FLOP count)."""
     import dataclasses
     from oracle.hstu_oracle import (HstuParams, SeqMaskParams, dense_mask, hstu_attention_backward,
                                     resolved_attn_scales)
@@ -597,10 +604,13 @@ def cpu_baseline_backward(w, q, k, v, d_o, budget_s: float = 6.0):
     f64 = lambda t: t.float().numpy().astype(np.float64)
     flops, done = 0.0, 0
     t0 = time.perf_counter()
-    for b in list(np.argsort(-w.lengths_q())):
+    order = np.argsort(w.lengths_q()) if bias is not None else np.argsort(-w.lengths_q())
+    for b in list(order):
         s0, s1 = int(off[b]), int(off[b + 1])
+        pb = sub if bias is None else dataclasses.replace(sub, timestamps_q=bias[0][s0:s1], rab_time=bias[2],
+                                                          rab_pos=bias[3])
         hstu_attention_backward(f64(q[s0:s1]), f64(k[s0:s1]), f64(v[s0:s1]), f64(d_o[s0:s1]),
-                                np.array([0, s1 - s0]), None, np.array([tg[b]]), sub)
+                                np.array([0, s1 - s0]), None, np.array([tg[b]]), pb)
         sp = SeqMaskParams(L_q=s1 - s0, L_kv=s1 - s0, context=int(w.context_len[0]), targets=int(tg[b]),
                            causal=w.causal, local=int(w.local_len[0]), minfull=int(w.minfull_len[0]), cross=False)
         flops += 2.0 * (3 * w.hdim_qk + 2 * w.hdim_v) * float(dense_mask(sp).sum()) * w.nhead
@@ -609,7 +619,8 @@ def cpu_baseline_backward(w, q, k, v, d_o, budget_s: float = 6.0):
             break
     el = time.perf_counter() - t0
     return {"value": flops / el / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-            "sample": f"{done} whole sequences (all {w.nhead} heads) of the {w.batch}, longest first, "
+            "sample": f"{done} whole sequences (all {w.nhead} heads) of the {w.batch}, "
+                      f"{'shortest first, with the bias' if bias is not None else 'longest first'}, "
                       f"fp64 numpy backward, {el:.1f} s"}
 
 
