@@ -244,7 +244,8 @@ hstu_status hstu_attn_bwd_workspace_size(const hstu_bwd_args* args, size_t* byte
  *   SiLU:    a = SiLU(s) masked       dv = c a^T g,  ds = (c g v^T) . SiLU'(s) masked
  *   softmax: p = exp(s - lse) masked  dv = c p^T g,  ds = p . (c g v^T - rowsum(g . o))
  *   both:    dq = alpha ds k,  dk = alpha ds^T q
- * Head dimensions: hdim_qk == hdim_v, 64 or 128 (others HSTU_ERR_UNSUPPORTED).
+ * Head dimensions: hdim_qk == hdim_v in {64, 96, 128}, or 96 with hdim_v 64
+ * (others HSTU_ERR_UNSUPPORTED); with a bias, 64 or 128 as in the forward.
  * With a relative attention bias in fwd, s includes it and every gradient
  * flows through it (the bias tables themselves get no gradient here).
  * Launches on `stream` the scheduler, in softmax mode a row-sum kernel, then

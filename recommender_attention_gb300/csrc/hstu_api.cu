@@ -234,12 +234,18 @@ hstu_status validate_bwd(const hstu_bwd_args* a) {
   const hstu_fwd_args f = bwd_fwd_view(a);
   const hstu_status st = validate(&f);
   if (st != HSTU_OK) return st;
-  if (f.hdim_v != f.hdim_qk || (f.hdim_qk != 64 && f.hdim_qk != 128)) return HSTU_ERR_UNSUPPORTED;
+  // hdim 64 and 128 (hdim_v equal), 96 with hdim_v 96 or 64; a bias only with 64 / 128 (validate)
+  const bool pair_ok = (f.hdim_v == f.hdim_qk && (f.hdim_qk == 64 || f.hdim_qk == 96 || f.hdim_qk == 128)) ||
+                       (f.hdim_qk == 96 && f.hdim_v == 64);
+  if (!pair_ok) return HSTU_ERR_UNSUPPORTED;
   const int64_t w = static_cast<int64_t>(f.nhead) * f.hdim_qk;
-  const int64_t strides[4] = {packed_or(a->do_row_stride, w), packed_or(a->dq_row_stride, w),
-                              packed_or(a->dk_row_stride, w), packed_or(a->dv_row_stride, w)};
-  for (int64_t x : strides)
-    if (x < w || (x * 2) % 16) return HSTU_ERR_INVALID_ARG;
+  const int64_t wv = static_cast<int64_t>(f.nhead) * f.hdim_v;
+  const int64_t sq[2] = {packed_or(a->dq_row_stride, w), packed_or(a->dk_row_stride, w)};
+  const int64_t sv[2] = {packed_or(a->do_row_stride, wv), packed_or(a->dv_row_stride, wv)};
+  for (int i = 0; i < 2; ++i) {
+    if (sq[i] < w || (sq[i] * 2) % 16) return HSTU_ERR_INVALID_ARG;
+    if (sv[i] < wv || (sv[i] * 2) % 16) return HSTU_ERR_INVALID_ARG;
+  }
   return HSTU_OK;
 }
 
@@ -493,14 +499,15 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   const bool bf16 = f.dtype == HSTU_DTYPE_BF16;
   const int D = f.hdim_qk;
   const int64_t w = static_cast<int64_t>(f.nhead) * D;
-  const int64_t do_stride = packed_or(a->do_row_stride, w);
+  const int64_t wv = static_cast<int64_t>(f.nhead) * f.hdim_v;
+  const int64_t do_stride = packed_or(a->do_row_stride, wv);
   BwdMaps maps;
   if (!encode_map(&maps.q, f.q, bf16, w, f.total_q, packed_or(f.q_row_stride, w)) ||
       !encode_map(&maps.q8, f.q, bf16, w, f.total_q, packed_or(f.q_row_stride, w), 8) ||
       !encode_map(&maps.k, f.k, bf16, w, f.total_kv, packed_or(f.k_row_stride, w)) ||
-      !encode_map(&maps.v, f.v, bf16, w, f.total_kv, packed_or(f.v_row_stride, w)) ||
-      !encode_map(&maps.d_o, a->d_o, bf16, w, f.total_q, do_stride) ||
-      !encode_map(&maps.d_o8, a->d_o, bf16, w, f.total_q, do_stride, 8))
+      !encode_map(&maps.v, f.v, bf16, wv, f.total_kv, packed_or(f.v_row_stride, wv)) ||
+      !encode_map(&maps.d_o, a->d_o, bf16, wv, f.total_q, do_stride) ||
+      !encode_map(&maps.d_o8, a->d_o, bf16, wv, f.total_q, do_stride, 8))
     return HSTU_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(f.workspace);
@@ -515,7 +522,7 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   if (launch_prep(pp, stream) != cudaSuccess) return HSTU_ERR_CUDA;
 
   float* delta = f.softmax ? reinterpret_cast<float*>(ws + bp.off_delta) : nullptr;
-  if (f.softmax && launch_bwd_delta(f.o, packed_or(f.o_row_stride, w), a->d_o, do_stride, delta, f.total_q,
+  if (f.softmax && launch_bwd_delta(f.o, packed_or(f.o_row_stride, wv), a->d_o, do_stride, delta, f.total_q,
                                     f.nhead, f.hdim_v, bf16, stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
 
@@ -539,7 +546,7 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   bw.group_scale = pp.group_scale;
   bw.dq_stride = packed_or(a->dq_row_stride, w);
   bw.dk_stride = packed_or(a->dk_row_stride, w);
-  bw.dv_stride = packed_or(a->dv_row_stride, w);
+  bw.dv_stride = packed_or(a->dv_row_stride, wv);
   bw.total_q = f.total_q;
   bw.batch = f.batch;
   bw.nhead = f.nhead;
@@ -564,8 +571,9 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   cudaError_t e;
   if (rab) e = D == 64 ? launch_bwd_rab_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream)
                        : launch_bwd_rab_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
-  else e = D == 64 ? launch_bwd_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream)
-                   : launch_bwd_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
+  else if (D == 64) e = launch_bwd_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
+  else if (D == 96) e = launch_bwd_d96(maps, bw, f.hdim_v, bf16, f.softmax != 0, grid_q, grid_kv, stream);
+  else e = launch_bwd_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 

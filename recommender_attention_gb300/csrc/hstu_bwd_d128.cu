@@ -8,7 +8,7 @@ static_assert(BwdCfg<128, 128>::SMEM_BYTES + sizeof(BwdCtl) <= 232448, "shared m
 
 cudaError_t launch_bwd_d128(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q, int grid_kv,
                            cudaStream_t stream) {
-  return launch_bwd_dispatch<128, false>(m, p, bf16, softmax, grid_q, grid_kv, stream);
+  return launch_bwd_dispatch<128, 128, false>(m, p, bf16, softmax, grid_q, grid_kv, stream);
 }
 
 }  // namespace hstu

@@ -195,14 +195,16 @@ __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t a_base, uin
     for (int j = 0; j < 8; ++j) { ad[j] = ad0 + off(g + j); bd[j] = bd0 + off(g + j); }
     ptx::umma_ss_x8(d_tmem, ad, bd, idesc, g > 0 ? 1u : 0u);
   }
-  if constexpr (KS % 8 != 0) {
-    static_assert(KS % 8 == 4, "k-steps");
+  if constexpr (KS % 8 >= 4) {
     constexpr int g = KS / 8 * 8;
     uint64_t ad[4], bd[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) { ad[j] = ad0 + off(g + j); bd[j] = bd0 + off(g + j); }
     ptx::umma_ss_x4(d_tmem, ad, bd, idesc, g > 0 ? 1u : 0u);
   }
+#pragma unroll
+  for (int ks = KS / 4 * 4; ks < KS; ++ks)   // hdim 96: the last two k-steps
+    ptx::umma_ss(d_tmem, ad0 + off(ks), bd0 + off(ks), idesc, ks > 0 ? 1u : 0u);
 }
 // C[tmem] (+)= A B over one half tile: A (128 x 64, 16-bit) packed in TMEM by
 // the elementwise warps (warpgroup w's 32 columns at a_tmem + 32 w, 16 columns
@@ -572,18 +574,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_after();
       const float mul = alpha * u.scale;
 #pragma unroll 1
-      for (int c = 0; c < D / 2; c += 32) {
-        uint32_t o[32];
-        ptx::tmem_ld32(tmem + lane_base + Cfg::ACC + wg * (D / 2) + c, o);
+      for (int c = 0; c < D / 2; c += 16) {   // 16 columns at a time (hdim 96: 48 per warpgroup)
+        uint32_t o[16];
+        ptx::tmem_ld16(tmem + lane_base + Cfg::ACC + wg * (D / 2) + c, o);
         ptx::tmem_ld_wait(o);
         if (valid) {
-          uint32_t q2[16];
+          uint32_t q2[8];
 #pragma unroll
-          for (int k = 0; k < 32; k += 2)
+          for (int k = 0; k < 16; k += 2)
             q2[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
-#pragma unroll
-          for (int k = 0; k < 16; k += 4)
-            *reinterpret_cast<uint4*>(dq_row + c + 2 * k) = make_uint4(q2[k], q2[k + 1], q2[k + 2], q2[k + 3]);
+          *reinterpret_cast<uint4*>(dq_row + c) = make_uint4(q2[0], q2[1], q2[2], q2[3]);
+          *reinterpret_cast<uint4*>(dq_row + c + 8) = make_uint4(q2[4], q2[5], q2[6], q2[7]);
         }
       }
       ptx::tc_fence_before();
@@ -895,18 +896,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t col0 = Cfg::ACC + (part == 0 ? 0 : DV) + wg * (W / 2);
         uint16_t* dst = part == 0 ? dv_row : dk_row;
 #pragma unroll 1
-        for (int c = 0; c < W / 2; c += 32) {
-          uint32_t o[32];
-          ptx::tmem_ld32(tmem + lane_base + col0 + c, o);
+        for (int c = 0; c < W / 2; c += 16) {   // 16 columns at a time (hdim 96: 48 per warpgroup)
+          uint32_t o[16];
+          ptx::tmem_ld16(tmem + lane_base + col0 + c, o);
           ptx::tmem_ld_wait(o);
           if (kvalid) {
-            uint32_t pk[16];
+            uint32_t pk[8];
 #pragma unroll
-            for (int k = 0; k < 32; k += 2)
+            for (int k = 0; k < 16; k += 2)
               pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
-#pragma unroll
-            for (int k = 0; k < 16; k += 4)
-              *reinterpret_cast<uint4*>(dst + c + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
+            *reinterpret_cast<uint4*>(dst + c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(dst + c + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
       }
@@ -919,11 +919,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // Host side: both backward kernels of one head dimension, the dQ kernel first.
-template <int D, bool BF16, bool SOFTMAX, bool RAB>
+template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB>
 cudaError_t launch_bwd_pair(const BwdMaps& m, const BwdParams& p, int grid_q, int grid_kv, cudaStream_t stream) {
-  constexpr int smem = BwdCfg<D, D, RAB>::SMEM_BYTES;
-  auto kq = hstu_bwd_dq_kernel<D, D, BF16, SOFTMAX, RAB>;
-  auto kkv = hstu_bwd_dkdv_kernel<D, D, BF16, SOFTMAX, RAB>;
+  constexpr int smem = BwdCfg<D, DV, RAB>::SMEM_BYTES;
+  auto kq = hstu_bwd_dq_kernel<D, DV, BF16, SOFTMAX, RAB>;
+  auto kkv = hstu_bwd_dkdv_kernel<D, DV, BF16, SOFTMAX, RAB>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -941,13 +941,13 @@ cudaError_t launch_bwd_pair(const BwdMaps& m, const BwdParams& p, int grid_q, in
   return cudaGetLastError();
 }
 
-template <int D, bool RAB>
+template <int D, int DV, bool RAB>
 cudaError_t launch_bwd_dispatch(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q,
                                 int grid_kv, cudaStream_t stream) {
-  if (bf16) return softmax ? launch_bwd_pair<D, true, true, RAB>(m, p, grid_q, grid_kv, stream)
-                           : launch_bwd_pair<D, true, false, RAB>(m, p, grid_q, grid_kv, stream);
-  return softmax ? launch_bwd_pair<D, false, true, RAB>(m, p, grid_q, grid_kv, stream)
-                 : launch_bwd_pair<D, false, false, RAB>(m, p, grid_q, grid_kv, stream);
+  if (bf16) return softmax ? launch_bwd_pair<D, DV, true, true, RAB>(m, p, grid_q, grid_kv, stream)
+                           : launch_bwd_pair<D, DV, true, false, RAB>(m, p, grid_q, grid_kv, stream);
+  return softmax ? launch_bwd_pair<D, DV, false, true, RAB>(m, p, grid_q, grid_kv, stream)
+                 : launch_bwd_pair<D, DV, false, false, RAB>(m, p, grid_q, grid_kv, stream);
 }
 
 }  // namespace hstu

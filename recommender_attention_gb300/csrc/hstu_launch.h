@@ -36,6 +36,9 @@ cudaError_t launch_bwd_d64(const BwdMaps& m, const BwdParams& p, bool bf16, bool
                            cudaStream_t stream);
 cudaError_t launch_bwd_d128(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q, int grid_kv,
                             cudaStream_t stream);
+// hdim_qk 96 with hdim_v 96 or 64
+cudaError_t launch_bwd_d96(const BwdMaps& m, const BwdParams& p, int hdim_v, bool bf16, bool softmax, int grid_q,
+                           int grid_kv, cudaStream_t stream);
 // with a relative attention bias (BwdParams::ts_q / rab_time / rab_pos)
 cudaError_t launch_bwd_rab_d64(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q,
                                int grid_kv, cudaStream_t stream);

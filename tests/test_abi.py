@@ -147,8 +147,11 @@ def _bwd_ws(lib, b):
 
 @pytest.mark.parametrize("kw,status", [
     ({}, 0), ({"hdim_qk": 64, "hdim_v": 64}, 0), ({"num_splits": 5}, 0),   # splits are ignored
-    ({"hdim_qk": 96, "hdim_v": 96}, 2), ({"hdim_qk": 256, "hdim_v": 256}, 2),
-    ({"hdim_qk": 96, "hdim_v": 64}, 2), ({"dtype": 7}, 2), ({"batch": 0}, 1),
+    ({"hdim_qk": 96, "hdim_v": 96}, 0), ({"hdim_qk": 256, "hdim_v": 256}, 2),
+    ({"hdim_qk": 96, "hdim_v": 64}, 0), ({"dtype": 7}, 2), ({"batch": 0}, 1),
+    # dv / dO strides are checked against nhead * hdim_v (128 here), dq / dk against nhead * hdim_qk (192)
+    ({"hdim_qk": 96, "hdim_v": 64, "dv_row_stride": 136}, 0), ({"hdim_qk": 96, "hdim_v": 64, "do_row_stride": 120}, 1),
+    ({"hdim_qk": 96, "hdim_v": 64, "dq_row_stride": 136}, 1),
     ({"do_row_stride": 100}, 1), ({"dk_row_stride": 258}, 1), ({"dv_row_stride": 260}, 1)])
 def test_backward_host_validation(lib, kw, status):
     assert _bwd_ws(lib, _bwd(**kw))[0] == status

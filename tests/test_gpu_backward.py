@@ -86,6 +86,20 @@ def test_fuzz_backward(seed, softmax):
     check_backward(w)
 
 
+# ---------------------------------------------------------------- head dimension 96, and 96/64
+@pytest.mark.parametrize("softmax", [False, True])
+@pytest.mark.parametrize("dv", [96, 64])
+def test_hdim96_backward(softmax, dv):
+    check_backward(W.jagged_readme().with_(hdim_qk=96, hdim_v=dv, softmax=softmax))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_fuzz_hdim96_backward(seed):
+    w = W.random_small(200 + seed, hdim=96, hdim_v=[96, 64][seed % 2], softmax=seed % 3 == 2,
+                       dtype="bf16" if seed % 2 else "fp16", kv_targets=seed == 5)
+    check_backward(w)
+
+
 # ---------------------------------------------------------------- with a relative attention bias
 @pytest.mark.parametrize("cfg", ["tiny", "jagged"])
 @pytest.mark.parametrize("softmax", [False, True])
