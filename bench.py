@@ -392,36 +392,61 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
     return out
 
 
-def time_e2e_steps(call, host, dev, steps, warmup, world, stream):
-    """Public-API round trip per step: pinned host q/k/v/offsets/targets -> device,
-    forward, device o -> pinned host."""
+def time_e2e_steps(w, host, device, steps, warmup, world, stream):
+    """Public-API round trip per step from pinned host memory, pipelined over
+    two buffer sets: step i's q/k/v/offsets/targets go host -> device on a copy
+    stream, its forward (hstu_attn_fwd) runs on the compute stream once they
+    have landed, and its o goes device -> pinned host on a third stream, so
+    step i+1's copies overlap step i's forward.  Every step moves its own
+    inputs and its own result; the events order each buffer's reuse."""
     hq, hk, hv, hoff, htg = host
-    dq, dk, dv, doff, dtg = dev
-    ho = torch.empty(call.o.shape, dtype=call.o.dtype, pin_memory=True)
+    sets = []
+    for _ in range(2):
+        call, dev = device_call(w, hq, hk, hv, device)
+        sets.append({"call": call, "dev": dev, "ho": torch.empty(call.o.shape, dtype=call.o.dtype, pin_memory=True),
+                     "ev_in": torch.cuda.Event(), "ev_fwd": torch.cuda.Event(), "ev_out": torch.cuda.Event(),
+                     "used": False})
+    # (copies spread over three copy streams measured the same: the host link,
+    # about 250 GB/s for both directions together, is the limit)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
-    def one():
-        with torch.cuda.stream(stream):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            doff.copy_(hoff, non_blocking=True)
-            dtg.copy_(htg, non_blocking=True)
-            call.launch(stream)
-            ho.copy_(call.o, non_blocking=True)
+    def one(i):
+        b = sets[i % 2]
+        dq, dk, dv, doff, dtg = b["dev"]
+        with torch.cuda.stream(s_in):
+            if b["used"]:
+                s_in.wait_event(b["ev_fwd"])        # the last forward on this set has read its inputs
+            for dst, src in ((dq, hq), (dk, hk), (dv, hv), (doff, hoff), (dtg, htg)):
+                dst.copy_(src, non_blocking=True)
+            b["ev_in"].record(s_in)
+        stream.wait_event(b["ev_in"])
+        if b["used"]:
+            stream.wait_event(b["ev_out"])          # the last read-back of this set's o is done
+        b["call"].launch(stream)
+        b["ev_fwd"].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(b["ev_fwd"])
+            b["ho"].copy_(b["call"].o, non_blocking=True)
+            b["ev_out"].record(s_out)
+        b["used"] = True
 
-    for _ in range(warmup):
-        one()
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize()
     barrier(world)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for _ in range(steps):
-        one()
+    s_in.wait_event(start)
+    for i in range(steps):
+        one(warmup + i)
+    stream.wait_stream(s_out)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hoff, htg))
-    d2h = ho.numel() * ho.element_size()
+    d2h = sets[0]["ho"].numel() * sets[0]["ho"].element_size()
+    for b in sets:
+        b["call"].check(stream)
     return start.elapsed_time(end) / steps, h2d, d2h
 
 
@@ -452,7 +477,7 @@ def run_cuda(args):
     clocks = clk.summary()
     host = tuple(t.pin_memory() for t in (q, k, v, torch.from_numpy(w.seq_offsets_q()),
                                           torch.from_numpy(w.num_targets())))
-    e2e_ms, h2d, d2h = time_e2e_steps(call, host, dev, args.steps, args.warmup, world, stream)
+    e2e_ms, h2d, d2h = time_e2e_steps(w, host, device, args.steps, args.warmup, world, stream)
 
     # the same workload at the other head dimensions (one forward kernel per
     # step, same timing rules): 256, 96 and the asymmetric 96/64
@@ -526,7 +551,9 @@ def run_cuda(args):
                          "kernel": "hstu_fwd_kernel<128,bf16,SiLU>", "kernel_ms": fwd_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max,
+                    "pipelining": "two buffer sets: step i+1's host-to-device copies and step i-1's "
+                                  "read-back overlap step i's forward"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
