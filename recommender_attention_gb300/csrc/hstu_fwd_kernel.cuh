@@ -195,51 +195,51 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
 }
 
 // SiLU of the 64 scores of key columns [c0, c0+64) of one row (fp32 bit
-// patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.  Each
-// 16-pair chunk runs stage by stage so the pairs' latencies overlap.
+// patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.
 template <bool BF16, bool MASKED, bool PRESCALED = false>
 __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tmem, uint32_t ha,
                                           const RowMask& rm, int c0) {
+  // all 32 pairs stage by stage (more independent tanh in flight than two
+  // 16-pair passes; measured 2 % faster per call), one 32-column store
+  uint32_t h[32], t[32];
+  if constexpr (BF16) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    uint32_t h[16], t[16];
-    if constexpr (BF16) {
+    for (int k = 0; k < 32; ++k)
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "r"(r[2 * k + 1]), "r"(r[2 * k]));
+    if constexpr (!PRESCALED) {   // else r already holds alpha s / 2 (plus the halved bias)
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "r"(r[32 * q + 2 * k + 1]), "r"(r[32 * q + 2 * k]));
-      if constexpr (!PRESCALED) {   // else r already holds alpha s / 2 (plus the halved bias)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
-      }
-#pragma unroll
-      for (int k = 0; k < 16; ++k) asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
-#pragma unroll
-      for (int k = 0; k < 16; ++k) asm("fma.rn.bf16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
-    } else {
-      const float haf = PRESCALED ? 1.0f : __uint_as_float(ha);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float h0 = __uint_as_float(r[32 * q + 2 * k]) * haf;
-        const float h1 = __uint_as_float(r[32 * q + 2 * k + 1]) * haf;
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "f"(h1), "f"(h0));
-      }
-#pragma unroll
-      for (int k = 0; k < 16; ++k) asm("tanh.approx.f16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
-#pragma unroll
-      for (int k = 0; k < 16; ++k) asm("fma.rn.f16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
+      for (int k = 0; k < 32; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
     }
-    if constexpr (MASKED) {
-      // bit 2k (2k+1) of the chunk's mask keeps the low (high) half of pair k
-      const uint32_t mb = rm.bits32(c0 + 32 * q);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(mb << (31 - 2 * k)) >> 31);
-        const uint32_t hi = static_cast<uint32_t>(static_cast<int32_t>(mb << (30 - 2 * k)) >> 31);
-        h[k] &= (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
-      }
+    for (int k = 0; k < 32; ++k) asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
+#pragma unroll
+    for (int k = 0; k < 32; ++k) asm("fma.rn.bf16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
+  } else {
+    const float haf = PRESCALED ? 1.0f : __uint_as_float(ha);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float h0 = __uint_as_float(r[2 * k]) * haf;
+      const float h1 = __uint_as_float(r[2 * k + 1]) * haf;
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "f"(h1), "f"(h0));
     }
-    ptx::tmem_st16(p_tmem + 16 * q, h);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) asm("tanh.approx.f16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
+#pragma unroll
+    for (int k = 0; k < 32; ++k) asm("fma.rn.f16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
   }
+  if constexpr (MASKED) {
+    // bit 2k (2k+1) of a chunk's mask keeps the low (high) half of its pair k
+    const uint32_t mb0 = rm.bits32(c0), mb1 = rm.bits32(c0 + 32);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const uint32_t mb = k < 16 ? mb0 : mb1;
+      const int kk = k & 15;
+      const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(mb << (31 - 2 * kk)) >> 31);
+      const uint32_t hi = static_cast<uint32_t>(static_cast<int32_t>(mb << (30 - 2 * kk)) >> 31);
+      h[k] &= (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
+    }
+  }
+  ptx::tmem_st32(p_tmem, h);
 }
 
 template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
