@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the HSTU attention forward.
+"""fp64 CPU oracle for the HSTU attention forward and backward.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import or call this
 module: only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
