@@ -127,8 +127,11 @@ __device__ __forceinline__ RabCols rab_cols(int ts, int pos, bool valid) {
 // position is c.pmin + k (keys of a tile), else it comes from lane k.  Each
 // term is one constant per row when the row's timestamp (position) lies
 // outside the columns' range and both ends fall in the same bucket (are at
-// least np - 1 away); the constant or key-by-key form is chosen per term for
-// the whole warp, so every lane runs the same shuffles.  Warp-collective.
+// least np - 1 away).  The whole warp takes one of three forms, so every lane
+// runs the same shuffles: both terms constant, only the distance looked up
+// key by key, or both looked up (a constant distance term then reads the
+// table's last entry).  Fewer unrolled forms keep the code small enough to
+// stay in the instruction cache.  Warp-collective.
 template <bool CONTIG>
 __device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWarp& w, int np, bool has_time,
                                             const RabRow& row, const RabCols& c) {
@@ -156,15 +159,7 @@ __device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWar
       d = d < np - 1 ? d : np - 1;
       r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, w.pos[d] + wt_const));
     }
-  } else if (all_pos) {    // the time bucket varies, the distance term does not
-    const float bp = w.pos[np - 1];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int tk = __shfl_sync(0xffffffffu, c.ts, k);
-      const float wt = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
-      r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, bp + wt));
-    }
-  } else {
+  } else {   // the time bucket varies (and the distance may)
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
       const int tk = __shfl_sync(0xffffffffu, c.ts, k);
