@@ -194,44 +194,45 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
   return ok;
 }
 
-// SiLU of the 64 scores of key columns [c0, c0+64) of one row (fp32 bit
-// patterns in r); the packed P goes to the 32 TMEM columns at p_tmem.
-template <bool BF16, bool MASKED, bool PRESCALED = false>
-__device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tmem, uint32_t ha,
+// SiLU of the 2 NP scores of key columns [c0, c0 + 2 NP) of one row (fp32 bit
+// patterns in r); the NP packed P words go to the TMEM columns at p_tmem.
+template <bool BF16, bool MASKED, bool PRESCALED = false, int NP = 32>
+__device__ __forceinline__ void silu_half(const uint32_t (&r)[2 * NP], uint32_t p_tmem, uint32_t ha,
                                           const RowMask& rm, int c0) {
-  // all 32 pairs stage by stage (more independent tanh in flight than two
-  // 16-pair passes; measured 2 % faster per call), one 32-column store
-  uint32_t h[32], t[32];
+  static_assert(NP == 16 || NP == 32, "16 or 32 pairs");
+  // all pairs stage by stage (more independent tanh in flight than two
+  // 16-pair passes; measured 2 % faster per call), one store
+  uint32_t h[NP], t[NP];
   if constexpr (BF16) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k)
+    for (int k = 0; k < NP; ++k)
       asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "r"(r[2 * k + 1]), "r"(r[2 * k]));
     if constexpr (!PRESCALED) {   // else r already holds alpha s / 2 (plus the halved bias)
 #pragma unroll
-      for (int k = 0; k < 32; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
+      for (int k = 0; k < NP; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
     }
 #pragma unroll
-    for (int k = 0; k < 32; ++k) asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
+    for (int k = 0; k < NP; ++k) asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
 #pragma unroll
-    for (int k = 0; k < 32; ++k) asm("fma.rn.bf16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
+    for (int k = 0; k < NP; ++k) asm("fma.rn.bf16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
   } else {
     const float haf = PRESCALED ? 1.0f : __uint_as_float(ha);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < NP; ++k) {
       const float h0 = __uint_as_float(r[2 * k]) * haf;
       const float h1 = __uint_as_float(r[2 * k + 1]) * haf;
       asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "f"(h1), "f"(h0));
     }
 #pragma unroll
-    for (int k = 0; k < 32; ++k) asm("tanh.approx.f16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
+    for (int k = 0; k < NP; ++k) asm("tanh.approx.f16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
 #pragma unroll
-    for (int k = 0; k < 32; ++k) asm("fma.rn.f16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
+    for (int k = 0; k < NP; ++k) asm("fma.rn.f16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
   }
   if constexpr (MASKED) {
     // bit 2k (2k+1) of a chunk's mask keeps the low (high) half of its pair k
-    const uint32_t mb0 = rm.bits32(c0), mb1 = rm.bits32(c0 + 32);
+    const uint32_t mb0 = rm.bits32(c0), mb1 = NP > 16 ? rm.bits32(c0 + 32) : 0u;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < NP; ++k) {
       const uint32_t mb = k < 16 ? mb0 : mb1;
       const int kk = k & 15;
       const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(mb << (31 - 2 * kk)) >> 31);
@@ -239,7 +240,8 @@ __device__ __forceinline__ void silu_half(const uint32_t (&r)[64], uint32_t p_tm
       h[k] &= (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
     }
   }
-  ptx::tmem_st32(p_tmem, h);
+  if constexpr (NP == 32) ptx::tmem_st32(p_tmem, h);
+  else ptx::tmem_st16(p_tmem, h);
 }
 
 template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
@@ -800,22 +802,45 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tc_fence_after();
         const uint32_t s_tmem = tmem + lane_base + (si & 1) * 128 + c0;
         uint32_t r[64];
-        ptx::tmem_ld64(s_tmem, r);
-        ptx::tmem_ld_wait(r);
-        if constexpr (RAB) {
-          // r becomes alpha s + rab, scaled for the arithmetic below (SiLU: / 2;
-          // softmax: * log2 e)
+        if constexpr (RAB && !SOFTMAX) {
+          // SiLU with the bias: a runtime loop over the two 32-column halves,
+          // so the bias code is inlined once per tile.  Each half is loaded,
+          // becomes (alpha s + rab) / 2, and packs into its 16 P words at the
+          // columns the one-store form uses (word k holds columns 2k, 2k+1):
+          // half 0 over its own first 16 S columns, half 1 over half 0's
+          // last 16, all already in registers.
           const RabWarp& rw = rabw[warp - 2 - kEpiWarps];
-          const float mul = SOFTMAX ? scale_log2 : 0.5f * p.alpha;
+          const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t x[32];
+            ptx::tmem_ld32(s_tmem + 32 * hh, x);
+            ptx::tmem_ld_wait(x);
+            // keys past the sequence repeat its last one: every column counts in the ranges
+            rab_apply32<true>(x, 0.5f * p.alpha, rw, p.rab_np, has_time, rrow,
+                              rab_cols(hh ? tsk1 : tsk0, j0 + c0 + 32 * hh + lane, true));
+            if (full) silu_half<BF16, false, true, 16>(x, s_tmem + 16 * hh, ha2, rm, c0 + 32 * hh);
+            else silu_half<BF16, true, true, 16>(x, s_tmem + 16 * hh, ha2, rm, c0 + 32 * hh);
+          }
+        } else {
+          ptx::tmem_ld64(s_tmem, r);
+          ptx::tmem_ld_wait(r);
+        }
+        if constexpr (RAB && SOFTMAX) {
+          // r becomes (alpha s + rab) * log2 e
+          const RabWarp& rw = rabw[warp - 2 - kEpiWarps];
           const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
           // keys past the sequence repeat its last one: every column counts in the ranges
-          rab_apply32<true>(r, mul, rw, p.rab_np, has_time, rrow, rab_cols(tsk0, j0 + c0 + lane, true));
-          rab_apply32<true>(r + 32, mul, rw, p.rab_np, has_time, rrow, rab_cols(tsk1, j0 + c0 + 32 + lane, true));
+          rab_apply32<true>(r, scale_log2, rw, p.rab_np, has_time, rrow, rab_cols(tsk0, j0 + c0 + lane, true));
+          rab_apply32<true>(r + 32, scale_log2, rw, p.rab_np, has_time, rrow,
+                            rab_cols(tsk1, j0 + c0 + 32 + lane, true));
         }
         if constexpr (!SOFTMAX) {
-          // P is packed over this warpgroup's S columns (already in registers)
-          if (full) silu_half<BF16, false, RAB>(r, s_tmem, ha2, rm, c0);
-          else silu_half<BF16, true, RAB>(r, s_tmem, ha2, rm, c0);
+          if constexpr (!RAB) {
+            // P is packed over this warpgroup's S columns (already in registers)
+            if (full) silu_half<BF16, false>(r, s_tmem, ha2, rm, c0);
+            else silu_half<BF16, true>(r, s_tmem, ha2, rm, c0);
+          }
         } else {
           float mx = -INFINITY;
           if (full) {
