@@ -225,6 +225,26 @@ def test_defaults_alpha_and_attn_scale():
     np.testing.assert_allclose(o_ovr * 20, o_def * 9, rtol=1e-12)
 
 
+def test_attn_scale_default_per_group_and_empty_group():
+    # zero attn_scale per group: group 0 (UIH 3 and 6) resolves to 1/6 from its
+    # own sequences only; group 1 has no UIH rows at all (context and targets
+    # only) and resolves to 1.0 -- its rows still attend to context keys and
+    # their own target key, so the scale shows in their output
+    rng = np.random.default_rng(10)
+    w = W.random_small(5, cross=False).with_(num_groups=2, batch=4, uih_q=[3, 6, 0, 0],
+                                             targets=[1, 2, 1, 3], context_len=[1, 2],
+                                             local_len=[0, 0], minfull_len=[0, 0], max_uih_len=[0, 0],
+                                             attn_scale=[0.0, 0.0], alpha=0.5, causal=True)
+    q, k, v = (rng.standard_normal((w.total_q, 2, 8)) for _ in range(3))
+    o_def, _ = hstu_attention_forward(q, k, v, w.seq_offsets_q(), None, w.num_targets(), oracle_params(w))
+    explicit = oracle_params(w)
+    explicit.attn_scale = [1.0 / 6, 1.0]
+    o_exp, _ = hstu_attention_forward(q, k, v, w.seq_offsets_q(), None, w.num_targets(), explicit)
+    np.testing.assert_allclose(o_def, o_exp, rtol=1e-13)
+    off = w.seq_offsets_q()
+    assert np.abs(o_def[off[2]:]).max() > 0   # the empty group's rows are not all zero
+
+
 def test_empty_rows_give_zero_and_minus_inf():
     # cross-attention with fewer key UIH than query UIH and no context: the
     # earliest query UIH rows sit before the first key and see nothing
