@@ -373,8 +373,10 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
         barrier(world)
         bw.check(stream)
         ms = reduce_max(a.elapsed_time(b) / steps, world, device)
+        # useful: S, dP, dV, dQ, dK once per allowed pair; executed: both
+        # kernels form S and dP, the dQ kernel dQ, the dK/dV kernel dV and dK
         useful = 2.0 * (3 * w.hdim_qk + 2 * w.hdim_v) * st["allowed_pairs"]
-        executed = 2.0 * 128 * 128 * (5 * w.hdim_qk + 4 * w.hdim_v) * st["executed_tiles"]
+        executed = 2.0 * 128 * 128 * (4 * w.hdim_qk + 3 * w.hdim_v) * st["executed_tiles"]
         tot = reduce_sum(useful, world, device)
         tf = tot / (ms * 1e-3) / 1e12
         per_gpu = useful / (ms * 1e-3) / 1e12
