@@ -12,6 +12,11 @@
 #include "hstu_attn.h"
 #include "hstu_common.cuh"
 #include "hstu_launch.h"
+#include "hstu_rab.cuh"
+
+// The ABI's bias limits size the kernels' shared-memory tables.
+static_assert(HSTU_RAB_MAX_POS == hstu::kRabMaxPos, "positional table size differs from the ABI limit");
+static_assert(HSTU_RAB_TIME_BUCKETS == hstu::kRabTimeBuckets, "time-bucket count differs from the ABI");
 
 using namespace hstu;
 
