@@ -697,9 +697,17 @@ def run_reference(args):
         cpu_baseline(w, q, k, v, budget_s=per_step)
     vals = [cpu_baseline(w, q, k, v, budget_s=per_step) for _ in range(args.steps)]
     value = statistics.mean(x["value"] for x in vals)
+    # a step of the whole workload at the sampled rate (the sample is bounded)
+    from oracle.hstu_oracle import HstuParams, allowed_pair_count
+    p = HstuParams(num_groups=w.num_groups, context_len=w.context_len, local_len=w.local_len,
+                   minfull_len=w.minfull_len, max_uih_len=w.max_uih_len, attn_scale=w.attn_scale,
+                   alpha=w.alpha, causal=w.causal, softmax=w.softmax)
+    step_flops = 2.0 * (w.hdim_qk + w.hdim_v) * allowed_pair_count(w.seq_offsets_q(), None, w.num_targets(), p,
+                                                                   w.nhead)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_flops / (value * 1e12) * 1e3,
+        "ms_per_step_basis": "the whole workload's useful FLOPs at the sampled rate",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic N(0,1) bf16 rounded, seed 7",
         "config": {"workload": f"large jagged SiLU HSTU self-attention, hdim {w.hdim_qk}",

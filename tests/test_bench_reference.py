@@ -1,0 +1,30 @@
+"""bench.py's reference arm (the fp64 oracle on the host cores) prints one
+JSON line with the keys the measurement contract names.  CPU only: a short
+run with a few seconds of oracle work per step."""
+import contextlib
+import io
+import json
+
+import bench
+
+
+def test_reference_arm_line(monkeypatch):
+    for var in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(var, raising=False)
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-seconds", "4"])
+    lines = [x for x in out.getvalue().splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert (d["n_gpus"], d["steps"], d["warmup"]) == (1, 1, 3)
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["dtype"] == "f64"
+    assert d["config"]["workload"].startswith("large jagged") and d["config"]["batch"] == 64
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # the whole step at the sampled rate: the workload's useful FLOPs / value
+    step_flops = d["ms_per_step"] * 1e-3 * d["value"] * 1e12
+    assert 5.0e11 < step_flops < 5.6e11   # 2 * 256 * ~1.03e9 allowed pairs
