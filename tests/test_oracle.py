@@ -630,4 +630,24 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(orc, "query_key_positions", lambda p, rows: np.asarray(rows, dtype=np.int64))
     assert not rab_pins_pass()
     monkeypatch.undo()
-    assert _pins_pass() and _mfalcon_pin_passes() and _backward_pin_passes() and rab_pins_pass()
+
+    # 9. the attn_scale default from the whole batch's largest UIH length
+    #    instead of each group's own
+    def scale_pins_pass():
+        try:
+            test_defaults_alpha_and_attn_scale()
+            test_attn_scale_default_per_group_and_empty_group()
+        except AssertionError:
+            return False
+        return True
+
+    def batch_wide_scales(params, batch, off_q, targets):
+        m = max(orc._seq_params(params, b, batch, off_q, None, targets)[1].uih_q for b in range(batch))
+        return np.array([float(a) if a != 0 else (1.0 / m if m > 0 else 1.0) for a in params.attn_scale])
+
+    assert scale_pins_pass()
+    monkeypatch.setattr(orc, "resolved_attn_scales", batch_wide_scales)
+    assert not scale_pins_pass()
+    monkeypatch.undo()
+    assert (_pins_pass() and _mfalcon_pin_passes() and _backward_pin_passes() and rab_pins_pass()
+            and scale_pins_pass())
