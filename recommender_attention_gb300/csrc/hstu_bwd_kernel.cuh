@@ -222,44 +222,43 @@ __device__ __forceinline__ void mma_half_ts(uint32_t d_tmem, uint32_t a_tmem, ui
   ptx::umma_ts_x4(d_tmem, pa, bd, idesc, accumulate ? 1u : 0u);
 }
 
-// SiLU and its derivative for the 32 scores of one row, on packed bf16 pairs
-// (the forward's SiLU arithmetic): with h = alpha s / 2, t = tanh(h),
+// SiLU and its derivative for the 32 scores of one row, in fp32 (packed f32x2
+// products, tanh.approx.f32 per element): with h = alpha s / 2, t = tanh(h),
 // sig = (1 + t) / 2, SiLU(x) = h (1 + t) and SiLU'(x) = sig + SiLU(x) (1 - sig).
-// pa receives SiLU(x) (when WANT_A), pr receives dp * SiLU'(x); pairs whose bit
-// in `allow` is clear give 0 (MASKED).  PRESCALED: sv already holds h (with a
-// relative attention bias, alpha s / 2 + rab / 2).
-template <bool WANT_A, bool MASKED, bool PRESCALED = false>
-__device__ __forceinline__ void silu_bwd_bf16(const uint32_t (&sv)[32], const uint32_t (&dv)[32], uint32_t ha2,
-                                              uint32_t allow, uint32_t (&pa)[16], uint32_t (&pr)[16]) {
-  constexpr uint32_t kHalf2 = 0x3F003F00u, kNegHalf2 = 0xBF00BF00u;   // bf16 pairs (0.5, 0.5), (-0.5, -0.5)
+// pa receives SiLU(x) (when WANT_A), pr receives dp * SiLU'(x), each rounded
+// once to the storage type; pairs whose bit in `allow` is clear give 0
+// (MASKED).  PRESCALED: sv already holds h (with a relative attention bias,
+// alpha s / 2 + rab / 2).
+template <bool BF16, bool WANT_A, bool MASKED, bool PRESCALED = false>
+__device__ __forceinline__ void silu_bwd_f32(const uint32_t (&sv)[32], const uint32_t (&dv)[32], float half_alpha,
+                                             uint32_t allow, uint32_t (&pa)[16], uint32_t (&pr)[16]) {
+  const uint64_t ha = ptx::f32x2(half_alpha, half_alpha);
+  const uint64_t half = ptx::f32x2(0.5f, 0.5f), neg_half = ptx::f32x2(-0.5f, -0.5f);
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    uint32_t h, t, sg, a, om, d, g, r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "r"(sv[2 * k + 1]), "r"(sv[2 * k]));
-    if constexpr (!PRESCALED) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h) : "r"(ha2));   // else sv holds h
-    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t) : "r"(h));
-    asm("fma.rn.bf16x2 %0, %1, %2, %2;" : "=r"(sg) : "r"(t), "r"(kHalf2));
-    asm("fma.rn.bf16x2 %0, %1, %2, %1;" : "=r"(a) : "r"(h), "r"(t));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(om) : "r"(t), "r"(kNegHalf2), "r"(kHalf2));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(om), "r"(sg));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(g) : "r"(dv[2 * k + 1]), "r"(dv[2 * k]));
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(g), "r"(d));
+    uint64_t h = ptx::f32x2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]));
+    if constexpr (!PRESCALED) h = ptx::mul_f32x2(h, ha);
+    float h0, h1;
+    ptx::f32x2_split(h, h0, h1);
+    const uint64_t t = ptx::f32x2(ptx::tanh_approx(h0), ptx::tanh_approx(h1));
+    const uint64_t sg = ptx::fma_f32x2(t, half, half);        // sig
+    const uint64_t a = ptx::fma_f32x2(h, t, h);               // SiLU(x)
+    const uint64_t om = ptx::fma_f32x2(t, neg_half, half);    // 1 - sig
+    const uint64_t d = ptx::fma_f32x2(a, om, sg);             // SiLU'(x)
+    const uint64_t g = ptx::f32x2(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1]));
+    uint32_t a16 = 0;
+    if constexpr (WANT_A) a16 = ptx::cvt_pack16<BF16>(a);
+    uint32_t r16 = ptx::cvt_pack16<BF16>(ptx::mul_f32x2(g, d));
     if constexpr (MASKED) {
       const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(allow << (31 - 2 * k)) >> 31);
       const uint32_t hi = static_cast<uint32_t>(static_cast<int32_t>(allow << (30 - 2 * k)) >> 31);
       const uint32_t keep = (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
-      a &= keep;
-      r &= keep;
+      a16 &= keep;
+      r16 &= keep;
     }
-    if constexpr (WANT_A) pa[k] = a;
-    pr[k] = r;
+    if constexpr (WANT_A) pa[k] = a16;
+    pr[k] = r16;
   }
-}
-
-__device__ __forceinline__ float tanh_approx(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // Teardown shared by both kernels: after an abort let copies and MMAs in
@@ -447,8 +446,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float alpha = p.alpha;
     const float half_alpha = 0.5f * p.alpha;
-    uint32_t ha2 = 0;
-    if constexpr (BF16) ha2 = pack2<true>(half_alpha, half_alpha);
     constexpr float kLog2e = 1.4426950408889634f;
     int s_it = 0, t_it = 0, u_it = 0, ui = -1;
     bool ok = true;
@@ -537,9 +534,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                               rab_cols(p.ts_q != nullptr ? rab_rel_ts(ck, base) : 0,
                                        j0 + kHalf * hh + 32 * wg + lane, true));
           }
-          if constexpr (BF16 && !SOFTMAX) {
-            if (full) silu_bwd_bf16<false, false, RAB>(sv, dv, ha2, mb, pk, pk);
-            else silu_bwd_bf16<false, true, RAB>(sv, dv, ha2, mb, pk, pk);
+          if constexpr (!SOFTMAX) {
+            if (full) silu_bwd_f32<BF16, false, false, RAB>(sv, dv, half_alpha, mb, pk, pk);
+            else silu_bwd_f32<BF16, false, true, RAB>(sv, dv, half_alpha, mb, pk, pk);
           } else {
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
@@ -548,15 +545,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               for (int e = 0; e < 2; ++e) {
                 const float s = __uint_as_float(sv[k + e]);
                 const float g = __uint_as_float(dv[k + e]);
-                float r;
-                if constexpr (SOFTMAX) {
-                  r = ex2_approx((RAB ? s : s * (alpha * kLog2e)) - lse2) * (g - dlt);
-                } else {
-                  const float h = RAB ? s : s * half_alpha;   // x / 2
-                  const float sig = fmaf(0.5f, tanh_approx(h), 0.5f);
-                  const float xs = 2.0f * h * sig;
-                  r = g * (sig + fmaf(-xs, sig, xs));
-                }
+                const float r = ex2_approx((RAB ? s : s * (alpha * kLog2e)) - lse2) * (g - dlt);
                 ds[e] = ((mb >> (k + e)) & 1u) ? r : 0.f;
               }
               pk[k >> 1] = pack2<BF16>(ds[0], ds[1]);
@@ -742,8 +731,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float alpha = p.alpha;
     const float half_alpha = 0.5f * p.alpha;
-    uint32_t ha2 = 0;
-    if constexpr (BF16) ha2 = pack2<true>(half_alpha, half_alpha);
     constexpr float kLog2e = 1.4426950408889634f;
     const float4* stat4 = reinterpret_cast<const float4*>(&ctl.col_stat[ew][0]);
     int s_it = 0, t_it = 0, a_it = 0, ui = -1;
@@ -844,31 +831,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  p.ts_q != nullptr && p.rab_time != nullptr, krow_rab,
                                  rab_cols(c_ts, c_pos, qi >= 0));
             }
-            if constexpr (BF16 && !SOFTMAX) {
-              if (masked) silu_bwd_bf16<true, true, RAB>(sv, dv, ha2, allow, pp, pd);
-              else silu_bwd_bf16<true, false, RAB>(sv, dv, ha2, allow, pp, pd);
+            if constexpr (!SOFTMAX) {
+              if (masked) silu_bwd_f32<BF16, true, true, RAB>(sv, dv, half_alpha, allow, pp, pd);
+              else silu_bwd_f32<BF16, true, false, RAB>(sv, dv, half_alpha, allow, pp, pd);
             } else {
 #pragma unroll
               for (int k = 0; k < 32; k += 2) {
                 float pv[2], ds[2];
-                float4 st4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if constexpr (SOFTMAX) st4 = stat4[k >> 1];   // columns k, k + 1
+                const float4 st4 = stat4[k >> 1];   // columns k, k + 1
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                   const float s = __uint_as_float(sv[k + e]);
                   const float g = __uint_as_float(dv[k + e]);
-                  float a, r;
-                  if constexpr (SOFTMAX) {
-                    const float l2 = e ? st4.z : st4.x;
-                    const float dl = e ? st4.w : st4.y;
-                    a = ex2_approx((RAB ? s : s * (alpha * kLog2e)) - l2);
-                    r = a * (g - dl);
-                  } else {
-                    const float h = RAB ? s : s * half_alpha;   // x / 2
-                    const float sig = fmaf(0.5f, tanh_approx(h), 0.5f);
-                    a = 2.0f * h * sig;                    // SiLU(x)
-                    r = g * (sig + fmaf(-a, sig, a));      // SiLU'(x) = sig + x sig (1 - sig)
-                  }
+                  const float l2 = e ? st4.z : st4.x;
+                  const float dl = e ? st4.w : st4.y;
+                  const float a = ex2_approx((RAB ? s : s * (alpha * kLog2e)) - l2);
+                  const float r = a * (g - dl);
                   const bool al = (allow >> (k + e)) & 1u;
                   pv[e] = al ? a : 0.f;
                   ds[e] = al ? r : 0.f;
@@ -924,16 +902,11 @@ cudaError_t launch_bwd_pair(const BwdMaps& m, const BwdParams& p, int grid_q, in
   constexpr int smem = BwdCfg<D, DV, RAB>::SMEM_BYTES;
   auto kq = hstu_bwd_dq_kernel<D, DV, BF16, SOFTMAX, RAB>;
   auto kkv = hstu_bwd_dkdv_kernel<D, DV, BF16, SOFTMAX, RAB>;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static_assert(smem + sizeof(BwdCtl) <= 232448, "shared memory over the 227 KB a CTA may use");
+  static std::atomic<unsigned long long> q_attr_set{0}, kv_attr_set{0};
+  cudaError_t e = ensure_smem_attr(kq, smem, q_attr_set);
+  if (e == cudaSuccess) e = ensure_smem_attr(kkv, smem, kv_attr_set);
   if (e != cudaSuccess) return e;
-  static bool attr_done[64] = {};
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
-  }
   kq<<<grid_q, kBwdThreads, smem, stream>>>(m.q, m.k, m.v, m.d_o, m.q8, m.d_o8, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -37,14 +37,17 @@
 // columns, or TMA zero fill past the last head) is never read, and P V with
 // N = 96 reads only the first 96 columns of the V tile.
 //
-// SiLU is evaluated as SiLU(s) = h + h tanh(h), h = s/2, in packed 16-bit
-// arithmetic of the storage type (one tanh.approx per two elements); P is
-// rounded to that type for the second product in any case.
+// The mask and SiLU run in fp32 on the fp32 scores read out of TMEM:
+// SiLU(x) = h + h tanh(h) with h = x / 2, the products in packed f32x2
+// arithmetic and tanh.approx.f32 per element.  P is rounded once, to the
+// storage type, as the A operand of the second product; attn_scale multiplies
+// the fp32 O accumulator in the epilogue (it is linear in P).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "hstu_common.cuh"
+#include "hstu_launch.h"
 #include "hstu_rab.cuh"
 #include "ptx.cuh"
 
@@ -106,12 +109,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
 }
 
 // Bits [0, x) of a word, x clamped to [0, 32].
@@ -195,39 +192,32 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
 }
 
 // SiLU of the 2 NP scores of key columns [c0, c0 + 2 NP) of one row (fp32 bit
-// patterns in r); the NP packed P words go to the TMEM columns at p_tmem.
+// patterns in r), in fp32: h = alpha s / 2 (one packed f32x2 multiply per
+// pair), t = tanh(h) (tanh.approx.f32 per element), SiLU(alpha s) = h + h t
+// (one packed f32x2 fma per pair).  Each pair is rounded once, to the storage
+// type, when it is packed into its P word; the NP words go to the TMEM columns
+// at p_tmem.  PRESCALED: r already holds alpha s / 2 (plus the halved bias).
 template <bool BF16, bool MASKED, bool PRESCALED = false, int NP = 32>
-__device__ __forceinline__ void silu_half(const uint32_t (&r)[2 * NP], uint32_t p_tmem, uint32_t ha,
+__device__ __forceinline__ void silu_pack(const uint32_t (&r)[2 * NP], uint32_t p_tmem, float half_alpha,
                                           const RowMask& rm, int c0) {
   static_assert(NP == 16 || NP == 32, "16 or 32 pairs");
-  // all pairs stage by stage (more independent tanh in flight than two
-  // 16-pair passes; measured 2 % faster per call), one store
-  uint32_t h[NP], t[NP];
-  if constexpr (BF16) {
+  // all pairs stage by stage, so the NP tanh pairs are in flight together; one store
+  const uint64_t ha = ptx::f32x2(half_alpha, half_alpha);
+  uint64_t h[NP];
+  uint32_t pk[NP];
 #pragma unroll
-    for (int k = 0; k < NP; ++k)
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "r"(r[2 * k + 1]), "r"(r[2 * k]));
-    if constexpr (!PRESCALED) {   // else r already holds alpha s / 2 (plus the halved bias)
-#pragma unroll
-      for (int k = 0; k < NP; ++k) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(ha));
-    }
-#pragma unroll
-    for (int k = 0; k < NP; ++k) asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
-#pragma unroll
-    for (int k = 0; k < NP; ++k) asm("fma.rn.bf16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
-  } else {
-    const float haf = PRESCALED ? 1.0f : __uint_as_float(ha);
-#pragma unroll
-    for (int k = 0; k < NP; ++k) {
-      const float h0 = __uint_as_float(r[2 * k]) * haf;
-      const float h1 = __uint_as_float(r[2 * k + 1]) * haf;
-      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h[k]) : "f"(h1), "f"(h0));
-    }
-#pragma unroll
-    for (int k = 0; k < NP; ++k) asm("tanh.approx.f16x2 %0, %1;" : "=r"(t[k]) : "r"(h[k]));
-#pragma unroll
-    for (int k = 0; k < NP; ++k) asm("fma.rn.f16x2 %0, %0, %1, %0;" : "+r"(h[k]) : "r"(t[k]));
+  for (int k = 0; k < NP; ++k) {
+    h[k] = ptx::f32x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+    if constexpr (!PRESCALED) h[k] = ptx::mul_f32x2(h[k], ha);
   }
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    float h0, h1;
+    ptx::f32x2_split(h[k], h0, h1);
+    h[k] = ptx::fma_f32x2(h[k], ptx::f32x2(ptx::tanh_approx(h0), ptx::tanh_approx(h1)), h[k]);
+  }
+#pragma unroll
+  for (int k = 0; k < NP; ++k) pk[k] = ptx::cvt_pack16<BF16>(h[k]);
   if constexpr (MASKED) {
     // bit 2k (2k+1) of a chunk's mask keeps the low (high) half of its pair k
     const uint32_t mb0 = rm.bits32(c0), mb1 = NP > 16 ? rm.bits32(c0 + 32) : 0u;
@@ -237,11 +227,11 @@ __device__ __forceinline__ void silu_half(const uint32_t (&r)[2 * NP], uint32_t 
       const int kk = k & 15;
       const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(mb << (31 - 2 * kk)) >> 31);
       const uint32_t hi = static_cast<uint32_t>(static_cast<int32_t>(mb << (30 - 2 * kk)) >> 31);
-      h[k] &= (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
+      pk[k] &= (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
     }
   }
-  if constexpr (NP == 32) ptx::tmem_st32(p_tmem, h);
-  else ptx::tmem_st16(p_tmem, h);
+  if constexpr (NP == 32) ptx::tmem_st32(p_tmem, pk);
+  else ptx::tmem_st16(p_tmem, pk);
 }
 
 template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
@@ -695,12 +685,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int rloc = quarter * 32 + lane;    // row within the query tile
     const int c0 = wg * 64;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    // alpha/2: a packed bf16 pair (the raw scores are rounded to bf16, whose
-    // range is fp32's, before scaling) or an fp32 bit pattern for fp16 (scaled
-    // in fp32 first so large raw scores cannot overflow fp16)
-    uint32_t ha2;
-    if constexpr (BF16) ha2 = pack2<true>(0.5f * p.alpha, 0.5f * p.alpha);
-    else ha2 = __float_as_uint(0.5f * p.alpha);
+    const float half_alpha = 0.5f * p.alpha;   // SiLU's argument halved: h = alpha s / 2
     const float scale_log2 = p.alpha * 1.4426950408889634f;
     int s_it = 0, q_it = 0, sched_it = 0;
     while (!ctl.abort_flag) {
@@ -819,8 +804,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             // keys past the sequence repeat its last one: every column counts in the ranges
             rab_apply32<true>(x, 0.5f * p.alpha, rw, p.rab_np, has_time, rrow,
                               rab_cols(hh ? tsk1 : tsk0, j0 + c0 + 32 * hh + lane, true));
-            if (full) silu_half<BF16, false, true, 16>(x, s_tmem + 16 * hh, ha2, rm, c0 + 32 * hh);
-            else silu_half<BF16, true, true, 16>(x, s_tmem + 16 * hh, ha2, rm, c0 + 32 * hh);
+            if (full) silu_pack<BF16, false, true, 16>(x, s_tmem + 16 * hh, half_alpha, rm, c0 + 32 * hh);
+            else silu_pack<BF16, true, true, 16>(x, s_tmem + 16 * hh, half_alpha, rm, c0 + 32 * hh);
           }
         } else {
           ptx::tmem_ld64(s_tmem, r);
@@ -838,8 +823,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if constexpr (!SOFTMAX) {
           if constexpr (!RAB) {
             // P is packed over this warpgroup's S columns (already in registers)
-            if (full) silu_half<BF16, false>(r, s_tmem, ha2, rm, c0);
-            else silu_half<BF16, true>(r, s_tmem, ha2, rm, c0);
+            if (full) silu_pack<BF16, false>(r, s_tmem, half_alpha, rm, c0);
+            else silu_pack<BF16, true>(r, s_tmem, half_alpha, rm, c0);
           }
         } else {
           float mx = -INFINITY;
@@ -946,6 +931,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------- host launch
+// One instantiation of the forward: its shared-memory limit set once per
+// device, launched as a programmatic dependent of the scheduler kernel that
+// precedes it on the stream.
+template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB>
+cudaError_t launch_fwd_inst(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
+                            const FwdParams& p, int grid, cudaStream_t stream) {
+  constexpr int smem = FwdCfg<D, DV, SOFTMAX, RAB>::SMEM_BYTES;
+  static_assert(smem + sizeof(FwdSmemCtl) <= 232448, "shared memory over the 227 KB a CTA may use");
+  auto kern = hstu_fwd_kernel<D, DV, BF16, SOFTMAX, RAB>;
+  static std::atomic<unsigned long long> attr_set{0};
+  cudaError_t e = ensure_smem_attr(kern, smem, attr_set);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFwdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, q8, p);
+}
+
+// The four dtype x nonlinearity instantiations of one head-dimension pair.
+template <int D, int DV, bool RAB>
+cudaError_t launch_fwd_dispatch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& q8, const FwdParams& p, bool bf16, bool softmax, int grid,
+                                cudaStream_t stream) {
+  if (bf16) return softmax ? launch_fwd_inst<D, DV, true, true, RAB>(q, k, v, q8, p, grid, stream)
+                           : launch_fwd_inst<D, DV, true, false, RAB>(q, k, v, q8, p, grid, stream);
+  return softmax ? launch_fwd_inst<D, DV, false, true, RAB>(q, k, v, q8, p, grid, stream)
+                 : launch_fwd_inst<D, DV, false, false, RAB>(q, k, v, q8, p, grid, stream);
 }
 
 }  // namespace hstu
