@@ -77,3 +77,52 @@ def kernel_executed_tiles(w) -> int:
             blk = mask[rows]
             total += sum(1 for n in range(nk) if blk[:, 128 * n:128 * n + 128].any())
     return total * w.nhead
+
+
+def _oracle_sequence(task):
+    """One sequence of a one-group self-attention workload through the oracle
+    (a worker of oracle_forward_parallel)."""
+    from oracle.hstu_oracle import hstu_attention_forward
+    qs, ks, vs, targets, params = task
+    L = qs.shape[0]
+    return hstu_attention_forward(qs, ks, vs, np.array([0, L]), None, np.array([targets], dtype=np.int32),
+                                  params)
+
+
+def oracle_forward_parallel(w, q, k, v, processes=None):
+    """oracle_forward of a one-group self-attention workload, one sequence per
+    task on a pool of spawned processes (one BLAS thread each).  Each task gets
+    the attn_scale the whole batch resolves to, so the result equals the
+    whole-batch call.  Returns (o, lse) like oracle_forward."""
+    import dataclasses
+    import multiprocessing as mp
+    import os
+
+    from oracle.hstu_oracle import resolved_attn_scales
+    assert w.num_groups == 1 and not w.cross
+    p = oracle_params(w)
+    off, tg = w.seq_offsets_q(), w.num_targets()
+    tg = np.zeros(w.batch, dtype=np.int32) if tg is None else tg
+    p = dataclasses.replace(p, attn_scale=[float(resolved_attn_scales(p, w.batch, off, tg)[0])])
+    qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
+    order = list(np.argsort(-w.lengths_q()))   # longest first, for the pool's balance
+    tasks = [(qd[off[b]:off[b + 1]], kd[off[b]:off[b + 1]], vd[off[b]:off[b + 1]], int(tg[b]), p) for b in order]
+    saved = {x: os.environ.get(x) for x in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for x in saved:
+        os.environ[x] = "1"
+    try:
+        with mp.get_context("spawn").Pool(processes or os.cpu_count()) as pool:
+            results = pool.map(_oracle_sequence, tasks, chunksize=1)
+    finally:
+        for x, val in saved.items():
+            if val is None:
+                os.environ.pop(x, None)
+            else:
+                os.environ[x] = val
+    o = np.zeros((w.total_q, w.nhead, w.hdim_v))
+    lse = np.full((w.nhead, w.total_q), -np.inf) if w.softmax else None
+    for b, (ob, lb) in zip(order, results):
+        o[off[b]:off[b + 1]] = ob
+        if lse is not None:
+            lse[:, off[b]:off[b + 1]] = lb
+    return o, lse

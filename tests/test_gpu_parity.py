@@ -10,7 +10,7 @@ from oracle.hstu_oracle import (allowed_pair_count,
                                 hstu_attention_forward_rows)
 from recommender_attention_gb300 import workloads as W
 from tests.gpu_helpers import assert_parity, gpu_call, gpu_forward
-from tests.helpers import as_f64, kernel_executed_tiles, oracle_forward, oracle_params
+from tests.helpers import as_f64, kernel_executed_tiles, oracle_forward, oracle_forward_parallel, oracle_params
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +93,18 @@ def test_large_jagged_sampled_parity(hdim):
         for h in range(w.nhead):
             ob, _ = hstu_attention_forward_rows(qd, kd, vd, off, None, w.num_targets(), p, b, h, rows)
             assert_parity(o[off[b] + np.array(rows), h], ob, w.dtype, what=f"b{b} h{h}")
+
+
+def test_large_jagged_whole_output_parity():
+    """The headline workload (hdim 128, SiLU) exactly as the bench launches it,
+    every row of every head against the oracle (composable_kernel README,
+    "Test / Verify": -v=1 checks the whole output against the host reference).
+    The oracle runs after the GPU call, on a pool of spawned processes."""
+    w = W.large_jagged(hdim=128)
+    q, k, v = w.tensors()
+    o, _ = gpu_forward(w, q, k, v)
+    o_ref, _ = oracle_forward_parallel(w, q, k, v)
+    assert_parity(o, o_ref, w.dtype, what=f"{w.name}: all {w.total_q} rows x {w.nhead} heads")
 
 
 # ---------------------------------------------------------------- fuzz
