@@ -281,7 +281,9 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* args, void* stream);
  *    split-KV on long batches, whose fp32 partials need more room).
  *  - The first call on a device looks up the array's device address (which
  *    may load this library's kernels into the context) and sets the kernels'
- *    attributes; make that first call before any stream capture begins.
+ *    attributes; make that first call before any stream capture begins.  If
+ *    the lookup fails the call returns HSTU_ERR_CUDA and the next call tries
+ *    it again; only a successful lookup is kept.
  *  - There is one scratch per device.  Calls on one stream run one after
  *    another and are safe; calls in flight at the same time on different
  *    streams or from different host threads race on it and give wrong results.

@@ -3,9 +3,28 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "hstu_common.cuh"
 
 namespace hstu {
+
+// Raises a kernel's dynamic shared-memory limit to `smem` bytes on the current
+// device, once per device (devices 0..63; others set it on every call).
+// `done` is one bit per device, owned by the caller's kernel instantiation.
+// Safe from several host threads: two first calls may both set the attribute,
+// which is harmless; a bit is published only after a successful set.
+template <typename Kernel>
+inline cudaError_t ensure_smem_attr(Kernel kern, int smem, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Persistent forward over the scheduler's work units; one CTA per SM.  q8 is
 // the q tensor map with 8-row boxes (query tiles whose rows come in two runs).

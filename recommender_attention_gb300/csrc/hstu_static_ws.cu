@@ -1,11 +1,12 @@
 // hstu_attn_fwd_static_ws: the forward with its scratch in a fixed device
 // array of this library instead of a caller-provided workspace.  The call
 // allocates nothing: the array below is placed by the module loader, its
-// device address is looked up once per device, and every later call only
-// clears its header and hands it to hstu_attn_fwd.
+// device address is looked up on a device's first call (and kept once the
+// lookup has succeeded), and every later call only clears its header and hands
+// it to hstu_attn_fwd.
 #include <cuda_runtime.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "hstu_attn.h"
 #include "hstu_common.cuh"
@@ -21,26 +22,24 @@ static __device__ __align__(256) unsigned char g_static_ws[HSTU_STATIC_WS_BYTES]
 
 constexpr int kMaxDevices = 64;
 
-struct DeviceSlot {
-  std::once_flag once;
-  void* addr = nullptr;
-  cudaError_t err = cudaSuccess;
-};
+// Per device: the looked-up address, or nullptr while no lookup has succeeded.
+std::atomic<void*> g_addr[kMaxDevices];
 
-DeviceSlot g_slots[kMaxDevices];
-
-// Device address of g_static_ws on the current device, looked up on the first
-// call for that device only.  nullptr on failure.
+// Device address of g_static_ws on the current device.  Only a successful
+// lookup is kept: a failed one (say, a first call made while the context could
+// not answer) is retried on the next call.  Racing first calls may both look
+// it up; they store the same address.  nullptr on failure.
 void* static_ws_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  DeviceSlot& s = g_slots[dev];
-  std::call_once(s.once, [&s] {
-    void* p = nullptr;
-    s.err = cudaGetSymbolAddress(&p, g_static_ws);
-    s.addr = s.err == cudaSuccess ? p : nullptr;
-  });
-  return s.addr;
+  void* a = g_addr[dev].load(std::memory_order_acquire);
+  if (a != nullptr) return a;
+  if (cudaGetSymbolAddress(&a, g_static_ws) != cudaSuccess) {
+    cudaGetLastError();   // reset the runtime's last error, so this failure shows up in no later check
+    return nullptr;
+  }
+  g_addr[dev].store(a, std::memory_order_release);
+  return a;
 }
 
 }  // namespace
