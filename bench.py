@@ -184,6 +184,20 @@ def recorded_traffic():
         return None
 
 
+# ---------------------------------------------------------------- the workload's description
+def workload_config(w, allowed_pairs: int, world: int) -> dict:
+    """The `config` of both arms' lines: what the workload is, nothing about
+    how an implementation runs it (split counts and tile counts go elsewhere)."""
+    tok = w.total_q
+    in_out = 2 * w.nhead * tok * (2 * w.hdim_qk + 2 * w.hdim_v)
+    return {"workload": f"large jagged SiLU HSTU self-attention, hdim {w.hdim_qk}",
+            "batch": w.batch, "nhead": w.nhead, "hdim_qk": w.hdim_qk, "hdim_v": w.hdim_v,
+            "uih": "U_int[1024,4096]", "targets": "U_int[1,32]", "context_len": 6, "local_len": 0,
+            "minfull_len": 0, "causal": 1, "total_tokens": tok, "allowed_pairs": int(allowed_pairs),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (q+k+v+o %.0f MB > 129 MB)" % (in_out / 1e6)}
+
+
 # ---------------------------------------------------------------- CUDA arm
 def device_call(w, q, k, v, device):
     from recommender_attention_gb300.hstu import HstuCall
@@ -232,7 +246,26 @@ def time_device_steps(call, steps, warmup, world, stream):
     return step_ms, fwd_ms
 
 
-def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float):
+def time_sustained(call, stream, step_ms: float, seconds: float, gpu_index: int, world: int):
+    """The headline step back to back for about `seconds` (long enough for the
+    power cap and clocks to settle), with its own clock samples.  Returns
+    (ms per step, steps, clock summary)."""
+    n = max(20, int(seconds / (step_ms * 1e-3)))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    with ClockSampler(gpu_index) as clk:
+        start.record(stream)
+        for _ in range(n):
+            call.launch(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    call.check(stream)
+    return start.elapsed_time(end) / n, n, clk.summary()
+
+
+def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float, only=None):
     """The other workloads of the scope (tiny, jagged, batched, group cross
     split-KV in SiLU and softmax, an M-FALCON candidate microbatch over cached
     history keys): one whole call (scheduler + forward [+
@@ -246,6 +279,16 @@ def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float)
              ("group_cross_splitkv_silu", W.group_cross_splitkv(softmax=False), {}),
              ("group_cross_splitkv_softmax", W.group_cross_splitkv(softmax=True), {}),
              ("mfalcon_microbatch", W.mfalcon(), {})]
+    # the split-KV workload with the split count forced, beside the automatic choice
+    for splits in (2, 4):
+        for sm in (False, True):
+            cases.append((f"group_cross_splitkv_{'softmax' if sm else 'silu'}_splits{splits}",
+                          W.group_cross_splitkv(softmax=sm), {"num_splits": splits}))
+    if only:
+        unknown = set(only) - {c[0] for c in cases}
+        if unknown:
+            raise SystemExit(f"unknown scope workload(s): {sorted(unknown)}")
+        cases = [c for c in cases if c[0] in only]
     out = {}
     for name, w, over in cases:
         q, k, v = w.tensors()
@@ -277,14 +320,31 @@ def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float)
             times.append(a.elapsed_time(b))
         call.check(stream)
         ms = statistics.median(times)
+        # the forward kernel alone (events between the scheduler and the forward
+        # launch, which stop their overlap; the rest of the call is the
+        # scheduler, the combine and the launch gaps)
+        ktimes = []
+        for _ in range(steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+            ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            ev[0].record(stream)
+            ev[1].record(stream)
+            call.launch(stream, events=ev)
+            ev[1].synchronize()
+            ktimes.append(ev[0].elapsed_time(ev[1]))
+        call.check(stream)
+        kms = statistics.median(ktimes)
         tq, tkv = dq.shape[0], dk.shape[0]
         nbytes = 2 * w.nhead * (tq * w.hdim_qk + tkv * (w.hdim_qk + w.hdim_v) + tq * w.hdim_v)
         if w.softmax:
             nbytes += 4 * w.nhead * tq
         flops = 2.0 * (w.hdim_qk + w.hdim_v) * st["allowed_pairs"]
         gbs = nbytes / (ms * 1e-3) / 1e9
+        kgbs = nbytes / (kms * 1e-3) / 1e9
         out[name] = {"ms": ms, "tflops_useful": flops / (ms * 1e-3) / 1e12, "gbs_algorithmic": gbs,
                      "hbm_frac": gbs / hbm_peak, "algorithmic_bytes": nbytes,
+                     "fwd_kernel_ms": kms, "fwd_kernel_hbm_frac": kgbs / hbm_peak,
                      "allowed_pairs": st["allowed_pairs"], "executed_tiles": st["executed_tiles"],
                      "num_splits": st["num_splits"], "timing": f"median of {steps}, L2 flushed between calls"}
         del call, dq, dk, dv
@@ -466,6 +526,18 @@ def run_cuda(args):
     barrier(world)
     hstu.load_library()
     stream = torch.cuda.Stream(device)
+    if args.scope_only is not None:
+        # only the other scope workloads (for profiling them); not the bench line
+        if rank == 0:
+            peaks0, _ = load_peaks()
+            only = [x for x in args.scope_only.split(",") if x]
+            lines = small_config_lines(device, stream, args.steps, args.warmup,
+                                       float(peaks0.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), only)
+            print(json.dumps({"scope_only": True, "configs": lines}), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
 
     w = rank_workload(rank, args.hdim)
     q, k, v = w.tensors()
@@ -477,6 +549,12 @@ def run_cuda(args):
     with ClockSampler(local) as clk:
         step_ms, fwd_ms = time_device_steps(call, args.steps, args.warmup, world, stream)
     clocks = clk.summary()
+    sustained = None
+    if args.sustained_seconds > 0:
+        s_ms, s_n, s_clk = time_sustained(call, stream, step_ms, args.sustained_seconds, local, world)
+        s_ms = reduce_max(s_ms, world, device)
+        sustained = {"ms_per_step": s_ms, "steps": s_n, "seconds": s_ms * s_n * 1e-3, "clocks": s_clk,
+                     "timing": "the headline step back to back on the same resident inputs (larger than L2)"}
     host = tuple(t.pin_memory() for t in (q, k, v, torch.from_numpy(w.seq_offsets_q()),
                                           torch.from_numpy(w.num_targets())))
     e2e_ms, h2d, d2h = time_e2e_steps(w, host, device, args.steps, args.warmup, world, stream)
@@ -536,15 +614,9 @@ def run_cuda(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic N(0,1) bf16, seed 7 (+rank)",
-            "config": {"workload": f"large jagged SiLU HSTU self-attention, hdim {w.hdim_qk}",
-                       "batch": w.batch, "nhead": w.nhead, "hdim_qk": w.hdim_qk,
-                       "hdim_v": w.hdim_v, "uih": "U_int[1024,4096]", "targets": "U_int[1,32]",
-                       "context_len": 6, "local_len": 0, "minfull_len": 0, "causal": 1,
-                       "total_tokens": w.total_q, "allowed_pairs": st["allowed_pairs"],
-                       "executed_tiles": st["executed_tiles"], "num_splits": st["num_splits"],
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (q+k+v+o %.0f MB > 129 MB)" %
-                             ((q.numel() + k.numel() + v.numel() + q.numel()) * 2 / 1e6)},
+            "config": workload_config(w, st["allowed_pairs"], world),
+            "schedule": {"executed_tiles": st["executed_tiles"], "num_splits": st["num_splits"],
+                         "work_units": st["work_units"]},
             "pct_of_bf16_peak": 100.0 * value / world / peak,
             "executed_tile_tflops": reduce_sum(exec_flops, 1) / (step_ms_max * 1e-3) / 1e12,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
@@ -559,6 +631,14 @@ def run_cuda(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+        if sustained is not None:
+            sp = float(peaks.get("bf16_tflops_sustained", peak))
+            sv = total_flops / (sustained["ms_per_step"] * 1e-3) / 1e12
+            sustained.update({"value": sv, "unit": UNIT, "peak": sp,
+                              "peak_source": f"{src} bf16 dense (sustained)" if "bf16_tflops_sustained" in peaks
+                              else f"{src} bf16 dense (burst; no sustained figure)",
+                              "frac": sv / world / sp})
+            line["sustained"] = sustained
         line.update(extra)
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -691,27 +771,32 @@ def run_reference(args):
         return
     w = rank_workload(0, args.hdim)
     q, k, v = w.tensors()
-    # each step: a bounded sample of the workload through the oracle
-    per_step = max(1.0, min(20.0, args.ref_seconds / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        cpu_baseline(w, q, k, v, budget_s=per_step)
-    vals = [cpu_baseline(w, q, k, v, budget_s=per_step) for _ in range(args.steps)]
-    value = statistics.mean(x["value"] for x in vals)
-    # a step of the whole workload at the sampled rate (the sample is bounded)
     from oracle.hstu_oracle import HstuParams, allowed_pair_count
     p = HstuParams(num_groups=w.num_groups, context_len=w.context_len, local_len=w.local_len,
                    minfull_len=w.minfull_len, max_uih_len=w.max_uih_len, attn_scale=w.attn_scale,
                    alpha=w.alpha, causal=w.causal, softmax=w.softmax)
-    step_flops = 2.0 * (w.hdim_qk + w.hdim_v) * allowed_pair_count(w.seq_offsets_q(), None, w.num_targets(), p,
-                                                                   w.nhead)
+    pairs = allowed_pair_count(w.seq_offsets_q(), None, w.num_targets(), p, w.nhead)
+    # Each step is one bounded sample of the workload through the oracle (whole
+    # (sequence, head) problems, longest first, for a fixed time budget); the
+    # step's time is that sample's measured time and its rate the sample's.
+    per_step = max(1.0, min(20.0, args.ref_seconds / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, q, k, v, budget_s=per_step)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        vals.append(cpu_baseline(w, q, k, v, budget_s=per_step))
+        secs.append(time.perf_counter() - t0)
+    value = statistics.mean(x["value"] for x in vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_flops / (value * 1e12) * 1e3,
-        "ms_per_step_basis": "the whole workload's useful FLOPs at the sampled rate",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "ms_per_step_basis": f"measured wall time of one step; a step is a bounded sample of about "
+                             f"{per_step:.1f} s of the workload (whole (sequence, head) problems, longest "
+                             f"first), not the whole workload",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic N(0,1) bf16 rounded, seed 7",
-        "config": {"workload": f"large jagged SiLU HSTU self-attention, hdim {w.hdim_qk}",
-                   "batch": w.batch, "nhead": w.nhead},
+        "data": "synthetic N(0,1) bf16, seed 7 (+rank)",
+        "config": workload_config(w, pairs, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
                          "cores": vals[0]["cores"], "sample": vals[0]["sample"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -733,6 +818,11 @@ def main(argv=None):
     ap.add_argument("--no-configs", action="store_true", help="skip the other scope workloads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--scope-only", default=None, metavar="NAMES",
+                    help="run only these scope workloads (comma-separated names of the 'configs' lines; "
+                         "empty: all) and print their lines alone; for profiling")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="seconds of back-to-back headline steps for the 'sustained' figure (0: skip)")
     args = ap.parse_args(argv)
     if args.impl == "cuda":
         args.warmup = max(3, args.warmup)   # timing rule: at least 3 untimed warm-up steps
