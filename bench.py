@@ -268,8 +268,7 @@ def time_sustained(call, stream, step_ms: float, seconds: float, gpu_index: int,
 def small_config_lines(device, stream, steps: int, warmup: int, hbm_peak: float, only=None):
     """The other workloads of the scope (tiny, jagged, batched, group cross
     split-KV in SiLU and softmax, an M-FALCON candidate microbatch over cached
-    history keys): one whole call (scheduler + forward [+
-    combine]) timed with CUDA events on the launching stream, L2 flushed
+    history keys): one whole call (scheduler + forward [+ combine]) timed with CUDA events on the launching stream, L2 flushed
     between calls (their inputs fit in L2).  Reported as useful TFLOP/s and
     algorithmic HBM GB/s (q, k, v read once, o and lse written once)."""
     from recommender_attention_gb300.hstu import HstuCall
@@ -608,7 +607,7 @@ def run_cuda(args):
         achieved = flops_step / (fwd_ms * 1e-3) / 1e12
         traffic = recorded_traffic()
         cpu = None if args.no_cpu_baseline else cpu_baseline(w, q, k, v, budget_s=args.cpu_seconds)
-        launches_per_step = 2 + (1 if st["num_splits"] > 1 else 0)
+        launches_per_step = 2 + (1 if st["num_splits"] > 1 else 0)   # scheduler, forward [, combine]
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,

@@ -164,8 +164,9 @@ hstu_status hstu_attn_fwd_workspace_size(const hstu_fwd_args* args, size_t* byte
 
 /*
  * The forward (README "Forward computation").  Launches, on `stream`, the
- * scheduler kernel, the persistent tcgen05 forward kernel and, with split-KV,
- * the combine kernel; returns without synchronising.  Host-checkable errors
+ * scheduler kernel, the persistent tcgen05 forward kernel and, with split-KV
+ * (README "Split-KV"), the combine kernel that merges the splits' fp32
+ * partials into o (and lse); returns without synchronising.  Host-checkable errors
  * return before anything is launched and leave o/lse untouched.
  * Data-dependent errors (bad offsets, lengths beyond the hints) make the
  * kernels skip all work and set the device error word, read back by

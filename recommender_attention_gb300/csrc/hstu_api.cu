@@ -1,6 +1,6 @@
 // C ABI of the HSTU forward and backward: argument validation, workspace
-// planning, TMA tensor-map encoding and the launches (scheduler -> forward ->
-// combine; scheduler -> row sums -> dQ -> dK/dV).
+// planning, TMA tensor-map encoding and the launches (scheduler -> forward
+// [-> split-KV combine]; scheduler -> row sums -> dQ -> dK/dV).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -128,10 +128,13 @@ int choose_splits(const hstu_fwd_args* a, int max_seq_q, int max_seq_kv, int sms
   const long long q_tiles = (max_seq_q + kBlockM - 1) / kBlockM;
   const long long units = static_cast<long long>(a->batch) * q_tiles * a->nhead;
   const int kv_tiles = (max_seq_kv + kBlockN - 1) / kBlockN;
-  const long long target = 4LL * (sms > 0 ? sms : 148);
-  if (units >= target || kv_tiles < 8) return 1;
+  // about 8 units per SM: the splits of long key ranges balance the persistent
+  // queue; each split keeps at least 12 key tiles, so the partials' extra
+  // traffic (written, then merged by the combine kernel) stays small
+  const long long target = 8LL * (sms > 0 ? sms : 148);
+  if (units >= target || kv_tiles < 24) return 1;
   long long s = (target + units - 1) / units;
-  if (s > kv_tiles / 4) s = kv_tiles / 4;
+  if (s > kv_tiles / 12) s = kv_tiles / 12;
   if (s > kMaxSplits) s = kMaxSplits;
   return s < 1 ? 1 : static_cast<int>(s);
 }
@@ -350,15 +353,21 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   const int D = a->hdim_qk;
   const int64_t wq = static_cast<int64_t>(a->nhead) * D;
   const int64_t wv = static_cast<int64_t>(a->nhead) * a->hdim_v;
-  CUtensorMap tq, tk, tv, tq8;
-  if (!encode_map(&tq, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq)) ||
-      !encode_map(&tq8, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq), 8) ||
-      !encode_map(&tk, a->k, bf16, wq, a->total_kv, packed_or(a->k_row_stride, wq)) ||
-      !encode_map(&tv, a->v, bf16, wv, a->total_kv, packed_or(a->v_row_stride, wv)))
+  FwdMaps maps;
+  if (!encode_map(&maps.q, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq)) ||
+      !encode_map(&maps.q8, a->q, bf16, wq, a->total_q, packed_or(a->q_row_stride, wq), 8) ||
+      !encode_map(&maps.k, a->k, bf16, wq, a->total_kv, packed_or(a->k_row_stride, wq)) ||
+      !encode_map(&maps.v, a->v, bf16, wv, a->total_kv, packed_or(a->v_row_stride, wv)) ||
+      !encode_map(&maps.o, a->o, bf16, wv, a->total_q, packed_or(a->o_row_stride, wv), 32))
     return HSTU_ERR_CUDA;
 
   const PrepParams pp = make_prep(a, pl);
-  if (launch_prep(pp, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  // Batches up to kFusedMaxBatch sequences are scheduled inside the forward
+  // kernel, after a one-block reset of the header; larger ones by the
+  // scheduler kernel.
+  const bool fused = a->batch <= kFusedMaxBatch;
+  if ((fused ? launch_fwd_reset(pp.ws_header, stream) : launch_prep(pp, stream)) != cudaSuccess)
+    return HSTU_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   FwdParams fp;
@@ -394,17 +403,26 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
     fp.rab_np = a->rab_pos != nullptr ? a->rab_pos_buckets : 1;
   }
   fill_group_params(a, fp.ctx, fp.loc, fp.mf);
+  fp.fused = fused ? 1 : 0;
+  fp.total_kv = a->total_kv;
+  fp.max_seqlen_q = pl.max_seq_q;
+  fp.max_seqlen_kv = pl.max_seq_kv;
+  for (int g = 0; g < kMaxGroups; ++g) {
+    fp.max_uih[g] = pp.max_uih[g];
+    fp.attn_scale[g] = pp.attn_scale[g];
+  }
   const int grid = pl.max_units < sms ? (pl.max_units > 0 ? pl.max_units : 1) : sms;
   if (a->event_fwd_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_begin), stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
   cudaError_t e;
-  if (rab) e = D == 64 ? launch_fwd_rab_d64(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream)
-                       : launch_fwd_rab_d128(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
-  else if (D == 64) e = launch_fwd_d64(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
-  else if (D == 96) e = launch_fwd_d96(tq, tk, tv, tq8, fp, a->hdim_v, bf16, a->softmax != 0, grid, stream);
-  else if (D == 128) e = launch_fwd_d128(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
-  else e = launch_fwd_d256(tq, tk, tv, tq8, fp, bf16, a->softmax != 0, grid, stream);
+  const bool sm = a->softmax != 0;
+  if (rab) e = D == 64 ? launch_fwd_rab_d64(maps, fp, bf16, sm, grid, stream)
+                       : launch_fwd_rab_d128(maps, fp, bf16, sm, grid, stream);
+  else if (D == 64) e = launch_fwd_d64(maps, fp, bf16, sm, grid, stream);
+  else if (D == 96) e = launch_fwd_d96(maps, fp, a->hdim_v, bf16, sm, grid, stream);
+  else if (D == 128) e = launch_fwd_d128(maps, fp, bf16, sm, grid, stream);
+  else e = launch_fwd_d256(maps, fp, bf16, sm, grid, stream);
   if (e != cudaSuccess) return HSTU_ERR_CUDA;
   if (a->event_fwd_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_end), stream) != cudaSuccess)
@@ -418,17 +436,15 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
     cp.o_part = fp.o_part;
     cp.ml_part = fp.ml_part;
     cp.off_q = a->seq_offsets_q;
-    cp.group_scale = pp.group_scale;
     cp.ws_header = pp.ws_header;
     cp.o_stride = fp.o_stride;
     cp.total_q = a->total_q;
     cp.nhead = a->nhead;
     cp.batch = a->batch;
-    cp.batch_per_group = fp.batch_per_group;
     cp.splits = pl.splits;
-    cp.softmax = a->softmax;
-    if (launch_combine(cp, a->hdim_v, bf16, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+    if (launch_combine(cp, a->hdim_v, bf16, sm, sms, stream) != cudaSuccess) return HSTU_ERR_CUDA;
   }
+
   return HSTU_OK;
 }
 

@@ -32,6 +32,8 @@ namespace hstu {
 
 constexpr int kBlockM = 128;      // query rows per tile
 constexpr int kBlockN = 128;      // keys per tile
+constexpr int kFwdEpiWarps = 4;   // epilogue warps of the forward kernel (32 query rows each)
+constexpr int kFusedMaxBatch = 128;   // largest batch the forward kernel schedules by itself
 constexpr int kMaxGroups = 256;   // per-group parameter slots in the launch parameters
 constexpr int kMaxSplits = 16;
 
@@ -339,7 +341,14 @@ struct FwdParams {
   const float* rab_time;
   const float* rab_pos;
   int rab_np;
+  // in-kernel scheduling (fused != 0, batch <= kFusedMaxBatch): every CTA
+  // validates the offsets and orders the units itself; units and
+  // group_scale above are then unused
+  int fused;
+  int total_kv, max_seqlen_q, max_seqlen_kv;
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
+  int max_uih[kMaxGroups];        // per-group override of the attn_scale default (0 = automatic)
+  float attn_scale[kMaxGroups];   // per-group attn_scale (0 = 1 / max UIH length of the group)
 };
 
 // Per query tile, for the backward's key-tile units: its TileSet (6 range ends
@@ -399,20 +408,27 @@ struct BwdParams {
   const float* rab_time;
   const float* rab_pos;
   int rab_np;
+  // in-kernel scheduling (fused != 0, batch <= kFusedMaxBatch): every CTA
+  // validates the offsets and orders the units itself; units and
+  // group_scale above are then unused
+  int fused;
+  int total_kv, max_seqlen_q, max_seqlen_kv;
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
+  int max_uih[kMaxGroups];        // per-group override of the attn_scale default (0 = automatic)
+  float attn_scale[kMaxGroups];   // per-group attn_scale (0 = 1 / max UIH length of the group)
 };
 
 // Combine kernel parameters (split-KV).
+// Split-KV combine kernel parameters.  The partials are already x attn_scale.
 struct CombineParams {
   void* o;
   float* lse;
-  const float* o_part;
-  const float* ml_part;
+  const float* o_part;     // [splits, total_q, nhead, hdim_v]
+  const float* ml_part;    // [splits, nhead, total_q, 2]: running max (log2 units), row sum
   const int* off_q;
-  const float* group_scale;
   const int* ws_header;
   long long o_stride;
-  int total_q, nhead, batch, batch_per_group, splits, softmax;
+  int total_q, nhead, batch, splits;
 };
 
 // Fills the geometry of sequence b from the device/host offset arrays.

@@ -4,10 +4,9 @@
 
 namespace hstu {
 
-cudaError_t launch_fwd_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                            const CUtensorMap& q8, const FwdParams& p, bool bf16, bool softmax, int grid,
+cudaError_t launch_fwd_d128(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
                             cudaStream_t stream) {
-  return launch_fwd_dispatch<128, 128, false>(q, k, v, q8, p, bf16, softmax, grid, stream);
+  return launch_fwd_dispatch<128, 128, false>(m, p, bf16, softmax, grid, stream);
 }
 
 }  // namespace hstu

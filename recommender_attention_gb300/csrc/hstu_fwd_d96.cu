@@ -5,11 +5,10 @@
 
 namespace hstu {
 
-cudaError_t launch_fwd_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
-                           const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
+cudaError_t launch_fwd_d96(const FwdMaps& m, const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
                            cudaStream_t stream) {
-  if (hdim_v == 96) return launch_fwd_dispatch<96, 96, false>(q, k, v, q8, p, bf16, softmax, grid, stream);
-  if (hdim_v == 64) return launch_fwd_dispatch<96, 64, false>(q, k, v, q8, p, bf16, softmax, grid, stream);
+  if (hdim_v == 96) return launch_fwd_dispatch<96, 96, false>(m, p, bf16, softmax, grid, stream);
+  if (hdim_v == 64) return launch_fwd_dispatch<96, 64, false>(m, p, bf16, softmax, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -8,7 +8,7 @@
 //       = exp(alpha S - m) with a running max m                 (softmax mode, online)
 //     O += P V                        tcgen05.mma, A = P from TMEM (aliasing S), B = V (MN-major)
 // and writes O * attn_scale (softmax: / rowsum, plus LSE) or, with split-KV,
-// fp32 partials for the combine kernel.
+// fp32 partials (x attn_scale) and row statistics for the combine kernel.
 //
 // Roles (512 threads, one CTA per SM, all waits time-bounded):
 //   warp 0       Q/K producer: TMA loads of Q once per unit (the next unit's Q
@@ -69,13 +69,24 @@ struct FwdCfg {
   static constexpr int VTILE_BYTES = VCH * CHUNK_BYTES;   // one V tile
   // Q is double-buffered where it fits so the next unit's Q streams in early.
   static constexpr int QBUF = D <= 128 ? 2 : 1;
-  // K ring depth (one stage less with a relative attention bias, whose tables take its room)
-  static constexpr int KSTAGES = D == 64 ? 4 : (D <= 128 ? ((SOFTMAX || RAB) ? 2 : 3) : 1);
+  // K ring depth: two stages at hdim 128 (the O staging of the TMA-store
+  // epilogue, the softmax scratch and the bias tables take the third's room);
+  // three at hdim 96, four at hdim 64
+  static constexpr int KSTAGES = D == 64 ? 4 : (D <= 128 ? ((SOFTMAX || RAB || D == 128) ? 2 : 3) : 1);
   static constexpr int VSTAGES = D == 64 ? 4 : (D <= 128 ? 2 : 1);                   // V ring depth
   static constexpr int TILES_BYTES = (QBUF + KSTAGES) * TILE_BYTES + VSTAGES * VTILE_BYTES;
   static constexpr int SOFTMAX_BYTES = SOFTMAX ? static_cast<int>(sizeof(SoftmaxScratch)) : 0;
   static constexpr int RAB_BYTES = RAB ? static_cast<int>(sizeof(RabWarp)) * 8 : 0;   // one per elementwise warp
-  static constexpr int SMEM_BYTES = TILES_BYTES + SOFTMAX_BYTES + RAB_BYTES + 1024;
+  // TMA-store epilogue (output widths that are whole 64-column boxes): per
+  // epilogue warp, STAGE_BUFS buffers of one 32-row x 64-column box (4 KB,
+  // 128-byte swizzle); two when they fit in the 227 KB a CTA may use (with
+  // 2 KB kept for the static control block), else one
+  static constexpr int STAGE_BOX_BYTES = 32 * 128;
+  static constexpr int BASE_BYTES = TILES_BYTES + SOFTMAX_BYTES + RAB_BYTES + 1024;
+  static constexpr int STAGE_BUFS =
+      DV % 64 != 0 ? 0 : (BASE_BYTES + 2 * kFwdEpiWarps * STAGE_BOX_BYTES + 2048 <= 232448 ? 2 : 1);
+  static constexpr int STAGE_BYTES = STAGE_BUFS * kFwdEpiWarps * STAGE_BOX_BYTES;
+  static constexpr int SMEM_BYTES = BASE_BYTES + STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 256;
   static constexpr int O_BUFS = DV <= 128 ? 2 : 1;
@@ -83,13 +94,12 @@ struct FwdCfg {
   static_assert(D % 16 == 0 && DV % 32 == 0 && DV <= 256, "head dimensions");
 };
 
-constexpr int kEpiWarps = 4;       // epilogue warpgroup
+constexpr int kEpiWarps = kFwdEpiWarps;   // epilogue warpgroup
 constexpr int kEwThreads = 256;    // two elementwise warpgroups
 constexpr int kFwdThreads = 64 + 32 * kEpiWarps + kEwThreads + 64;   // 512: 128 registers per thread
 constexpr int kSchedWarp = kFwdThreads / 32 - 2;
 constexpr int kVProdWarp = kFwdThreads / 32 - 1;
 constexpr int kSchedDepth = 2;   // published-unit ring (deeper claims ahead hurt the tail balance)
-constexpr int kSchedBatch = 1;   // units taken from the global queue per atomic
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait, then give up
 
 
@@ -168,7 +178,153 @@ struct FwdSmemCtl {
   int sched_live[kSchedDepth];        // 0: no more units
   uint32_t tmem_base;
   volatile int abort_flag;
+  // in-kernel schedule (FwdParams::fused): position -> sequence (longest
+  // first), first unit of each position, attn_scale of each position's group,
+  // and the device error bits the offsets raised
+  uint8_t f_order[kFusedMaxBatch];
+  int f_ubase[kFusedMaxBatch + 1];
+  float f_pscale[kFusedMaxBatch];
+  int f_err;
 };
+
+// Largest k in [0, n) with a[k] <= x (a non-decreasing, a[0] <= x).
+__device__ __forceinline__ int seg_find(const int* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Exclusive prefix sum of v[0, n) (n <= 32 * 4) by one warp, in place; v[n]
+// receives the total.
+__device__ __forceinline__ void warp_exclusive_scan(int* v, int n, int lane) {
+  constexpr int kPer = kFusedMaxBatch / 32;
+  int loc[kPer], sum = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = lane * kPer + k;
+    loc[k] = i < n ? v[i] : 0;
+    sum += loc[k];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = lane * kPer + k;
+    if (i < n) v[i] = run;
+    run += loc[k];
+  }
+  if (lane == 31) v[n] = incl;
+}
+
+// The scheduler's work, done by every CTA for itself (FwdParams::fused, batch
+// <= kFusedMaxBatch), by all threads of the CTA before any role starts, so
+// that no separate scheduler kernel runs before the forward.  The same
+// validation and order as hstu_prep_kernel: each sequence's offsets are
+// checked (errors go to ctl.f_err and leave no units), its query tiles and
+// executed key tiles are counted, the sequences are ranked by executed tiles
+// (most first, ties by index) and the units are numbered per position with
+// heads outer, query tiles from the last down and splits innermost.
+// `scratch` (3 batch + 2 ints) is shared memory no TMA load uses yet.
+// Returns the number of units.
+__device__ __forceinline__ int fused_schedule(const FwdParams& p, FwdSmemCtl& ctl, int* scratch, int tid, int nthreads) {
+  const int B = p.batch;
+  const int G = p.num_groups;
+  int* tb = scratch;        // [B + 1] query tiles per sequence, then their exclusive prefix
+  int* cost = tb + B + 1;   // [B] executed key tiles per sequence
+  int* gmax = cost + B;     // [G] largest query UIH length of each group
+  for (int i = tid; i < B; i += nthreads) cost[i] = 0;
+  for (int g = tid; g < G; g += nthreads) gmax[g] = 0;
+  if (tid == 0) ctl.f_err = 0;
+  __syncthreads();
+  for (int b = tid; b < B; b += nthreads) {
+    const int g = b / p.batch_per_group;
+    const int c = p.ctx[g];
+    int err = 0;
+    const int q0 = p.off_q[b], q1 = p.off_q[b + 1];
+    if (q0 < 0 || q1 < q0 || q1 > p.total_q) err |= kErrOffsets;
+    const int t = p.targets ? p.targets[b] : 0;
+    if (t < 0 || q1 - q0 < c + t) err |= kErrQLayout;
+    int Lkv = q1 - q0;
+    if (!p.self_attn) {
+      const int k0 = p.off_kv[b], k1 = p.off_kv[b + 1];
+      if (k0 < 0 || k1 < k0 || k1 > p.total_kv) err |= kErrOffsets;
+      Lkv = k1 - k0;
+      if (Lkv < c + (p.kv_targets ? t : 0)) err |= kErrKvLayout;
+    }
+    if (q1 - q0 > p.max_seqlen_q || Lkv > p.max_seqlen_kv) err |= kErrMaxSeqlen;
+    if (err) atomicOr(&ctl.f_err, err);
+    else atomicMax(&gmax[g], q1 - q0 - c - t);
+    tb[b] = err ? 0 : q_layout(q1 - q0, c).nq;
+  }
+  __syncthreads();
+  if (ctl.f_err != 0) return 0;
+  if (tid < 32) warp_exclusive_scan(tb, B, tid);
+  __syncthreads();
+  const int n_items = tb[B];
+  for (int i = tid; i < n_items; i += nthreads) {
+    const int b = seg_find(tb, B, i);
+    const int g = b / p.batch_per_group;
+    const SeqGeom sg = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[g], p.loc[g], p.mf[g], p.causal,
+                                 p.self_attn, p.kv_targets);
+    atomicAdd(&cost[b], query_tile_kv_tiles(sg, q_layout(sg), i - tb[b]).count);
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += nthreads) {
+    const int cb = cost[b];
+    int r = 0;
+    for (int b2 = 0; b2 < B; ++b2) {
+      const int c2 = cost[b2];
+      r += (c2 > cb) | ((c2 == cb) & (b2 < b));
+    }
+    ctl.f_order[r] = static_cast<uint8_t>(b);
+  }
+  __syncthreads();
+  for (int pos = tid; pos < B; pos += nthreads) {
+    const int b = ctl.f_order[pos];
+    ctl.f_ubase[pos] = (tb[b + 1] - tb[b]) * p.nhead * p.splits;
+    const int g = b / p.batch_per_group;
+    float sc = p.attn_scale[g];
+    if (sc == 0.f) {   // 0 means 1 / max UIH length of the group
+      const int mu = p.max_uih[g] > 0 ? p.max_uih[g] : gmax[g];
+      sc = mu > 0 ? 1.f / static_cast<float>(mu) : 1.f;
+    }
+    ctl.f_pscale[pos] = sc;
+  }
+  __syncthreads();
+  if (tid < 32) warp_exclusive_scan(ctl.f_ubase, B, tid);
+  __syncthreads();
+  return ctl.f_ubase[B];
+}
+
+// decode_unit for the in-kernel schedule.
+__device__ __forceinline__ UnitView decode_fused_unit(const FwdParams& p, const FwdSmemCtl& ctl, int unit) {
+  const int pos = seg_find(ctl.f_ubase, p.batch, unit);
+  const int b = ctl.f_order[pos];
+  UnitView u;
+  u.g = b / p.batch_per_group;
+  u.s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[u.g], p.loc[u.g], p.mf[u.g], p.causal, p.self_attn,
+                  p.kv_targets);
+  u.L = q_layout(u.s);
+  const int local = unit - ctl.f_ubase[pos];
+  const int per_h = u.L.nq * p.splits;
+  u.h = local / per_h;
+  const int rem = local - u.h * per_h;
+  u.m = u.L.nq - 1 - rem / p.splits;
+  u.sp = rem % p.splits;
+  u.ts = query_tile_kv_tiles(u.s, u.L, u.m);
+  u.tb = q_tile_bounds(u.s, u.L, u.m);
+  split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);
+  u.scale = ctl.f_pscale[pos];
+  return u;
+}
 
 // Bounded wait; on timeout flags the error word and asks every role to stop.
 __device__ __forceinline__ bool wait_or_abort(FwdSmemCtl& ctl, const FwdParams& p, uint64_t* bar,
@@ -238,7 +394,7 @@ template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     hstu_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q8,
-                    const __grid_constant__ FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ FwdParams p) {
   using Cfg = FwdCfg<D, DV, SOFTMAX, RAB>;
   constexpr int KCH = Cfg::KCH;
   constexpr int VCH = Cfg::VCH;
@@ -253,8 +409,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = smem + QB * Cfg::TILE_BYTES;
   uint8_t* sV = sK + KST * Cfg::TILE_BYTES;
-  SoftmaxScratch* sx = reinterpret_cast<SoftmaxScratch*>(smem + Cfg::TILES_BYTES);   // softmax only
-  RabWarp* rabw = reinterpret_cast<RabWarp*>(smem + Cfg::TILES_BYTES + Cfg::SOFTMAX_BYTES);   // bias only
+  uint8_t* sStage = smem + Cfg::TILES_BYTES;   // O staging of the TMA-store epilogue (1024-byte aligned)
+  SoftmaxScratch* sx = reinterpret_cast<SoftmaxScratch*>(smem + Cfg::TILES_BYTES + Cfg::STAGE_BYTES);   // softmax only
+  RabWarp* rabw =
+      reinterpret_cast<RabWarp*>(smem + Cfg::TILES_BYTES + Cfg::STAGE_BYTES + Cfg::SOFTMAX_BYTES);   // bias only
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -293,6 +451,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::prefetch_tensormap(&tm_q);
     ptx::prefetch_tensormap(&tm_k);
     ptx::prefetch_tensormap(&tm_v);
+    if constexpr (Cfg::STAGE_BUFS > 0) ptx::prefetch_tensormap(&tm_o);
   }
   if (warp == 1) {
     ptx::tmem_alloc(&ctl.tmem_base, Cfg::TMEM_COLS);
@@ -302,10 +461,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  // Launched as a programmatic dependent of the scheduler kernel: everything
-  // above overlapped its tail; the work list and header are read only now.
-  ptx::grid_dependency_wait();
-  const int n_units = p.ws_header[kWsUnits];
+  // Launched as a programmatic dependent of the kernel before it on the stream
+  // (the scheduler, or with the in-kernel schedule the header reset): the
+  // work list and the header are read only after it has completed.  With the
+  // in-kernel schedule, every CTA orders the units itself first (reading only
+  // the offsets and targets, which that kernel does not write), in shared
+  // memory no TMA load uses yet; only the dynamic claims wait for the reset.
+  int n_units;
+  if (p.fused) {
+    n_units = fused_schedule(p, ctl, reinterpret_cast<int*>(sK), tid, kFwdThreads);
+    // the first epilogue warp (idle until the first unit's O) reports
+    if (tid == 64 && (ctl.f_err != 0 || blockIdx.x == 0)) {
+      ptx::grid_dependency_wait();
+      if (ctl.f_err != 0) atomicOr(&p.ws_header[kWsError], ctl.f_err);
+      else p.ws_header[kWsUnits] = n_units;   // read by the combine kernel
+    }
+  } else {
+    ptx::grid_dependency_wait();
+    n_units = p.ws_header[kWsUnits];
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -422,33 +596,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == kSchedWarp) {
     // ------------------------------------------------------------ scheduler
-    // Takes kSchedBatch units per atomic from the global queue; lanes
-    // 0..kSchedBatch-1 decode one each (their global reads overlap) and publish
-    // it into its own ring slot, running up to kSchedDepth units ahead.
+    // Takes units from the global queue (lane 0), decodes them and publishes
+    // each into its own ring slot, running up to kSchedDepth units ahead.  With
+    // the in-kernel schedule each CTA's first unit is its own index (no wait
+    // for the header reset, so its loads start at once) and the queue hands out
+    // the units from the grid size on.
     int sched_it = 0;
+    bool first = true, waited = !p.fused;
     while (!ctl.abort_flag) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&p.ws_header[kWsCounter], kSchedBatch);
-      base = __shfl_sync(0xffffffffu, base, 0);
-      bool ok = true, more = true;
-      if (lane < kSchedBatch) {
-        const int id = base + lane;
-        const bool live = id < n_units;
+      bool ok = true, live = false;
+      if (lane == 0) {
+        int id;
+        if (p.fused && first) {
+          id = static_cast<int>(blockIdx.x);
+        } else {
+          if (!waited) {
+            ptx::grid_dependency_wait();
+            waited = true;
+          }
+          id = atomicAdd(&p.ws_header[kWsCounter], 1) + (p.fused ? static_cast<int>(gridDim.x) : 0);
+        }
+        live = id < n_units;
         UnitView u;
-        if (live) u = decode_unit(p, id);
-        const int it = sched_it + lane;
-        const int slot = it % kSchedDepth;
-        ok = wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((it / kSchedDepth) & 1) ^ 1);
+        if (live) u = p.fused ? decode_fused_unit(p, ctl, id) : decode_unit(p, id);
+        const int slot = sched_it % kSchedDepth;
+        ok = wait_or_abort(ctl, p, &ctl.sched_empty[slot], ((sched_it / kSchedDepth) & 1) ^ 1);
         if (ok) {
           if (live) ctl.sched_view[slot] = u;
           ctl.sched_live[slot] = live ? 1 : 0;
           ptx::mbar_arrive(&ctl.sched_full[slot]);
         }
-        more = live;
       }
-      if (!__all_sync(0xffffffffu, ok)) break;
-      if (!__all_sync(0xffffffffu, more)) break;   // the queue is drained: end markers published
-      sched_it += kSchedBatch;
+      first = false;
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      if (!__shfl_sync(0xffffffffu, live ? 1 : 0, 0)) break;   // the queue is drained: end marker published
+      ++sched_it;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -598,9 +780,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------ epilogue warpgroup
     // One query row per thread, all DV output columns: waits for the unit's last
     // P V product, reads O out of TMEM, hands the buffer back, scales and stores.
+    // A warp whose 32 rows are consecutive rows of one sequence stages each
+    // 64-column box of its rows in shared memory (128-byte swizzle) and writes
+    // it with one TMA store; warps holding a ragged tail or the context rows of
+    // the last query tile store their rows with plain 16-byte stores.
     const int quarter = warp & 3;
     const int rloc = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t stage_warp = ptx::smem_u32(sStage) + (warp - 2) * Cfg::STAGE_BUFS * Cfg::STAGE_BOX_BYTES;
+    int st_it = 0;   // boxes this warp has stored with TMA (selects the staging buffer)
     int q_it = 0, sched_it = 0;
     while (!ctl.abort_flag) {
       const int slot = sched_it % kSchedDepth;
@@ -629,6 +817,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tc_fence_after();
       }
       const bool write_part = p.splits > 1;
+      const long long grow0 = __shfl_sync(0xffffffffu, grow, 0);
+      const bool tma_rows = Cfg::STAGE_BUFS > 0 && !write_part &&
+                            __all_sync(0xffffffffu, valid && grow == grow0 + lane);   // warp-uniform
       float mul = u.scale;
       if constexpr (SOFTMAX) mul = l_run > 0.f ? u.scale / l_run : 0.f;
 #pragma unroll 1
@@ -649,19 +840,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // unused lanes store nothing (a branch, not a `continue`: the warp stays
         // converged for the next collective TMEM load)
         if (valid && write_part) {
+          // fp32 partial, already x attn_scale (softmax: not yet / row sum)
           float* dst = p.o_part + ((static_cast<long long>(u.sp) * p.total_q + grow) * p.nhead + u.h) * DV + c * 32;
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+            *reinterpret_cast<float4*>(dst + k) =
+                make_float4(__uint_as_float(o[k]) * u.scale, __uint_as_float(o[k + 1]) * u.scale,
+                            __uint_as_float(o[k + 2]) * u.scale, __uint_as_float(o[k + 3]) * u.scale);
         } else if (valid) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
             pk[k >> 1] = pack2<BF16>(__uint_as_float(o[k]) * mul, __uint_as_float(o[k + 1]) * mul);
-          uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * DV + c * 32;
+          bool staged = false;
+          if constexpr (Cfg::STAGE_BUFS > 0) {
+            if (tma_rows) {
+              // columns [32 c, 32 c + 32) are 16-byte pieces 4 (c & 1) .. 4 (c & 1) + 3 of
+              // the row in box c / 2; piece j of row r sits at r * 128 + ((j ^ (r & 7)) * 16)
+              staged = true;
+              const uint32_t buf = stage_warp + (st_it % Cfg::STAGE_BUFS) * Cfg::STAGE_BOX_BYTES;
+              if ((c & 1) == 0 && st_it >= Cfg::STAGE_BUFS) {   // that buffer's last store has read it
+                if (lane == 0) ptx::bulk_wait_group_read<Cfg::STAGE_BUFS - 1>();
+                __syncwarp();
+              }
 #pragma unroll
-          for (int k = 0; k < 16; k += 4)
-            *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
+              for (int q = 0; q < 4; ++q) {
+                const int j = (c & 1) * 4 + q;
+                ptx::st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                                  pk[4 * q + 2], pk[4 * q + 3]);
+              }
+              if (c & 1) {
+                ptx::fence_proxy_async_smem();   // the generic-proxy writes, before the bulk copy reads them
+                __syncwarp();
+                if (lane == 0) {
+                  ptx::tma_store_2d(&tm_o, buf, u.h * DV + (c >> 1) * 64, static_cast<int>(grow0));
+                  ptx::bulk_commit_group();
+                }
+                ++st_it;
+              }
+            }
+          }
+          if (!staged) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + grow * p.o_stride + u.h * DV + c * 32;
+#pragma unroll
+            for (int k = 0; k < 16; k += 4)
+              *reinterpret_cast<uint4*>(dst + 2 * k) = make_uint4(pk[k], pk[k + 1], pk[k + 2], pk[k + 3]);
+          }
         }
       }
       if (nt > 0) ++q_it;
@@ -808,17 +1032,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             else silu_pack<BF16, true, true, 16>(x, s_tmem + 16 * hh, half_alpha, rm, c0 + 32 * hh);
           }
         } else {
+          if constexpr (RAB && SOFTMAX) {
+            // softmax with the bias: the same runtime loop over the halves,
+            // each half's (alpha s + rab) * log2 e written back over its own
+            // scores, then the 64-column pass below reads them all
+            const RabWarp& rw = rabw[warp - 2 - kEpiWarps];
+            const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t x[32];
+              ptx::tmem_ld32(s_tmem + 32 * hh, x);
+              ptx::tmem_ld_wait(x);
+              // keys past the sequence repeat its last one: every column counts in the ranges
+              rab_apply32<true>(x, scale_log2, rw, p.rab_np, has_time, rrow,
+                                rab_cols(hh ? tsk1 : tsk0, j0 + c0 + 32 * hh + lane, true));
+              ptx::tmem_st32(s_tmem + 32 * hh, x);
+            }
+            ptx::tmem_st_wait();
+          }
           ptx::tmem_ld64(s_tmem, r);
           ptx::tmem_ld_wait(r);
-        }
-        if constexpr (RAB && SOFTMAX) {
-          // r becomes (alpha s + rab) * log2 e
-          const RabWarp& rw = rabw[warp - 2 - kEpiWarps];
-          const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
-          // keys past the sequence repeat its last one: every column counts in the ranges
-          rab_apply32<true>(r, scale_log2, rw, p.rab_np, has_time, rrow, rab_cols(tsk0, j0 + c0 + lane, true));
-          rab_apply32<true>(r + 32, scale_log2, rw, p.rab_np, has_time, rrow,
-                            rab_cols(tsk1, j0 + c0 + 32 + lane, true));
         }
         if constexpr (!SOFTMAX) {
           if constexpr (!RAB) {
@@ -918,6 +1151,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  if constexpr (Cfg::STAGE_BUFS > 0) {
+    // epilogue warps: their TMA stores have read the staging buffers and landed
+    if (warp >= 2 && warp < 2 + kEpiWarps && lane == 0) ptx::bulk_wait_group<0>();
+  }
   if (ctl.abort_flag && tid == 0) {
     // let copies / MMAs already in flight land before the CTA releases its memory
     const uint64_t t0 = ptx::globaltimer_ns();
@@ -938,8 +1175,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // device, launched as a programmatic dependent of the scheduler kernel that
 // precedes it on the stream.
 template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB>
-cudaError_t launch_fwd_inst(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
-                            const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_fwd_inst(const FwdMaps& m, const FwdParams& p, int grid, cudaStream_t stream) {
   constexpr int smem = FwdCfg<D, DV, SOFTMAX, RAB>::SMEM_BYTES;
   static_assert(smem + sizeof(FwdSmemCtl) <= 232448, "shared memory over the 227 KB a CTA may use");
   auto kern = hstu_fwd_kernel<D, DV, BF16, SOFTMAX, RAB>;
@@ -956,18 +1192,17 @@ cudaError_t launch_fwd_inst(const CUtensorMap& q, const CUtensorMap& k, const CU
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, q8, p);
+  return cudaLaunchKernelEx(&cfg, kern, m.q, m.k, m.v, m.q8, m.o, p);
 }
 
 // The four dtype x nonlinearity instantiations of one head-dimension pair.
 template <int D, int DV, bool RAB>
-cudaError_t launch_fwd_dispatch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const CUtensorMap& q8, const FwdParams& p, bool bf16, bool softmax, int grid,
+cudaError_t launch_fwd_dispatch(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
                                 cudaStream_t stream) {
-  if (bf16) return softmax ? launch_fwd_inst<D, DV, true, true, RAB>(q, k, v, q8, p, grid, stream)
-                           : launch_fwd_inst<D, DV, true, false, RAB>(q, k, v, q8, p, grid, stream);
-  return softmax ? launch_fwd_inst<D, DV, false, true, RAB>(q, k, v, q8, p, grid, stream)
-                 : launch_fwd_inst<D, DV, false, false, RAB>(q, k, v, q8, p, grid, stream);
+  if (bf16) return softmax ? launch_fwd_inst<D, DV, true, true, RAB>(m, p, grid, stream)
+                           : launch_fwd_inst<D, DV, true, false, RAB>(m, p, grid, stream);
+  return softmax ? launch_fwd_inst<D, DV, false, true, RAB>(m, p, grid, stream)
+                 : launch_fwd_inst<D, DV, false, false, RAB>(m, p, grid, stream);
 }
 
 }  // namespace hstu

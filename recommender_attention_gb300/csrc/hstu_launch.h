@@ -26,25 +26,27 @@ inline cudaError_t ensure_smem_attr(Kernel kern, int smem, std::atomic<unsigned 
   return e;
 }
 
-// Persistent forward over the scheduler's work units; one CTA per SM.  q8 is
-// the q tensor map with 8-row boxes (query tiles whose rows come in two runs).
-cudaError_t launch_fwd_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
-                           const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
-cudaError_t launch_fwd_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
-                            const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
+// Tensor maps of the forward: q, k, v with 128-row boxes, q with 8-row boxes
+// (query tiles whose rows come in two runs), and o with 32-row boxes (the
+// TMA-store epilogue); every box is 64 columns wide with a 128-byte swizzle.
+struct FwdMaps {
+  CUtensorMap q, k, v, q8, o;
+};
+// Persistent forward over the scheduler's work units; one CTA per SM.
+cudaError_t launch_fwd_d64(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_fwd_d128(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_fwd_d256(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
+                            cudaStream_t stream);
 // hdim_qk 96 with hdim_v 96 or 64
-cudaError_t launch_fwd_d96(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
-                           const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
+cudaError_t launch_fwd_d96(const FwdMaps& m, const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
                            cudaStream_t stream);
 // with a relative attention bias (FwdParams::ts_q / rab_time / rab_pos), hdim_qk == hdim_v
-cudaError_t launch_fwd_rab_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                               const CUtensorMap& q8, const FwdParams& p, bool bf16, bool softmax, int grid,
+cudaError_t launch_fwd_rab_d64(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
                                cudaStream_t stream);
-cudaError_t launch_fwd_rab_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                const CUtensorMap& q8, const FwdParams& p, bool bf16, bool softmax, int grid,
+cudaError_t launch_fwd_rab_d128(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
                                 cudaStream_t stream);
-cudaError_t launch_fwd_d256(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q8,
-                            const FwdParams& p, bool bf16, bool softmax, int grid, cudaStream_t stream);
 // Tensor maps of the backward: 128-row boxes, and 8-row boxes for query tiles
 // whose rows come in two runs.
 struct BwdMaps {
@@ -67,8 +69,12 @@ cudaError_t launch_bwd_rab_d128(const BwdMaps& m, const BwdParams& p, bool bf16,
 cudaError_t launch_bwd_delta(const void* o, long long o_stride, const void* d_o, long long do_stride, float* delta,
                              int total_q, int nhead, int hdim_v, bool bf16, cudaStream_t stream);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+// Zeroes the forward's workspace header (kWsHeaderInts ints) before a forward
+// that schedules itself (FwdParams::fused).
+cudaError_t launch_fwd_reset(int* ws_header, cudaStream_t stream);
+// Split-KV merge (hdim_v 64, 96, 128 or 256), a programmatic dependent of the forward.
+cudaError_t launch_combine(const CombineParams& p, int hdim, bool bf16, bool softmax, int sms, cudaStream_t stream);
 cudaError_t launch_pairs(const PrepParams& p, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, int hdim, bool bf16, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* result, unsigned long long timeout_ns, cudaStream_t stream);
 
 }  // namespace hstu

@@ -1,6 +1,9 @@
-// Scheduler (prep), pair-count and split-KV combine kernels of the HSTU forward.
+// Scheduler (prep), header reset, pair-count, split-KV combine, softmax row-sum and self-test kernels.
 //
-// The scheduler runs as one CTA before the forward kernel, on the same stream:
+// The scheduler runs as one CTA before the forward kernel, on the same stream
+// (for batches above kFusedMaxBatch, for the stats call and for the backward;
+// smaller forwards order their units inside the forward kernel, after a
+// one-block kernel that zeroes the workspace header):
 // it validates the jagged offsets, counts for every query tile the key tiles
 // the functional mask does not fully exclude, orders the sequences longest
 // first (most executed tiles first, so the persistent kernel's dynamic queue
@@ -11,8 +14,8 @@
 // arguments": attn_scale 0 means 1/max_seqlen, the maximum UIH length).
 //
 // The combine kernel merges split-KV partials ("Split-KV" section of the same
-// README): SiLU partials add; softmax partials are merged with their running
-// maxima and row sums, and the LSE is written.
+// README): SiLU partials add; softmax partials are weighted by their running
+// maxima, divided by the merged row sum, and the LSE is written.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -328,71 +331,134 @@ __device__ __forceinline__ uint32_t pack2c(float lo, float hi) {
   }
 }
 
-// One warp per (token row, head); each lane owns D/32 consecutive columns.
-template <int D, bool BF16>
-__global__ void __launch_bounds__(256) hstu_combine_kernel(const __grid_constant__ CombineParams p) {
-  constexpr int E = D / 32;
-  const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+// Groups of R (token row, head) pairs per warp iteration (R = 4; 2 for
+// softmax and D = 256), lanes across the D columns (one float4 each, two for
+// D = 256; coalesced rows), over a grid of three resident blocks per SM that
+// strides through the groups.  Every load of an iteration (the statistics and the
+// partials of two splits at a time) is issued before any is used, and
+// validity is tested after the loads (all addresses stay inside the
+// workspace), so an iteration waits for about one memory round trip per two
+// splits.  Softmax: lane s holds split s's running max and row sum; the merged
+// max, weights and row sum come from warp reductions.  Launched as a
+// programmatic dependent of the forward kernel: it waits for the forward's
+// completion before reading.  Rows outside every sequence and calls whose
+// scheduler found a device error are left untouched.
+constexpr int kCombineBlocksPerSm = 3;
+
+template <int D, bool BF16, bool SOFTMAX>
+__global__ void __launch_bounds__(256, kCombineBlocksPerSm) hstu_combine_kernel(const __grid_constant__ CombineParams p) {
+  constexpr int NV4 = (D / 4 + 31) / 32;
+  constexpr int R = (D > 128 || SOFTMAX) ? 2 : 4;   // pairs per warp iteration
+  constexpr int SU = 2;                // splits per round of loads
+  ptx::grid_dependency_wait();
   const int lane = threadIdx.x & 31;
-  const long long row = wid / p.nhead;
-  const int h = static_cast<int>(wid % p.nhead);
-  if (row >= p.total_q || p.ws_header[kWsUnits] == 0) return;
-  if (row >= p.off_q[p.batch]) return;
-  int lo = 0, hi = p.batch;   // off_q[lo] <= row < off_q[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (p.off_q[mid] <= row) lo = mid; else hi = mid;
-  }
-  const float scale = p.group_scale[lo / p.batch_per_group];
-  float acc[E];
+  const long long npairs = static_cast<long long>(p.total_q) * p.nhead;
+  const int units = p.ws_header[kWsUnits];
+  const int row_lo = p.off_q[0], row_hi = p.off_q[p.batch];
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long g = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); g * R < npairs;
+       g += nwarps) {
+    const long long pair0 = g * R;
+    long long row[R];
+    int hh[R];
+    bool live[R];
 #pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float M = -INFINITY, L = 0.f;
-  if (p.softmax) {
-    for (int sp = 0; sp < p.splits; ++sp)
-      M = fmaxf(M, p.ml_part[((static_cast<long long>(sp) * p.nhead + h) * p.total_q + row) * 2]);
-  }
-  for (int sp = 0; sp < p.splits; ++sp) {
-    float w = 1.f;
-    if (p.softmax) {
-      const float* ml = p.ml_part + ((static_cast<long long>(sp) * p.nhead + h) * p.total_q + row) * 2;
-      w = ml[0] == -INFINITY ? 0.f : exp2f(ml[0] - M);
-      L += w * ml[1];
+    for (int r = 0; r < R; ++r) {
+      live[r] = pair0 + r < npairs;
+      const long long pr = live[r] ? pair0 + r : pair0;
+      row[r] = pr / p.nhead;
+      hh[r] = static_cast<int>(pr % p.nhead);
     }
-    const float* src = p.o_part + ((static_cast<long long>(sp) * p.total_q + row) * p.nhead + h) * D + lane * E;
-    if constexpr (E % 2 == 0) {
+    float wl[R], mul[R], lse[R];
 #pragma unroll
-      for (int e = 0; e < E; e += 2) {
-        const float2 v = *reinterpret_cast<const float2*>(src + e);
-        acc[e] += w * v.x;
-        acc[e + 1] += w * v.y;
+    for (int r = 0; r < R; ++r) {
+      wl[r] = 1.f;
+      mul[r] = 1.f;
+      lse[r] = 0.f;
+    }
+    if constexpr (SOFTMAX) {
+      float m[R], l[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+        if (lane < p.splits) {
+          const float2 ml = *reinterpret_cast<const float2*>(
+              p.ml_part + ((static_cast<long long>(lane) * p.nhead + hh[r]) * p.total_q + row[r]) * 2);
+          m[r] = ml.x;
+          l[r] = ml.y;
+        }
       }
-    } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += w * src[e];
+      for (int r = 0; r < R; ++r) {
+        float M = m[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        wl[r] = m[r] == -INFINITY ? 0.f : exp2f(m[r] - M);
+        float L = wl[r] * l[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        mul[r] = L > 0.f ? 1.f / L : 0.f;
+        lse[r] = L > 0.f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+      }
+    }
+    float4 acc[R][NV4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int k = 0; k < NV4; ++k) acc[r][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < p.splits; s0 += SU) {
+      float4 v[SU][R][NV4];
+#pragma unroll
+      for (int j = 0; j < SU; ++j)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float4* src = reinterpret_cast<const float4*>(
+              p.o_part + ((static_cast<long long>(s0 + j) * p.total_q + row[r]) * p.nhead + hh[r]) * D);
+#pragma unroll
+          for (int k = 0; k < NV4; ++k) {
+            const int c4 = lane + 32 * k;
+            v[j][r][k] = (s0 + j < p.splits && 4 * c4 < D) ? src[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+      for (int j = 0; j < SU; ++j)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float w = SOFTMAX ? __shfl_sync(0xffffffffu, wl[r], (s0 + j) & 31) : 1.f;
+#pragma unroll
+          for (int k = 0; k < NV4; ++k) {
+            acc[r][k].x = fmaf(w, v[j][r][k].x, acc[r][k].x);
+            acc[r][k].y = fmaf(w, v[j][r][k].y, acc[r][k].y);
+            acc[r][k].z = fmaf(w, v[j][r][k].z, acc[r][k].z);
+            acc[r][k].w = fmaf(w, v[j][r][k].w, acc[r][k].w);
+          }
+        }
+    }
+    if (units == 0) continue;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (!live[r] || row[r] < row_lo || row[r] >= row_hi) continue;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + row[r] * p.o_stride + static_cast<long long>(hh[r]) * D;
+#pragma unroll
+      for (int k = 0; k < NV4; ++k) {
+        const int c4 = lane + 32 * k;
+        if (4 * c4 < D)
+          *reinterpret_cast<uint2*>(dst + 4 * c4) =
+              make_uint2(pack2c<BF16>(acc[r][k].x * mul[r], acc[r][k].y * mul[r]),
+                         pack2c<BF16>(acc[r][k].z * mul[r], acc[r][k].w * mul[r]));
+      }
+      if (SOFTMAX && lane == 0 && p.lse != nullptr) p.lse[static_cast<long long>(hh[r]) * p.total_q + row[r]] = lse[r];
     }
   }
-  float mul = scale;
-  if (p.softmax) mul = L > 0.f ? scale / L : 0.f;
-  uint16_t* dst = reinterpret_cast<uint16_t*>(p.o) + row * p.o_stride + h * D + lane * E;
-  if constexpr (E % 2 == 0) {
-    uint32_t pk[E / 2];
-#pragma unroll
-    for (int e = 0; e < E; e += 2) pk[e / 2] = pack2c<BF16>(acc[e] * mul, acc[e + 1] * mul);
-    if constexpr (E == 2) {
-      *reinterpret_cast<uint32_t*>(dst) = pk[0];
-    } else if constexpr (E == 4) {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
-    } else {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-  } else {   // hdim_v 96: three elements per lane, stored one by one
-#pragma unroll
-    for (int e = 0; e < E; ++e) dst[e] = static_cast<uint16_t>(pack2c<BF16>(acc[e] * mul, 0.f) & 0xFFFFu);
-  }
-  if (p.softmax && p.lse != nullptr && lane == 0)
-    p.lse[static_cast<long long>(h) * p.total_q + row] =
-        L > 0.f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+}
+
+// Zeroes the forward's workspace header (work counter, error word, unit count)
+// before a forward that schedules itself; the forward kernel, its programmatic
+// dependent, starts as soon as this kernel has begun.
+__global__ void __launch_bounds__(kWsHeaderInts) hstu_fwd_reset_kernel(int* ws_header) {
+  ptx::grid_launch_dependents();
+  ws_header[threadIdx.x] = 0;
 }
 
 // One thread waits on a barrier that nothing arrives on; the bounded wait must
@@ -480,6 +546,32 @@ cudaError_t launch_wait_selftest(int* result, unsigned long long timeout_ns, cud
   return cudaGetLastError();
 }
 
+template <int D, bool BF16, bool SOFTMAX>
+cudaError_t launch_combine_t(const CombineParams& p, unsigned grid, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, hstu_combine_kernel<D, BF16, SOFTMAX>, p);
+}
+
+template <int D>
+cudaError_t launch_combine_d(const CombineParams& p, bool bf16, bool softmax, unsigned grid, cudaStream_t stream) {
+  if (bf16) return softmax ? launch_combine_t<D, true, true>(p, grid, stream)
+                           : launch_combine_t<D, true, false>(p, grid, stream);
+  return softmax ? launch_combine_t<D, false, true>(p, grid, stream) : launch_combine_t<D, false, false>(p, grid, stream);
+}
+
+cudaError_t launch_fwd_reset(int* ws_header, cudaStream_t stream) {
+  hstu_fwd_reset_kernel<<<1, kWsHeaderInts, 0, stream>>>(ws_header);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
   const size_t dsmem = p.batch <= kPrepSmemBatch ? (5 * static_cast<size_t>(p.batch) + 3) * sizeof(int) : 0;
   hstu_prep_kernel<<<1, kPrepThreads, dsmem, stream>>>(p);
@@ -491,22 +583,21 @@ cudaError_t launch_pairs(const PrepParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const CombineParams& p, int hdim, bool bf16, cudaStream_t stream) {
-  const long long warps = static_cast<long long>(p.total_q) * p.nhead;
-  const unsigned grid = static_cast<unsigned>((warps + 7) / 8);
+cudaError_t launch_combine(const CombineParams& p, int hdim, bool bf16, bool softmax, int sms, cudaStream_t stream) {
+  const int per_warp = (hdim > 128 || softmax) ? 2 : 4;
+  const long long warps = (static_cast<long long>(p.total_q) * p.nhead + per_warp - 1) / per_warp;
+  long long blocks = (warps + 7) / 8;
+  const long long resident = static_cast<long long>(kCombineBlocksPerSm) * (sms > 0 ? sms : 148);
+  if (blocks > resident) blocks = resident;
+  const unsigned grid = static_cast<unsigned>(blocks);
   if (grid == 0) return cudaSuccess;
-#define HSTU_COMBINE(DD)                                                            \
-  if (hdim == DD) {                                                                 \
-    if (bf16) hstu_combine_kernel<DD, true><<<grid, 256, 0, stream>>>(p);           \
-    else hstu_combine_kernel<DD, false><<<grid, 256, 0, stream>>>(p);               \
-    return cudaGetLastError();                                                      \
+  switch (hdim) {
+    case 64: return launch_combine_d<64>(p, bf16, softmax, grid, stream);
+    case 96: return launch_combine_d<96>(p, bf16, softmax, grid, stream);
+    case 128: return launch_combine_d<128>(p, bf16, softmax, grid, stream);
+    case 256: return launch_combine_d<256>(p, bf16, softmax, grid, stream);
+    default: return cudaErrorInvalidValue;
   }
-  HSTU_COMBINE(64)
-  HSTU_COMBINE(96)
-  HSTU_COMBINE(128)
-  HSTU_COMBINE(256)
-#undef HSTU_COMBINE
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace hstu

@@ -1,5 +1,5 @@
 // Inline-PTX wrappers for the sm_103a primitives the HSTU forward uses:
-// mbarriers (with time-bounded waits), TMA tiled loads, tcgen05 MMA / TMEM
+// mbarriers (with time-bounded waits), TMA tiled loads and stores, tcgen05 MMA / TMEM
 // load-store / allocation, and the shared-memory + instruction descriptors.
 //
 // Encodings follow the public PTX ISA (tcgen05 "Matrix descriptors" and
@@ -133,6 +133,29 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* map, uin
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+
+// 2-D tiled bulk-tensor store shared -> global of one box of the tensor map,
+// tracked by this thread's bulk async-groups (commit, then wait).
+// smem_src is a shared-space address (smem_u32).
+__device__ __forceinline__ void tma_store_2d(const void* map, uint32_t smem_src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(smem_src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until at most N of this thread's committed bulk groups are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Prefetch of a 2-D tile (same box as the tensor map) into L2; no completion.

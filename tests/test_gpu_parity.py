@@ -68,7 +68,7 @@ def test_softmax_rescale_in_some_rows_of_a_warp():
 @pytest.mark.parametrize("splits", [0, 5, 16])
 def test_splitkv_runs_of_empty_split_units(softmax, splits):
     """Local-window groups give query tiles of 2-3 key tiles: with 5 or 16
-    splits (and the automatic choice on 8 sequences, 5) most of their split
+    splits (and the automatic choice on 8 sequences) most of their split
     units are empty, several in a row, between non-empty ones."""
     w = W.group_cross_splitkv(softmax=softmax, batch=8)
     check_full(w, num_splits=splits)
