@@ -542,6 +542,19 @@ def run_cuda(args):
     q, k, v = w.tensors()
     call, dev = device_call(w, q, k, v, device)
     st = call.stats(stream)
+    if args.headline_only:
+        # the headline call alone, warm-up then timed launches (for profiling
+        # its kernels); not the bench line
+        for _ in range(args.warmup + args.steps):
+            call.launch(stream)
+        call.check(stream)
+        if rank == 0:
+            print(json.dumps({"headline_only": True, "launches": args.warmup + args.steps,
+                              "allowed_pairs": st["allowed_pairs"]}), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     flops_step = 2.0 * (w.hdim_qk + w.hdim_v) * st["allowed_pairs"]
     exec_flops = 2.0 * 128 * 128 * (w.hdim_qk + w.hdim_v) * st["executed_tiles"]
 
@@ -820,6 +833,8 @@ def main(argv=None):
     ap.add_argument("--scope-only", default=None, metavar="NAMES",
                     help="run only these scope workloads (comma-separated names of the 'configs' lines; "
                          "empty: all) and print their lines alone; for profiling")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="launch only the headline call (warm-up + steps times) and print a short line; for profiling")
     ap.add_argument("--sustained-seconds", type=float, default=2.0,
                     help="seconds of back-to-back headline steps for the 'sustained' figure (0: skip)")
     args = ap.parse_args(argv)
