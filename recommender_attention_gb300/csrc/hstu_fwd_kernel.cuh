@@ -1011,6 +1011,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ptx::tc_fence_after();
         const uint32_t s_tmem = tmem + lane_base + (si & 1) * 128 + c0;
         uint32_t r[64];
+        float rab_mx = -INFINITY;   // softmax with the bias: the row max of the biased scores
         if constexpr (RAB && !SOFTMAX) {
           // SiLU with the bias: a runtime loop over the two 32-column halves,
           // so the bias code is inlined once per tile.  Each half is loaded,
@@ -1034,8 +1035,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         } else {
           if constexpr (RAB && SOFTMAX) {
             // softmax with the bias: the same runtime loop over the halves,
-            // each half's (alpha s + rab) * log2 e written back over its own
-            // scores, then the 64-column pass below reads them all
+            // each half's (alpha s + rab) * log2 e, masked scores -inf, written
+            // back over its own scores and folded into the row max; the
+            // exponentials below take the halves again (32 score registers live
+            // at a time instead of 64)
             const RabWarp& rw = rabw[warp - 2 - kEpiWarps];
             const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
 #pragma unroll 1
@@ -1046,12 +1049,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               // keys past the sequence repeat its last one: every column counts in the ranges
               rab_apply32<true>(x, scale_log2, rw, p.rab_np, has_time, rrow,
                                 rab_cols(hh ? tsk1 : tsk0, j0 + c0 + 32 * hh + lane, true));
+              if (!full) {
+                const uint32_t mb = rm.bits32(c0 + 32 * hh);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                  const uint32_t keep = static_cast<uint32_t>(static_cast<int32_t>(mb << (31 - k)) >> 31);
+                  x[k] = (x[k] & keep) | (0xFF800000u & ~keep);   // masked scores become -inf
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 32; ++k) rab_mx = fmaxf(rab_mx, __uint_as_float(x[k]));
               ptx::tmem_st32(s_tmem + 32 * hh, x);
             }
             ptx::tmem_st_wait();
+          } else {
+            ptx::tmem_ld64(s_tmem, r);
+            ptx::tmem_ld_wait(r);
           }
-          ptx::tmem_ld64(s_tmem, r);
-          ptx::tmem_ld_wait(r);
         }
         if constexpr (!SOFTMAX) {
           if constexpr (!RAB) {
@@ -1060,8 +1074,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             else silu_pack<BF16, true>(r, s_tmem, half_alpha, rm, c0);
           }
         } else {
-          float mx = -INFINITY;
-          if (full) {
+          float mx = RAB ? rab_mx : -INFINITY;
+          if (RAB) {
+            // (max and mask already taken in the bias pass)
+          } else if (full) {
 #pragma unroll
             for (int k = 0; k < 64; ++k) mx = fmaxf(mx, __uint_as_float(r[k]));
           } else {
@@ -1113,21 +1129,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (grow) m_run = mx;
           const float nm = m_run == -INFINITY ? 0.f : -m_run;
           float lsum0 = 0.f, lsum1 = 0.f;
-          uint32_t pk[32];
-          // stage by stage so the exponentials of the 64 scores overlap
+          if constexpr (RAB) {
+            // the halves again: half 0's P words over its own first 16
+            // columns, half 1's over half 0's last 16 (both already read)
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t x[32], pk[16];
+              ptx::tmem_ld32(s_tmem + 32 * hh, x);
+              ptx::tmem_ld_wait(x);
 #pragma unroll
-          for (int k = 0; k < 64; ++k)   // masked scores are -inf and give 0
-            r[k] = __float_as_uint(RAB ? __uint_as_float(r[k]) + nm : fmaf(__uint_as_float(r[k]), scale_log2, nm));
+              for (int k = 0; k < 32; ++k)   // masked scores are -inf and give 0
+                x[k] = __float_as_uint(ex2_approx(__uint_as_float(x[k]) + nm));
 #pragma unroll
-          for (int k = 0; k < 64; ++k) r[k] = __float_as_uint(ex2_approx(__uint_as_float(r[k])));
+              for (int k = 0; k < 16; ++k) {
+                const float e0 = __uint_as_float(x[2 * k]), e1 = __uint_as_float(x[2 * k + 1]);
+                lsum0 += e0;
+                lsum1 += e1;
+                pk[k] = pack2<BF16>(e0, e1);
+              }
+              ptx::tmem_st16(s_tmem + 16 * hh, pk);
+            }
+          } else {
+            uint32_t pk[32];
+            // stage by stage so the exponentials of the 64 scores overlap
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float e0 = __uint_as_float(r[2 * k]), e1 = __uint_as_float(r[2 * k + 1]);
-            lsum0 += e0;
-            lsum1 += e1;
-            pk[k] = pack2<BF16>(e0, e1);
+            for (int k = 0; k < 64; ++k)   // masked scores are -inf and give 0
+              r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), scale_log2, nm));
+#pragma unroll
+            for (int k = 0; k < 64; ++k) r[k] = __float_as_uint(ex2_approx(__uint_as_float(r[k])));
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const float e0 = __uint_as_float(r[2 * k]), e1 = __uint_as_float(r[2 * k + 1]);
+              lsum0 += e0;
+              lsum1 += e1;
+              pk[k] = pack2<BF16>(e0, e1);
+            }
+            ptx::tmem_st32(s_tmem, pk);
           }
-          ptx::tmem_st32(s_tmem, pk);
           l_run += lsum0 + lsum1;
         }
         ptx::tmem_st_wait();
