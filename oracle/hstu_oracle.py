@@ -217,19 +217,33 @@ def query_key_positions(p: "SeqMaskParams", rows: np.ndarray) -> np.ndarray:
     return np.where(rows < p.context, rows, rows + (p.uih_kv - p.uih_q))
 
 
+def rab_indices(p: "SeqMaskParams", rows, ts_q, ts_kv, n_pos: int):
+    """For the given query rows of one sequence: the time-gap bucket of every
+    (row, key) pair (None when ts_q is None) and the clamped distance
+    min(|pos_i - j|, n_pos - 1) (None when n_pos is 0)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    bucket = dist = None
+    if ts_q is not None:
+        gap = np.abs(np.asarray(ts_q, dtype=np.float64)[rows][:, None] -
+                     np.asarray(ts_kv, dtype=np.float64)[None, :])
+        bucket = time_gap_bucket(gap)
+    if n_pos > 0:
+        d = np.abs(query_key_positions(p, rows)[:, None] - np.arange(p.L_kv)[None, :])
+        dist = np.minimum(d, n_pos - 1)
+    return bucket, dist
+
+
 def rab_rows(p: "SeqMaskParams", rows, h: int, ts_q, ts_kv, rab_time, rab_pos) -> np.ndarray:
     """rab[i, j] for the given query rows of one sequence and head; ts_q / ts_kv
     are the sequence's timestamps (None: no temporal term)."""
     rows = np.asarray(rows, dtype=np.int64)
     bias = np.zeros((rows.shape[0], p.L_kv), dtype=np.float64)
-    if rab_time is not None and ts_q is not None:
-        gap = np.abs(np.asarray(ts_q, dtype=np.float64)[rows][:, None] -
-                     np.asarray(ts_kv, dtype=np.float64)[None, :])
-        bias += np.asarray(rab_time, dtype=np.float64)[h][time_gap_bucket(gap)]
-    if rab_pos is not None:
-        table = np.asarray(rab_pos, dtype=np.float64)[h]
-        d = np.abs(query_key_positions(p, rows)[:, None] - np.arange(p.L_kv)[None, :])
-        bias += table[np.minimum(d, table.shape[0] - 1)]
+    n_pos = 0 if rab_pos is None else np.asarray(rab_pos).shape[1]
+    bucket, dist = rab_indices(p, rows, ts_q if rab_time is not None else None, ts_kv, n_pos)
+    if bucket is not None:
+        bias += np.asarray(rab_time, dtype=np.float64)[h][bucket]
+    if dist is not None:
+        bias += np.asarray(rab_pos, dtype=np.float64)[h][dist]
     return bias
 
 
@@ -447,7 +461,8 @@ def _head_backward(q, k, v, g, allowed, alpha, attn_scale, softmax, bias=None):
     softmax: o = c * p v,   p = M . exp(s - lse) (row-normalised over allowed keys)
              dv = c p^T g,  dp = c g v^T,  ds = p . (dp - rowsum(p . dp))
     both:    dq = alpha ds k,  dk = alpha ds^T q.
-    A relative attention bias enters s, and through it every derivative."""
+    A relative attention bias enters s, and through it every derivative; ds
+    is also its gradient (s = alpha q k^T + rab).  Returns (dq, dk, dv, ds)."""
     s = alpha * (q @ k.T)
     if bias is not None:
         s = s + bias
@@ -467,13 +482,18 @@ def _head_backward(q, k, v, g, allowed, alpha, attn_scale, softmax, bias=None):
         dv = attn_scale * (p.T @ g)
         dp = attn_scale * (g @ v.T)
         ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
-    return alpha * (ds @ k), alpha * (ds.T @ q), dv
+    return alpha * (ds @ k), alpha * (ds.T @ q), dv, ds
 
 
 def hstu_attention_backward(q, k, v, d_o, seq_offsets_q, seq_offsets_kv, num_targets,
-                            params: HstuParams):
+                            params: HstuParams, rab_grads: bool = False):
     """Gradients (dq, dk, dv) of the full forward for the output gradient d_o
-    [total_q, H, Dv], in float64.  Rows outside every sequence get zero."""
+    [total_q, H, Dv], in float64.  Rows outside every sequence get zero.
+
+    rab_grads: also return the gradients of the relative attention bias tables,
+    (dq, dk, dv, d_rab_time [H, 11] or None, d_rab_pos [H, P] or None): a
+    table entry's gradient is the sum of ds over the (row, key) pairs of every
+    sequence that read it (masked pairs have ds = 0)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -487,17 +507,33 @@ def hstu_attention_backward(q, k, v, d_o, seq_offsets_q, seq_offsets_kv, num_tar
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
+    use_time = params.rab_time is not None and params.timestamps_q is not None
+    n_pos = 0 if params.rab_pos is None else np.asarray(params.rab_pos).shape[1]
+    d_rab_time = np.zeros((H, len(TIME_BUCKET_EDGES))) if rab_grads and use_time else None
+    d_rab_pos = np.zeros((H, n_pos)) if rab_grads and n_pos > 0 else None
     for b in range(batch):
         g_, sp = _seq_params(params, b, batch, off_q, off_kv, num_targets)
         allowed = dense_mask(sp)
         q0 = off_q[b]
         kv0 = off_kv[b] if off_kv is not None else q0
+        if rab_grads and params.has_rab:
+            ts_q = ts_kv = None
+            if use_time:
+                ts_q = np.asarray(params.timestamps_q)[q0:q0 + sp.L_q]
+                ts_kv = np.asarray(params.timestamps_kv if sp.cross else params.timestamps_q)[kv0:kv0 + sp.L_kv]
+            bucket, dist = rab_indices(sp, np.arange(sp.L_q), ts_q, ts_kv, n_pos)
         for h in range(H):
             bias = _seq_bias(params, sp, q0, kv0, h, np.arange(sp.L_q))
-            a, bk, c = _head_backward(q[q0:q0 + sp.L_q, h], k[kv0:kv0 + sp.L_kv, h],
-                                      v[kv0:kv0 + sp.L_kv, h], d_o[q0:q0 + sp.L_q, h], allowed,
-                                      alpha, scales[g_], params.softmax, bias)
+            a, bk, c, ds = _head_backward(q[q0:q0 + sp.L_q, h], k[kv0:kv0 + sp.L_kv, h],
+                                          v[kv0:kv0 + sp.L_kv, h], d_o[q0:q0 + sp.L_q, h], allowed,
+                                          alpha, scales[g_], params.softmax, bias)
             dq[q0:q0 + sp.L_q, h] += a
             dk[kv0:kv0 + sp.L_kv, h] += bk
             dv[kv0:kv0 + sp.L_kv, h] += c
+            if d_rab_time is not None:
+                d_rab_time[h] += np.bincount(bucket.ravel(), weights=ds.ravel(), minlength=d_rab_time.shape[1])
+            if d_rab_pos is not None:
+                d_rab_pos[h] += np.bincount(dist.ravel(), weights=ds.ravel(), minlength=n_pos)
+    if rab_grads:
+        return dq, dk, dv, d_rab_time, d_rab_pos
     return dq, dk, dv

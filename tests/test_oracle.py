@@ -10,6 +10,8 @@ import itertools
 import math
 import os
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -538,6 +540,63 @@ def test_backward_with_rab_matches_finite_differences():
                 p.rab_time = rng.standard_normal((q.shape[1], 11))
                 p.rab_pos = rng.standard_normal((q.shape[1], 5))
                 _fd_check(q, k, v, g, off_q, off_kv, t, p, rng)
+
+
+def _rab_case(rng, softmax, cross, kvt):
+    q, k, v, g, off_q, off_kv, t, p = _fd_case(rng, softmax, cross, kvt)
+    # gaps up to ~2e6 s reach most of the time buckets
+    p.timestamps_q = np.sort(rng.integers(0, 2 * 10 ** 6, size=q.shape[0]))
+    p.timestamps_kv = np.sort(rng.integers(0, 2 * 10 ** 6, size=k.shape[0])) if cross else None
+    p.rab_time = rng.standard_normal((q.shape[1], 11))
+    p.rab_pos = rng.standard_normal((q.shape[1], 7))
+    return q, k, v, g, off_q, off_kv, t, p
+
+
+def test_rab_table_gradients_match_finite_differences():
+    """d_rab_time and d_rab_pos of the backward are the gradients of the
+    (separately pinned) forward's <o, g> with respect to the two bias tables:
+    central differences along random directions in each table, over random
+    masks, self- and cross-attention, SiLU and softmax."""
+    rng = np.random.default_rng(13)
+    eps = 1e-6
+    for softmax in (False, True):
+        for cross, kvt in ((False, False), (True, True)):
+            for _ in range(3):
+                q, k, v, g, off_q, off_kv, t, p = _rab_case(rng, softmax, cross, kvt)
+                _, _, _, d_time, d_pos = orc.hstu_attention_backward(q, k, v, g, off_q, off_kv, t, p,
+                                                                     rab_grads=True)
+
+                def loss(rt, rp):
+                    p2 = dataclasses.replace(p, rab_time=rt, rab_pos=rp)
+                    o, _ = hstu_attention_forward(q, k, v, off_q, off_kv, t, p2)
+                    return float((o * g).sum())
+
+                for grad, which in ((d_time, 0), (d_pos, 1)):
+                    for _ in range(3):
+                        d = rng.standard_normal(grad.shape)
+                        tabs_p, tabs_m = [p.rab_time, p.rab_pos], [p.rab_time, p.rab_pos]
+                        tabs_p[which] = tabs_p[which] + eps * d
+                        tabs_m[which] = tabs_m[which] - eps * d
+                        fd = (loss(*tabs_p) - loss(*tabs_m)) / (2 * eps)
+                        an = float((grad * d).sum())
+                        assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (softmax, cross, which, fd, an)
+
+
+def test_rab_table_gradient_sums():
+    """Every allowed (row, key) pair reads one entry of each table, so the two
+    tables' gradients have the same sum per head; in softmax mode a row's
+    probabilities do not change when all its scores shift together, so that
+    sum is zero."""
+    rng = np.random.default_rng(14)
+    for softmax in (False, True):
+        for cross, kvt in ((False, False), (True, False), (True, True)):
+            q, k, v, g, off_q, off_kv, t, p = _rab_case(rng, softmax, cross, kvt)
+            _, _, _, d_time, d_pos = orc.hstu_attention_backward(q, k, v, g, off_q, off_kv, t, p, rab_grads=True)
+            np.testing.assert_allclose(d_time.sum(axis=1), d_pos.sum(axis=1), rtol=1e-9, atol=1e-9)
+            if softmax:
+                np.testing.assert_allclose(d_time.sum(axis=1), 0.0, atol=1e-9)
+            else:
+                assert np.abs(d_time.sum(axis=1)).max() > 1e-3
 
 
 def test_backward_silu_grad_closed_form():
