@@ -393,14 +393,16 @@ def rab_lines(rank, device, stream, steps: int, warmup: int, world: int, peak: f
 
 def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, peak: float, cpu: bool):
     """The backward over the same large jagged workload (hdim 128; SiLU, and
-    softmax fed the forward's own o and lse): one step = one hstu_attn_bwd call
+    softmax fed the forward's own o and lse; SiLU with the relative attention
+    bias, without and with the gradients of its tables): one step = one hstu_attn_bwd call
     (scheduler [+ row sums] + dQ kernel + dK/dV kernel), inputs and dO resident
     (larger than L2).  Useful FLOPs per allowed pair: 2 (3 hdim_qk + 2 hdim_v),
     the five products (S, dP, dV, dK, dQ) counted once; the two kernels
     recompute S and dP, so the executed count is 2 (5 hdim_qk + 4 hdim_v)."""
     from recommender_attention_gb300.hstu import HstuBwdCall
     out = {}
-    for softmax, rab in ((False, False), (True, False), (False, True)):
+    for softmax, rab, rab_grads in ((False, False, False), (True, False, False), (False, True, False),
+                                    (False, True, True)):
         w = rank_workload(rank, 128).with_(softmax=softmax, rab_pos_buckets=128 if rab else 0)
         q, k, v = w.tensors()
         call, (dq, dk, dv, off_q, tg) = device_call(w, q, k, v, device)
@@ -417,7 +419,7 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
                          context_len=list(w.context_len), minfull_len=list(w.minfull_len),
                          max_uih_len=list(w.max_uih_len), num_groups=w.num_groups, softmax=w.softmax,
                          max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()),
-                         **bias_kw)
+                         rab_grads=rab_grads, **bias_kw)
         for _ in range(warmup):
             bw.launch(stream)
         bw.check(stream)
@@ -439,7 +441,7 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
         tot = reduce_sum(useful, world, device)
         tf = tot / (ms * 1e-3) / 1e12
         per_gpu = useful / (ms * 1e-3) / 1e12
-        out[("softmax" if softmax else "silu") + ("_rab" if rab else "")] = {
+        out[("softmax" if softmax else "silu") + ("_rab" if rab else "") + ("_grads" if rab_grads else "")] = {
             "value": tf, "unit": "TFLOP/s", "ms_per_step": ms, "pct_of_bf16_peak": 100.0 * tf / world / peak,
             "executed_tflops": reduce_sum(executed, world, device) / (ms * 1e-3) / 1e12,
             "launches_per_step": 3 + (1 if softmax else 0),
@@ -447,7 +449,7 @@ def backward_lines(rank, device, stream, steps: int, warmup: int, world: int, pe
                          "frac": per_gpu / peak, "traffic": None,
                          "kernel": "dQ + dK/dV kernels (whole backward step, useful FLOPs)"},
             "cpu_baseline": (cpu_baseline_backward(w, q, k, v, w.grad_output(), 4.0, bias)
-                             if cpu and rank == 0 else None)}
+                             if cpu and rank == 0 and not rab_grads else None)}
         del bw, call, dq, dk, dv, d_o, q, k, v
         torch.cuda.empty_cache()
     return out

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define HSTU_ABI_VERSION 4
+#define HSTU_ABI_VERSION 5
 #define HSTU_MAX_GROUPS 256
 #define HSTU_MAX_SPLITS 16
 #define HSTU_RAB_TIME_BUCKETS 11
@@ -226,6 +226,18 @@ typedef struct hstu_bwd_args {
   /* Elements between consecutive tokens; 0 = packed (nhead * hdim).  Row
    * strides * 2 bytes must be multiples of 16. */
   int64_t do_row_stride, dq_row_stride, dk_row_stride, dv_row_stride;
+  /* Gradients of the relative attention bias tables ("From transformer
+   * parallelism to HSTU" section 3.5: the bias is added to the scaled score,
+   * so an entry's gradient is the sum of ds over the (row, key) pairs, of every
+   * sequence, that read it).  Optional: NULL = not computed.
+   *   d_rab_time [dev] [H, HSTU_RAB_TIME_BUCKETS] fp32, needs fwd.rab_time and
+   *              fwd.timestamps_q;
+   *   d_rab_pos  [dev] [H, rab_pos_buckets] fp32, needs fwd.rab_pos.
+   * Written (overwritten) by the call; 4-byte aligned.  The sums are
+   * accumulated with floating-point atomics, so their last bits depend on
+   * the order the kernels run in. */
+  float* d_rab_time;
+  float* d_rab_pos;
 } hstu_bwd_args;
 
 /* sizeof(hstu_bwd_args) as compiled into the library (binding layout check). */
@@ -248,7 +260,8 @@ hstu_status hstu_attn_bwd_workspace_size(const hstu_bwd_args* args, size_t* byte
  * Head dimensions: hdim_qk == hdim_v in {64, 96, 128}, or 96 with hdim_v 64
  * (others HSTU_ERR_UNSUPPORTED); with a bias, 64 or 128 as in the forward.
  * With a relative attention bias in fwd, s includes it and every gradient
- * flows through it (the bias tables themselves get no gradient here).
+ * flows through it; d_rab_time / d_rab_pos (when set) receive the tables'
+ * gradients.
  * Launches on `stream` the scheduler, in softmax mode a row-sum kernel, then
  * one persistent tcgen05 kernel per query tile (dq) and one per key tile (dk,
  * dv); returns without synchronising.  Every row of every sequence gets its

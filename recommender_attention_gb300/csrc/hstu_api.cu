@@ -517,6 +517,12 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
     return HSTU_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(f.rab_time) | reinterpret_cast<uintptr_t>(f.rab_pos)) & 3)
     return HSTU_ERR_INVALID_ARG;
+  // gradients of the bias tables: only of a table the call uses (the time table
+  // needs its timestamps), 4-byte aligned
+  if (a->d_rab_time != nullptr && (f.rab_time == nullptr || f.timestamps_q == nullptr)) return HSTU_ERR_INVALID_ARG;
+  if (a->d_rab_pos != nullptr && f.rab_pos == nullptr) return HSTU_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->d_rab_time) | reinterpret_cast<uintptr_t>(a->d_rab_pos)) & 3)
+    return HSTU_ERR_INVALID_ARG;
   if (f.workspace == nullptr || (reinterpret_cast<uintptr_t>(f.workspace) & 255)) return HSTU_ERR_WORKSPACE;
   const int sms = sm_count_current();
   if (sms <= 0) return HSTU_ERR_CUDA;
@@ -590,6 +596,15 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
     bw.rab_time = f.rab_time;
     bw.rab_pos = f.rab_pos;
     bw.rab_np = f.rab_pos != nullptr ? f.rab_pos_buckets : 1;
+    bw.d_rab_time = a->d_rab_time;
+    bw.d_rab_pos = a->d_rab_pos;
+    // the dQ kernel sums into them
+    if (a->d_rab_time != nullptr &&
+        cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * f.nhead * HSTU_RAB_TIME_BUCKETS, stream) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+    if (a->d_rab_pos != nullptr &&
+        cudaMemsetAsync(a->d_rab_pos, 0, sizeof(float) * f.nhead * f.rab_pos_buckets, stream) != cudaSuccess)
+      return HSTU_ERR_CUDA;
   }
   fill_group_params(&f, bw.ctx, bw.loc, bw.mf);
   const int mu = bp.fwd.max_units, mk = bp.max_kv_units;

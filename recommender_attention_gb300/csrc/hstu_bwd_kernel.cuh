@@ -53,7 +53,9 @@ struct BwdCfg {
   static constexpr int TV = VCH * CHUNK;        // a V or dO tile
   static constexpr int STAGES = 2;
   static constexpr int RAB_OFFSET = (TQ + TV) * (1 + STAGES);   // relative attention bias tables, per warp
-  static constexpr int SMEM_BYTES = RAB_OFFSET + (RAB ? 8 * static_cast<int>(sizeof(RabWarp)) : 0) + 1024;
+  // then, per elementwise warp, the gradients of the bias tables over a unit (dQ kernel)
+  static constexpr int RAB_GRAD_OFFSET = RAB_OFFSET + (RAB ? 8 * static_cast<int>(sizeof(RabWarp)) : 0);
+  static constexpr int SMEM_BYTES = RAB_GRAD_OFFSET + (RAB ? 8 * static_cast<int>(sizeof(RabGradWarp)) : 0) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t ACC = 256;          // first accumulator column
   static_assert(D % 32 == 0 && DV % 32 == 0 && ACC + D + DV <= TMEM_COLS, "backward head dimensions");
@@ -228,10 +230,11 @@ __device__ __forceinline__ void mma_half_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 // pa receives SiLU(x) (when WANT_A), pr receives dp * SiLU'(x), each rounded
 // once to the storage type; pairs whose bit in `allow` is clear give 0
 // (MASKED).  PRESCALED: sv already holds h (with a relative attention bias,
-// alpha s / 2 + rab / 2).
+// alpha s / 2 + rab / 2).  ds_f32 (optional) receives dp * SiLU'(x) in fp32.
 template <bool BF16, bool WANT_A, bool MASKED, bool PRESCALED = false>
 __device__ __forceinline__ void silu_bwd_f32(const uint32_t (&sv)[32], const uint32_t (&dv)[32], float half_alpha,
-                                             uint32_t allow, uint32_t (&pa)[16], uint32_t (&pr)[16]) {
+                                             uint32_t allow, uint32_t (&pa)[16], uint32_t (&pr)[16],
+                                             float* ds_f32 = nullptr) {
   const uint64_t ha = ptx::f32x2(half_alpha, half_alpha);
   const uint64_t half = ptx::f32x2(0.5f, 0.5f), neg_half = ptx::f32x2(-0.5f, -0.5f);
 #pragma unroll
@@ -248,7 +251,14 @@ __device__ __forceinline__ void silu_bwd_f32(const uint32_t (&sv)[32], const uin
     const uint64_t g = ptx::f32x2(__uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1]));
     uint32_t a16 = 0;
     if constexpr (WANT_A) a16 = ptx::cvt_pack16<BF16>(a);
-    uint32_t r16 = ptx::cvt_pack16<BF16>(ptx::mul_f32x2(g, d));
+    const uint64_t r32 = ptx::mul_f32x2(g, d);
+    uint32_t r16 = ptx::cvt_pack16<BF16>(r32);
+    if (ds_f32 != nullptr) {   // the fp32 values too (masked: 0)
+      float r0, r1;
+      ptx::f32x2_split(r32, r0, r1);
+      ds_f32[2 * k] = (!MASKED || ((allow >> (2 * k)) & 1u)) ? r0 : 0.f;
+      ds_f32[2 * k + 1] = (!MASKED || ((allow >> (2 * k + 1)) & 1u)) ? r1 : 0.f;
+    }
     if constexpr (MASKED) {
       const uint32_t lo = static_cast<uint32_t>(static_cast<int32_t>(allow << (31 - 2 * k)) >> 31);
       const uint32_t hi = static_cast<uint32_t>(static_cast<int32_t>(allow << (30 - 2 * k)) >> 31);
@@ -311,7 +321,7 @@ __device__ __forceinline__ void bwd_init(BwdCtl& ctl, int tid, int warp) {
 namespace hstu {
 
 // ---------------------------------------------------------------------------------- dQ
-template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false>
+template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB = false, bool RAB_GRAD = false>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     hstu_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -492,10 +502,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       };
+      // gradients of the bias tables (when asked for): this warp's sums over the unit
+      RabGradWarp* rg = reinterpret_cast<RabGradWarp*>(smem + Cfg::RAB_GRAD_OFFSET) + (warp - 2);
+      RabGradAcc racc{-1, 0.f, 0.f};
+      // (RAB_GRAD: the instantiation that computes them, launched only when asked)
+      const bool grad_time = RAB_GRAD && p.d_rab_time != nullptr && p.ts_q != nullptr && p.rab_time != nullptr;
+      const bool grad_pos = RAB_GRAD && p.d_rab_pos != nullptr && p.rab_pos != nullptr;
       if constexpr (RAB) {
         __syncwarp();   // the previous unit's lookups are done
         rab_build(*rw, p.ts_q != nullptr ? p.rab_time : nullptr, p.rab_pos, p.rab_np, u.h,
                   SOFTMAX ? kLog2e : 0.5f, lane);
+        if (grad_time || grad_pos) {
+          for (int i = lane; i < kRabTimeBuckets + 1; i += 32) rg->t[i] = 0.f;
+          for (int i = lane; i < p.rab_np; i += 32) rg->pos[i] = 0.f;
+          racc = RabGradAcc{-1, 0.f, 0.f};
+        }
         __syncwarp();
         if (p.ts_q != nullptr) ts_row = p.ts_q[u.s.q0 + row];
         pos_row = row < u.s.c ? row : row + (u.s.ukv - u.s.u);
@@ -525,18 +546,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::tmem_ld32(sb + 64, dv);
           ptx::tmem_ld_wait(sv);
           ptx::tmem_ld_wait(dv);
+          RabRow rr{0, 0};
+          RabCols rc{};
+          RabChunk rk{};
+          const bool has_time = p.ts_q != nullptr && p.rab_time != nullptr;
           if constexpr (RAB) {   // sv becomes alpha s + rab, scaled (SiLU: / 2, softmax: * log2 e)
             const long long ck = hh ? ck1 : ck0;
             const long long base = __shfl_sync(0xffffffffu, ck, 0);
-            const RabRow rr{p.ts_q != nullptr ? rab_rel_ts(ts_row, base) : 0, pos_row};
-            rab_apply32<true>(sv, SOFTMAX ? alpha * kLog2e : half_alpha, *rw, p.rab_np,
-                              p.ts_q != nullptr && p.rab_time != nullptr, rr,
-                              rab_cols(p.ts_q != nullptr ? rab_rel_ts(ck, base) : 0,
-                                       j0 + kHalf * hh + 32 * wg + lane, true));
+            rr = RabRow{p.ts_q != nullptr ? rab_rel_ts(ts_row, base) : 0, pos_row};
+            rc = rab_cols(p.ts_q != nullptr ? rab_rel_ts(ck, base) : 0, j0 + kHalf * hh + 32 * wg + lane, true);
+            rk = rab_apply32<true>(sv, SOFTMAX ? alpha * kLog2e : half_alpha, *rw, p.rab_np, has_time, rr, rc);
           }
+          float dsf[32];   // dS in fp32, for the bias tables' gradients
+          const bool want_ds = RAB_GRAD && (grad_time || grad_pos);
           if constexpr (!SOFTMAX) {
-            if (full) silu_bwd_f32<BF16, false, false, RAB>(sv, dv, half_alpha, mb, pk, pk);
-            else silu_bwd_f32<BF16, false, true, RAB>(sv, dv, half_alpha, mb, pk, pk);
+            if (full) silu_bwd_f32<BF16, false, false, RAB>(sv, dv, half_alpha, mb, pk, pk, want_ds ? dsf : nullptr);
+            else silu_bwd_f32<BF16, false, true, RAB>(sv, dv, half_alpha, mb, pk, pk, want_ds ? dsf : nullptr);
           } else {
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
@@ -547,8 +572,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const float g = __uint_as_float(dv[k + e]);
                 const float r = ex2_approx((RAB ? s : s * (alpha * kLog2e)) - lse2) * (g - dlt);
                 ds[e] = ((mb >> (k + e)) & 1u) ? r : 0.f;
+                dsf[k + e] = ds[e];
               }
               pk[k >> 1] = pack2<BF16>(ds[0], ds[1]);
+            }
+          }
+          if constexpr (RAB) {
+            if (want_ds) {
+              // a lane with no row of the sequence (past a ragged last query
+              // tile) computed dS from rows that are not this sequence's: in a
+              // full tile nothing masked it, and its dQ is never stored
+              if (!valid) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) dsf[k] = 0.f;
+              }
+              rab_grad32<true>(dsf, rk, *rg, racc, *rw, p.rab_np, grad_time, grad_pos, rr, rc);
             }
           }
           ptx::tmem_st16(sb, pk);
@@ -558,6 +596,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       if (!ok) break;
+      if constexpr (RAB) {
+        // this warp's table gradients of the unit, x attn_scale (dS above is kept
+        // without it), into the outputs
+        if (grad_time || grad_pos) {
+          rab_grad_flush(racc, *rg, p.rab_np, grad_time, grad_pos);
+          __syncwarp();
+          if (grad_time && lane < kRabTimeBuckets) {
+            const float v = rg->t[lane] + (lane == kRabTimeBuckets - 1 ? rg->t[kRabTimeBuckets] : 0.f);
+            if (v != 0.f) atomicAdd(p.d_rab_time + u.h * kRabTimeBuckets + lane, v * u.scale);
+          }
+          if (grad_pos) {
+            for (int i = lane; i < p.rab_np; i += 32) {
+              const float v = rg->pos[i];
+              if (v != 0.f) atomicAdd(p.d_rab_pos + static_cast<long long>(u.h) * p.rab_np + i, v * u.scale);
+            }
+          }
+        }
+      }
       // dQ * alpha * attn_scale out of TMEM: this warpgroup's half of the D columns
       if (!bwd_warp_wait(ctl, p, &ctl.acc_full, u_it & 1)) break;
       ptx::tc_fence_after();
@@ -900,11 +956,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB>
 cudaError_t launch_bwd_pair(const BwdMaps& m, const BwdParams& p, int grid_q, int grid_kv, cudaStream_t stream) {
   constexpr int smem = BwdCfg<D, DV, RAB>::SMEM_BYTES;
-  auto kq = hstu_bwd_dq_kernel<D, DV, BF16, SOFTMAX, RAB>;
+  // the dQ kernel that also sums the bias tables' gradients, when they are asked for
+  const bool grad = RAB && (p.d_rab_time != nullptr || p.d_rab_pos != nullptr);
+  auto kq = grad ? hstu_bwd_dq_kernel<D, DV, BF16, SOFTMAX, RAB, RAB> : hstu_bwd_dq_kernel<D, DV, BF16, SOFTMAX, RAB>;
   auto kkv = hstu_bwd_dkdv_kernel<D, DV, BF16, SOFTMAX, RAB>;
   static_assert(smem + sizeof(BwdCtl) <= 232448, "shared memory over the 227 KB a CTA may use");
-  static std::atomic<unsigned long long> q_attr_set{0}, kv_attr_set{0};
-  cudaError_t e = ensure_smem_attr(kq, smem, q_attr_set);
+  static std::atomic<unsigned long long> q_attr_set{0}, qg_attr_set{0}, kv_attr_set{0};
+  cudaError_t e = ensure_smem_attr(kq, smem, grad ? qg_attr_set : q_attr_set);
   if (e == cudaSuccess) e = ensure_smem_attr(kkv, smem, kv_attr_set);
   if (e != cudaSuccess) return e;
   kq<<<grid_q, kBwdThreads, smem, stream>>>(m.q, m.k, m.v, m.d_o, m.q8, m.d_o8, p);

@@ -408,14 +408,11 @@ struct BwdParams {
   const float* rab_time;
   const float* rab_pos;
   int rab_np;
-  // in-kernel scheduling (fused != 0, batch <= kFusedMaxBatch): every CTA
-  // validates the offsets and orders the units itself; units and
-  // group_scale above are then unused
-  int fused;
-  int total_kv, max_seqlen_q, max_seqlen_kv;
+  // gradients of the bias tables, [nhead, 11] and [nhead, rab_np] (null = not
+  // wanted); zeroed by the host, summed into by the dQ kernel
+  float* d_rab_time;
+  float* d_rab_pos;
   int ctx[kMaxGroups], loc[kMaxGroups], mf[kMaxGroups];
-  int max_uih[kMaxGroups];        // per-group override of the attn_scale default (0 = automatic)
-  float attn_scale[kMaxGroups];   // per-group attn_scale (0 = 1 / max UIH length of the group)
 };
 
 // Combine kernel parameters (split-KV).

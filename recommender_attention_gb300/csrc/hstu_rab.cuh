@@ -34,6 +34,7 @@
 #include <stdint.h>
 
 #include "hstu_common.cuh"
+#include "ptx.cuh"
 
 namespace hstu {
 
@@ -121,56 +122,159 @@ __device__ __forceinline__ RabCols rab_cols(int ts, int pos, bool valid) {
   return c;
 }
 
-// r[k] (a raw score, fp32 bits) becomes fma(s, mul, scaled bias) for the 32
-// columns of the chunk: bias(row, column k) = time weight of |row.ts - ts_k|
-// plus distance weight of min(|row.pos - pos_k|, np - 1).  CONTIG: column k's
-// position is c.pmin + k (keys of a tile), else it comes from lane k.  Each
-// term is one constant per row when the row's timestamp (position) lies
-// outside the columns' range and both ends fall in the same bucket (are at
-// least np - 1 away).  The whole warp takes one of three forms, so every lane
-// runs the same shuffles: both terms constant, only the distance looked up
-// key by key, or both looked up (a constant distance term then reads the
-// table's last entry).  Fewer unrolled forms keep the code small enough to
-// stay in the instruction cache.  Warp-collective.
-template <bool CONTIG>
-__device__ __forceinline__ void rab_apply32(uint32_t* r, float mul, const RabWarp& w, int np, bool has_time,
-                                            const RabRow& row, const RabCols& c) {
+// How a chunk's two terms vary, for one row: the distance term is one constant
+// (the table's last entry) when every column is at least np - 1 away; the time
+// term is one constant when the row's timestamp lies outside the columns'
+// range and both ends fall in the same bucket (the extreme gaps are at the
+// range's ends).  all_* are the warp's agreement (warp-collective).
+struct RabChunk {
+  bool time_const;   // this row
+  int slot;          // this row's time slot at the columns' near end (the constant when time_const)
+  bool all_pos, all_time;
+};
+__device__ __forceinline__ RabChunk rab_classify(const RabWarp& w, int np, bool has_time, const RabRow& row,
+                                                 const RabCols& c) {
+  RabChunk k;
   const int dmin = row.pos <= c.pmin ? c.pmin - row.pos : (row.pos >= c.pmax ? row.pos - c.pmax : 0);
   const bool pos_const = dmin >= np - 1;
-  bool time_const = !has_time;
-  float wt_const = 0.f;
+  k.time_const = !has_time;
+  k.slot = -1;
   if (has_time && (row.ts >= c.tmax || row.ts <= c.tmin)) {
     const int g0 = abs(row.ts - c.tmin), g1 = abs(row.ts - c.tmax);
     const int s0 = rab_time_slot(w, g0), s1 = rab_time_slot(w, g1);
-    time_const = s0 == s1 || (s0 >= kRabTimeBuckets - 1 && s1 >= kRabTimeBuckets - 1);
-    wt_const = w.wt[s0];
+    k.time_const = s0 == s1 || (s0 >= kRabTimeBuckets - 1 && s1 >= kRabTimeBuckets - 1);
+    k.slot = s0;
   }
-  const bool all_pos = __all_sync(0xffffffffu, pos_const);
-  const bool all_time = __all_sync(0xffffffffu, time_const);
-  if (all_pos && all_time) {
+  k.all_pos = __all_sync(0xffffffffu, pos_const);
+  k.all_time = __all_sync(0xffffffffu, k.time_const);
+  return k;
+}
+
+// r[k] (a raw score, fp32 bits) becomes fma(s, mul, scaled bias) for the 32
+// columns of the chunk: bias(row, column k) = time weight of |row.ts - ts_k|
+// plus distance weight of min(|row.pos - pos_k|, np - 1).  CONTIG: column k's
+// position is c.pmin + k (keys of a tile), else it comes from lane k.  The
+// whole warp takes one of three forms (rab_classify), so every lane runs the
+// same shuffles: both terms constant, only the distance looked up key by key,
+// or both looked up (a constant distance term then reads the table's last
+// entry).  Fewer unrolled forms keep the code small enough to stay in the
+// instruction cache.  Returns the chunk's classification.  Warp-collective.
+template <bool CONTIG>
+__device__ __forceinline__ RabChunk rab_apply32(uint32_t* r, float mul, const RabWarp& w, int np, bool has_time,
+                                                const RabRow& row, const RabCols& c) {
+  const RabChunk k = rab_classify(w, np, has_time, row, c);
+  const float wt_const = k.slot >= 0 ? w.wt[k.slot] : 0.f;
+  if (k.all_pos && k.all_time) {
     const float b = w.pos[np - 1] + wt_const;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));
-  } else if (all_time) {   // the distance varies over the chunk, the time bucket does not
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(fmaf(__uint_as_float(r[j]), mul, b));
+  } else if (k.all_time) {   // the distance varies over the chunk, the time bucket does not
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int pk = CONTIG ? c.pmin + k : __shfl_sync(0xffffffffu, c.pos, k);
+    for (int j = 0; j < 32; ++j) {
+      const int pk = CONTIG ? c.pmin + j : __shfl_sync(0xffffffffu, c.pos, j);
       int d = abs(row.pos - pk);
       d = d < np - 1 ? d : np - 1;
-      r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, w.pos[d] + wt_const));
+      r[j] = __float_as_uint(fmaf(__uint_as_float(r[j]), mul, w.pos[d] + wt_const));
     }
   } else {   // the time bucket varies (and the distance may)
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const int tk = __shfl_sync(0xffffffffu, c.ts, k);
-      const int pk = CONTIG ? c.pmin + k : __shfl_sync(0xffffffffu, c.pos, k);
-      float b = time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
+    for (int j = 0; j < 32; ++j) {
+      const int tk = __shfl_sync(0xffffffffu, c.ts, j);
+      const int pk = CONTIG ? c.pmin + j : __shfl_sync(0xffffffffu, c.pos, j);
+      float b = k.time_const ? wt_const : rab_time_weight(w, abs(row.ts - tk));
       int d = abs(row.pos - pk);
       d = d < np - 1 ? d : np - 1;
       b += w.pos[d];
-      r[k] = __float_as_uint(fmaf(__uint_as_float(r[k]), mul, b));
+      r[j] = __float_as_uint(fmaf(__uint_as_float(r[j]), mul, b));
     }
   }
+  return k;
+}
+
+// Per elementwise warp: the gradients of the two tables over the current
+// unit (slot 11 of t stands for bucket 10, as in RabWarp::wt).
+struct RabGradWarp {
+  float t[kRabTimeBuckets + 1];
+  float pos[kRabMaxPos];
+};
+
+// One lane's running sums of score gradients between flushes: the time
+// bucket it is adding to (-1: none yet) and that sum, and the sum for the
+// distance table's last entry (every column at least np - 1 away).  A row's
+// bucket changes only a few times along a unit's key tiles, so most chunks
+// add in registers.
+struct RabGradAcc {
+  int t_slot;
+  float t_sum;
+  float far_pos;
+};
+__device__ __forceinline__ void rab_grad_time_add(RabGradAcc& a, RabGradWarp& g, int slot, float v) {
+  if (slot != a.t_slot) {
+    if (a.t_slot >= 0) atomicAdd(&g.t[a.t_slot], a.t_sum);
+    a.t_slot = slot;
+    a.t_sum = 0.f;
+  }
+  a.t_sum += v;
+}
+
+// Adds the score gradients ds[k] of one row's chunk (the columns rab_apply32
+// took, with the classification k it returned) to the entries of the two
+// tables they read:
+// time-bucket sums and the far distance entry in the lane's registers (acc),
+// nearer distances per column into the warp's shared sums (neighbouring rows
+// are at different distances, so those adds rarely collide).  has_time /
+// has_pos: the tables exist.  Warp-collective.
+template <bool CONTIG>
+__device__ __forceinline__ void rab_grad32(const float (&ds)[32], const RabChunk& k, RabGradWarp& g, RabGradAcc& acc,
+                                           const RabWarp& w, int np, bool has_time, bool has_pos, const RabRow& row,
+                                           const RabCols& c) {
+  float sum;
+  {
+    uint64_t s2 = ptx::f32x2(ds[0], ds[1]);
+#pragma unroll
+    for (int j = 2; j < 32; j += 2) s2 = ptx::fma_f32x2(ptx::f32x2(ds[j], ds[j + 1]), ptx::f32x2(1.f, 1.f), s2);
+    float lo, hi;
+    ptx::f32x2_split(s2, lo, hi);
+    sum = lo + hi;
+  }
+  if (has_pos) {
+    if (k.all_pos) {
+      acc.far_pos += sum;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int pk = CONTIG ? c.pmin + j : __shfl_sync(0xffffffffu, c.pos, j);
+        const int d = abs(row.pos - pk);
+        if (d < np - 1) atomicAdd(&g.pos[d], ds[j]);
+        else acc.far_pos += ds[j];
+      }
+    }
+  }
+  if (has_time) {
+    if (k.all_time) {
+      rab_grad_time_add(acc, g, k.slot, sum);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int tk = __shfl_sync(0xffffffffu, c.ts, j);
+        if (!k.time_const) rab_grad_time_add(acc, g, rab_time_slot(w, abs(row.ts - tk)), ds[j]);
+      }
+      if (k.time_const) rab_grad_time_add(acc, g, k.slot, sum);
+    }
+  }
+}
+
+// The lane's register sums into the warp's shared sums (the far distance
+// entry summed over the warp first).  Warp-collective.
+__device__ __forceinline__ void rab_grad_flush(RabGradAcc& acc, RabGradWarp& g, int np, bool has_time, bool has_pos) {
+  if (has_time && acc.t_slot >= 0) atomicAdd(&g.t[acc.t_slot], acc.t_sum);
+  if (has_pos) {
+    float tot = acc.far_pos;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&g.pos[np - 1], tot);
+  }
+  acc = RabGradAcc{-1, 0.f, 0.f};
 }
 
 }  // namespace hstu

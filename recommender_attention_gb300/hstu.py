@@ -65,6 +65,7 @@ class BwdArgs(ctypes.Structure):
         ("fwd", FwdArgs), ("d_o", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
         ("dv", ctypes.c_void_p), ("do_row_stride", ctypes.c_int64), ("dq_row_stride", ctypes.c_int64),
         ("dk_row_stride", ctypes.c_int64), ("dv_row_stride", ctypes.c_int64),
+        ("d_rab_time", ctypes.c_void_p), ("d_rab_pos", ctypes.c_void_p),
     ]
 
 
@@ -257,7 +258,8 @@ class HstuBwdCall:
     def __init__(self, q, k, v, d_o, seq_offsets_q, seq_offsets_kv=None, num_targets=None, *,
                  o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                  dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
-                 dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, **kw):
+                 dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 rab_grads: bool = False, **kw):
         kw.pop("num_splits", None)
         kw.pop("save_lse", None)
         self.fwd = HstuCall(q, k, v, seq_offsets_q, seq_offsets_kv, num_targets, out=o, lse=lse,
@@ -277,6 +279,15 @@ class HstuBwdCall:
         b.d_o, b.dq, b.dk, b.dv = _ptr(d_o), _ptr(self.dq), _ptr(self.dk), _ptr(self.dv)
         b.do_row_stride, b.dq_row_stride = d_o.stride(0), self.dq.stride(0)
         b.dk_row_stride, b.dv_row_stride = self.dk.stride(0), self.dv.stride(0)
+        # gradients of the bias tables the call uses (rab_grads=True)
+        self.d_rab_time = self.d_rab_pos = None
+        if rab_grads:
+            nh = q.shape[1]
+            if kw.get("rab_time") is not None and kw.get("timestamps_q") is not None:
+                self.d_rab_time = torch.empty((nh, 11), dtype=torch.float32, device=q.device)
+            if kw.get("rab_pos") is not None:
+                self.d_rab_pos = torch.empty((nh, kw["rab_pos"].shape[1]), dtype=torch.float32, device=q.device)
+        b.d_rab_time, b.d_rab_pos = _ptr(self.d_rab_time), _ptr(self.d_rab_pos)
         size = ctypes.c_size_t(0)
         st = self.lib.hstu_attn_bwd_workspace_size(ctypes.byref(b), ctypes.byref(size))
         if st != HSTU_OK:
@@ -308,11 +319,15 @@ def hstu_attn_bwd(q, k, v, d_o, seq_offsets_q, seq_offsets_kv=None, num_targets=
     """HSTU attention backward (``hstu_attn_bwd`` in ``include/hstu_attn.h``):
     the gradients of the forward with the same keyword arguments for the output
     gradient ``d_o``.  Softmax mode needs the forward's ``o=`` and ``lse=``.
-    Returns ``(dq, dk, dv)``."""
+    Returns ``(dq, dk, dv)``, or with ``rab_grads=True``
+    ``(dq, dk, dv, d_rab_time, d_rab_pos)`` (None for a table the call has no
+    use of)."""
     call = HstuBwdCall(q, k, v, d_o, seq_offsets_q, seq_offsets_kv, num_targets, **kw)
     call.launch(stream)
     if check:
         call.check(stream)
+    if kw.get("rab_grads"):
+        return call.dq, call.dk, call.dv, call.d_rab_time, call.d_rab_pos
     return call.dq, call.dk, call.dv
 
 

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_strings_and_struct_layout(lib):
-    assert lib.hstu_abi_version() == 4
+    assert lib.hstu_abi_version() == 5
     for s in range(6):
         assert lib.hstu_status_string(s)
     assert lib.hstu_status_string(99) == b"unknown status"
@@ -180,6 +180,28 @@ def test_backward_rejects_before_launch(lib):
     b.dk = 8192
     b.fwd.softmax = 1
     assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1     # softmax needs o and lse
+
+
+def test_backward_rab_gradients_need_their_table(lib):
+    """A bias-table gradient is only computed for a table the call uses (the
+    time table with its timestamps); otherwise the call returns
+    HSTU_ERR_INVALID_ARG before anything else is checked or launched."""
+    b = _bwd()
+    b.fwd.q = b.fwd.k = b.fwd.v = b.fwd.seq_offsets_q = 4096
+    b.d_o = b.dq = b.dk = b.dv = 8192
+    b.d_rab_time = 1 << 16
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1          # no time table
+    b.fwd.rab_time = 1 << 17
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1          # no timestamps
+    b.fwd.timestamps_q = 1 << 18
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 3          # accepted; then: no workspace
+    b.d_rab_pos = 1 << 19
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1          # no positional table
+    b.fwd.rab_pos, b.fwd.rab_pos_buckets = 1 << 20, 16
+    b.d_rab_pos = (1 << 19) + 2
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 1          # misaligned
+    b.d_rab_pos = 1 << 19
+    assert lib.hstu_attn_bwd(ctypes.byref(b), None) == 3
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

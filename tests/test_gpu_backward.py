@@ -33,28 +33,38 @@ def _host(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def gpu_backward(w, q, k, v, d_o, **over):
+def gpu_backward(w, q, k, v, d_o, rab_grads=False, **over):
     dq, dk, dv, off_q, off_kv, tg = device_inputs(w, q, k, v)
     kw = call_kwargs(w, **over)
     o = lse = None
     if w.softmax:
         o, lse = hstu.hstu_attn_fwd(dq, dk, dv, off_q, off_kv, tg, check=True, **kw)
-    g = hstu.hstu_attn_bwd(dq, dk, dv, d_o.cuda(), off_q, off_kv, tg, o=o, lse=lse, check=True, **kw)
+    g = hstu.hstu_attn_bwd(dq, dk, dv, d_o.cuda(), off_q, off_kv, tg, o=o, lse=lse, check=True,
+                           rab_grads=rab_grads, **kw)
     torch.cuda.synchronize()
-    return tuple(_host(x) for x in g)
+    return tuple(None if x is None else _host(x) for x in g)
 
 
-def check_backward(w, rab=False, **over):
-    """rab: with the workload's relative attention bias (Workload.rab_inputs)."""
+def check_backward(w, rab=False, use_time=True, use_pos=True, **over):
+    """rab: with the workload's relative attention bias (Workload.rab_inputs),
+    and then the gradients of its tables as well (use_time / use_pos keep one
+    table only)."""
     q, k, v = w.tensors()
     d_o = w.grad_output()
     bias = w.rab_inputs() if rab else None
     if rab:
-        over = {**over, **rab_kwargs(bias)}
-    got = gpu_backward(w, q, k, v, d_o, **over)
+        over = {**over, **rab_kwargs(bias, use_time, use_pos)}
+    got = gpu_backward(w, q, k, v, d_o, rab_grads=rab, **over)
     ref = hstu_attention_backward(as_f64(q), as_f64(k), as_f64(v), as_f64(d_o), w.seq_offsets_q(),
-                                  w.seq_offsets_kv(), w.num_targets(), oracle_params(w, bias))
-    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+                                  w.seq_offsets_kv(), w.num_targets(), oracle_params(w, bias, use_time, use_pos),
+                                  rab_grads=rab)
+    names = ("dq", "dk", "dv", "d_rab_time", "d_rab_pos")
+    for name, a, b in zip(names, got, ref):
+        if name.startswith("d_rab"):
+            # the tables a call uses get gradients; the others none
+            assert (a is None) == (b is None), f"{w.name} {name}: presence differs"
+            if a is None:
+                continue
         assert_parity(a, b, w.dtype, what=f"{w.name} {name}")
 
 
@@ -112,6 +122,15 @@ def test_fuzz_backward_rab(seed):
     w = W.random_small(100 + seed, hdim=[64, 128][seed % 2], softmax=seed % 4 >= 2,
                        dtype="bf16" if seed % 3 else "fp16", kv_targets=seed % 4 == 3)
     check_backward(w.with_(rab_pos_buckets=[1, 9, 64, 256][seed % 4]), rab=True)
+
+
+@pytest.mark.parametrize("use_time,use_pos", [(True, False), (False, True)])
+@pytest.mark.parametrize("softmax", [False, True])
+def test_backward_rab_one_table(softmax, use_time, use_pos):
+    """A bias with one table only: its gradient alone (the other output stays
+    unset), and dq, dk, dv through it."""
+    check_backward(W.jagged_readme().with_(softmax=softmax, rab_pos_buckets=32), rab=True, use_time=use_time,
+                   use_pos=use_pos)
 
 
 @pytest.mark.parametrize("softmax", [False, True])
