@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define HSTU_ABI_VERSION 5
+#define HSTU_ABI_VERSION 6
 #define HSTU_MAX_GROUPS 256
 #define HSTU_MAX_SPLITS 16
 #define HSTU_RAB_TIME_BUCKETS 11
@@ -136,6 +136,14 @@ typedef struct hstu_fwd_args {
   const float* rab_time;          /* [dev] [H, HSTU_RAB_TIME_BUCKETS] one scalar per head and bucket */
   const float* rab_pos;           /* [dev] [H, rab_pos_buckets] one scalar per head and clamped distance */
   int32_t rab_pos_buckets;        /* P: 1..HSTU_RAB_MAX_POS with rab_pos, else ignored */
+  /* Forward kernel choice where both apply (hdim_qk == hdim_v == 128, no
+   * bias, batch <= 128): the CTA-pair kernel runs two query tiles of one
+   * (sequence, head) on the two SMs of a TPC as one 256-row tile, each SM
+   * loading half of every key and value tile; the single-CTA kernel runs one
+   * query tile per SM.  Both compute the same results.
+   * 0 = automatic (single CTAs, the faster on every measured workload),
+   * 1 = pairs, -1 = single CTAs.  Ignored elsewhere. */
+  int32_t cta_pairs;
 } hstu_fwd_args;
 
 /* Counters of one call's schedule (hstu_attn_fwd_stats). */

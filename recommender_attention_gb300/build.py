@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libhstu_attn.so")
 
-SOURCES = ["hstu_api.cu", "hstu_sched.cu", "hstu_fwd_d64.cu", "hstu_fwd_d96.cu", "hstu_fwd_d128.cu", "hstu_fwd_d256.cu",
+SOURCES = ["hstu_api.cu", "hstu_sched.cu", "hstu_fwd_d64.cu", "hstu_fwd_d96.cu", "hstu_fwd_d128.cu", "hstu_fwd_pair_d128.cu", "hstu_fwd_d256.cu",
            "hstu_static_ws.cu", "hstu_bwd_d64.cu", "hstu_bwd_d96.cu", "hstu_bwd_d128.cu",
            "hstu_fwd_rab_d64.cu", "hstu_fwd_rab_d128.cu", "hstu_bwd_rab_d64.cu", "hstu_bwd_rab_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -75,6 +75,7 @@ hstu_status validate(const hstu_fwd_args* a) {
   if (!std::isfinite(a->alpha) || a->alpha < 0.f) return HSTU_ERR_INVALID_ARG;
   if (a->seq_offsets_kv == nullptr && a->total_kv != a->total_q) return HSTU_ERR_INVALID_ARG;
   if (a->kv_targets != 0 && a->kv_targets != 1) return HSTU_ERR_INVALID_ARG;
+  if (a->cta_pairs < -1 || a->cta_pairs > 1) return HSTU_ERR_INVALID_ARG;
   if (a->kv_targets && a->seq_offsets_kv == nullptr) return HSTU_ERR_INVALID_ARG;
   if (a->rab_time != nullptr || a->rab_pos != nullptr) {
     if (a->hdim_v != a->hdim_qk || (a->hdim_qk != 64 && a->hdim_qk != 128)) return HSTU_ERR_UNSUPPORTED;
@@ -360,12 +361,23 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
       !encode_map(&maps.v, a->v, bf16, wv, a->total_kv, packed_or(a->v_row_stride, wv)) ||
       !encode_map(&maps.o, a->o, bf16, wv, a->total_q, packed_or(a->o_row_stride, wv), 32))
     return HSTU_ERR_CUDA;
+  const bool rab = a->rab_time != nullptr || a->rab_pos != nullptr;
+  const bool fused = a->batch <= kFusedMaxBatch;
+  const bool sm = a->softmax != 0;
+  // CTA pairs when asked for (hdim 128 without a bias, in-kernel schedule)
+  int pair_clusters = 0;
+  if (D == 128 && a->hdim_v == 128 && !rab && fused && a->cta_pairs > 0) {
+    const int mc = fwd_pair_max_clusters_d128(bf16, sm);
+    pair_clusters = mc < pl.max_units ? mc : pl.max_units;
+    if (pair_clusters > 0 &&
+        !encode_map(&maps.k64, a->k, bf16, wq, a->total_kv, packed_or(a->k_row_stride, wq), kBlockN / 2))
+      return HSTU_ERR_CUDA;
+  }
 
   const PrepParams pp = make_prep(a, pl);
   // Batches up to kFusedMaxBatch sequences are scheduled inside the forward
   // kernel, after a one-block reset of the header; larger ones by the
   // scheduler kernel.
-  const bool fused = a->batch <= kFusedMaxBatch;
   if ((fused ? launch_fwd_reset(pp.ws_header, stream) : launch_prep(pp, stream)) != cudaSuccess)
     return HSTU_ERR_CUDA;
 
@@ -393,7 +405,6 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
   fp.kv_targets = a->kv_targets;
   fp.splits = pl.splits;
   fp.alpha = a->alpha != 0.f ? a->alpha : 1.f / std::sqrt(static_cast<float>(a->hdim_qk));
-  const bool rab = a->rab_time != nullptr || a->rab_pos != nullptr;
   if (rab) {
     fp.ts_q = a->rab_time != nullptr ? reinterpret_cast<const long long*>(a->timestamps_q) : nullptr;
     fp.ts_kv = fp.ts_q == nullptr ? nullptr
@@ -416,8 +427,8 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
       cudaEventRecord(static_cast<cudaEvent_t>(a->event_fwd_begin), stream) != cudaSuccess)
     return HSTU_ERR_CUDA;
   cudaError_t e;
-  const bool sm = a->softmax != 0;
-  if (rab) e = D == 64 ? launch_fwd_rab_d64(maps, fp, bf16, sm, grid, stream)
+  if (pair_clusters > 0) e = launch_fwd_pair_d128(maps, fp, bf16, sm, pair_clusters, stream);
+  else if (rab) e = D == 64 ? launch_fwd_rab_d64(maps, fp, bf16, sm, grid, stream)
                        : launch_fwd_rab_d128(maps, fp, bf16, sm, grid, stream);
   else if (D == 64) e = launch_fwd_d64(maps, fp, bf16, sm, grid, stream);
   else if (D == 96) e = launch_fwd_d96(maps, fp, a->hdim_v, bf16, sm, grid, stream);

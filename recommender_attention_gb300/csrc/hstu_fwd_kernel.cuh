@@ -233,8 +233,10 @@ __device__ __forceinline__ void warp_exclusive_scan(int* v, int n, int lane) {
 // (most first, ties by index) and the units are numbered per position with
 // heads outer, query tiles from the last down and splits innermost.
 // `scratch` (3 batch + 2 ints) is shared memory no TMA load uses yet.
-// Returns the number of units.
-__device__ __forceinline__ int fused_schedule(const FwdParams& p, FwdSmemCtl& ctl, int* scratch, int tid, int nthreads) {
+// TPU: query tiles per unit (2: the CTA-pair kernel, whose unit is two query
+// tiles of one head, from the last down).  Returns the number of units.
+template <int TPU = 1, typename Ctl>
+__device__ __forceinline__ int fused_schedule(const FwdParams& p, Ctl& ctl, int* scratch, int tid, int nthreads) {
   const int B = p.batch;
   const int G = p.num_groups;
   int* tb = scratch;        // [B + 1] query tiles per sequence, then their exclusive prefix
@@ -289,7 +291,7 @@ __device__ __forceinline__ int fused_schedule(const FwdParams& p, FwdSmemCtl& ct
   __syncthreads();
   for (int pos = tid; pos < B; pos += nthreads) {
     const int b = ctl.f_order[pos];
-    ctl.f_ubase[pos] = (tb[b + 1] - tb[b]) * p.nhead * p.splits;
+    ctl.f_ubase[pos] = ((tb[b + 1] - tb[b] + TPU - 1) / TPU) * p.nhead * p.splits;
     const int g = b / p.batch_per_group;
     float sc = p.attn_scale[g];
     if (sc == 0.f) {   // 0 means 1 / max UIH length of the group
@@ -327,8 +329,8 @@ __device__ __forceinline__ UnitView decode_fused_unit(const FwdParams& p, const 
 }
 
 // Bounded wait; on timeout flags the error word and asks every role to stop.
-__device__ __forceinline__ bool wait_or_abort(FwdSmemCtl& ctl, const FwdParams& p, uint64_t* bar,
-                                              uint32_t parity) {
+template <typename Ctl>
+__device__ __forceinline__ bool wait_or_abort(Ctl& ctl, const FwdParams& p, uint64_t* bar, uint32_t parity) {
   if (ptx::mbar_wait(bar, parity, kWaitLimitNs)) return true;
   ctl.abort_flag = 1;
   atomicOr(&p.ws_header[kWsError], kErrTimeout);
@@ -337,8 +339,8 @@ __device__ __forceinline__ bool wait_or_abort(FwdSmemCtl& ctl, const FwdParams& 
 
 // Warp-uniform bounded wait for the elementwise group: every lane waits, then
 // the warp agrees (and reconverges) before the next .sync.aligned tcgen05 op.
-__device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdParams& p, uint64_t* bar,
-                                                   uint32_t parity) {
+template <typename Ctl>
+__device__ __forceinline__ bool warp_wait_or_abort(Ctl& ctl, const FwdParams& p, uint64_t* bar, uint32_t parity) {
   const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, kWaitLimitNs));
   if (!ok) {
     ctl.abort_flag = 1;
@@ -351,16 +353,15 @@ __device__ __forceinline__ bool warp_wait_or_abort(FwdSmemCtl& ctl, const FwdPar
 // patterns in r), in fp32: h = alpha s / 2 (one packed f32x2 multiply per
 // pair), t = tanh(h) (tanh.approx.f32 per element), SiLU(alpha s) = h + h t
 // (one packed f32x2 fma per pair).  Each pair is rounded once, to the storage
-// type, when it is packed into its P word; the NP words go to the TMEM columns
-// at p_tmem.  PRESCALED: r already holds alpha s / 2 (plus the halved bias).
+// type, when it is packed into its P word pk[k] (masked columns: 0).
+// PRESCALED: r already holds alpha s / 2 (plus the halved bias).
 template <bool BF16, bool MASKED, bool PRESCALED = false, int NP = 32>
-__device__ __forceinline__ void silu_pack(const uint32_t (&r)[2 * NP], uint32_t p_tmem, float half_alpha,
-                                          const RowMask& rm, int c0) {
+__device__ __forceinline__ void silu_words(const uint32_t (&r)[2 * NP], uint32_t (&pk)[NP], float half_alpha,
+                                           const RowMask& rm, int c0) {
   static_assert(NP == 16 || NP == 32, "16 or 32 pairs");
-  // all pairs stage by stage, so the NP tanh pairs are in flight together; one store
+  // all pairs stage by stage, so the NP tanh pairs are in flight together
   const uint64_t ha = ptx::f32x2(half_alpha, half_alpha);
   uint64_t h[NP];
-  uint32_t pk[NP];
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     h[k] = ptx::f32x2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
@@ -386,6 +387,14 @@ __device__ __forceinline__ void silu_pack(const uint32_t (&r)[2 * NP], uint32_t 
       pk[k] &= (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
     }
   }
+}
+
+// silu_words, then the NP words to the TMEM columns at p_tmem (one store).
+template <bool BF16, bool MASKED, bool PRESCALED = false, int NP = 32>
+__device__ __forceinline__ void silu_pack(const uint32_t (&r)[2 * NP], uint32_t p_tmem, float half_alpha,
+                                          const RowMask& rm, int c0) {
+  uint32_t pk[NP];
+  silu_words<BF16, MASKED, PRESCALED, NP>(r, pk, half_alpha, rm, c0);
   if constexpr (NP == 32) ptx::tmem_st32(p_tmem, pk);
   else ptx::tmem_st16(p_tmem, pk);
 }

@@ -27,10 +27,12 @@ inline cudaError_t ensure_smem_attr(Kernel kern, int smem, std::atomic<unsigned 
 }
 
 // Tensor maps of the forward: q, k, v with 128-row boxes, q with 8-row boxes
-// (query tiles whose rows come in two runs), and o with 32-row boxes (the
-// TMA-store epilogue); every box is 64 columns wide with a 128-byte swizzle.
+// (query tiles whose rows come in two runs), o with 32-row boxes (the
+// TMA-store epilogue) and k with 64-row boxes (the CTA-pair kernel, where each
+// CTA loads half of a key tile); every box is 64 columns wide with a 128-byte
+// swizzle.
 struct FwdMaps {
-  CUtensorMap q, k, v, q8, o;
+  CUtensorMap q, k, v, q8, o, k64;
 };
 // Persistent forward over the scheduler's work units; one CTA per SM.
 cudaError_t launch_fwd_d64(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
@@ -42,6 +44,12 @@ cudaError_t launch_fwd_d256(const FwdMaps& m, const FwdParams& p, bool bf16, boo
 // hdim_qk 96 with hdim_v 96 or 64
 cudaError_t launch_fwd_d96(const FwdMaps& m, const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
                            cudaStream_t stream);
+// CTA pairs (hdim 128, no bias, in-kernel schedule: FwdParams::fused), on
+// 2 x clusters CTAs; fwd_pair_max_clusters_d128 gives how many clusters fit on
+// the device at once (0: none).
+int fwd_pair_max_clusters_d128(bool bf16, bool softmax);
+cudaError_t launch_fwd_pair_d128(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int clusters,
+                                 cudaStream_t stream);
 // with a relative attention bias (FwdParams::ts_q / rab_time / rab_pos), hdim_qk == hdim_v
 cudaError_t launch_fwd_rab_d64(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
                                cudaStream_t stream);

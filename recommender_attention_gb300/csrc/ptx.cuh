@@ -370,6 +370,149 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- CTA pair (cluster of two)
+// A pair of CTAs on one TPC shares each tcgen05.mma of cta_group::2: the MMA
+// is issued by one thread of the even CTA, its M = 256 rows are A's 128 rows in
+// each CTA's shared memory (or TMEM), its N columns are split in halves between
+// the two CTAs' shared memory (the same offsets in both), and each CTA's TMEM
+// receives its own 128 rows of D.  Every tcgen05 instruction of such a kernel
+// names cta_group::2, allocation included (one warp of each CTA, together).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// All threads of both CTAs (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of shared::cta address `saddr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of any CTA of the cluster (release at cluster scope:
+// the arriving thread's prior memory writes are visible to a thread of either
+// CTA that observes the phase with an acquire at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Arrive on an mbarrier of any CTA of the cluster with the default (CTA-scope)
+// release: no cluster-wide fence.  For hand-offs of tensor-core state (TMEM
+// written or read, ordered by tcgen05.fence::before_thread_sync before the
+// arrival), not of data in memory.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok;
+}
+// mbar_wait for a barrier that the other CTA arrives on (acquire at cluster
+// scope, so its writes before the arrival are visible).  Time-bounded.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+// 2-D tiled load into this CTA's shared memory whose completion (bytes) is
+// counted on an mbarrier of either CTA of the pair (a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* map, uint32_t bar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(map), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Eight pair MMAs, A and B in shared memory (as umma_ss_x8).
+__device__ __forceinline__ void umma_ss_x8_pair(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, Q;\n\tsetp.ne.b32 P, %18, 0;\n\tsetp.eq.b32 Q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %9, %17, P;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %2, %10, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %3, %11, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %4, %12, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %5, %13, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %6, %14, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %7, %15, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %8, %16, %17, Q;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Eight pair MMAs, A in TMEM (columns a[k], the same in both CTAs) and B in shared memory.
+__device__ __forceinline__ void umma_ts_x8_pair(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, Q;\n\tsetp.ne.b32 P, %18, 0;\n\tsetp.eq.b32 Q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %9, %17, P;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%2], %10, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%3], %11, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%4], %12, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%5], %13, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%6], %14, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%7], %15, %17, Q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%8], %16, %17, Q;\n\t"
+      "}\n" ::"r"(d_tmem),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+      "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on the mbarrier at shared::cta offset `bar` in each CTA of
+// `cta_mask` when every pair MMA issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4 bits 46-48 fixed 0b001

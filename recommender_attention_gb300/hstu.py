@@ -56,6 +56,7 @@ class FwdArgs(ctypes.Structure):
         ("kv_targets", ctypes.c_int32),
         ("timestamps_q", ctypes.c_void_p), ("timestamps_kv", ctypes.c_void_p),
         ("rab_time", ctypes.c_void_p), ("rab_pos", ctypes.c_void_p), ("rab_pos_buckets", ctypes.c_int32),
+        ("cta_pairs", ctypes.c_int32),
     ]
 
 
@@ -146,7 +147,8 @@ class HstuCall:
                  save_lse: bool = True, workspace: Optional[torch.Tensor] = None,
                  static_workspace: bool = False, kv_targets: bool = False,
                  timestamps_q: Optional[torch.Tensor] = None, timestamps_kv: Optional[torch.Tensor] = None,
-                 rab_time: Optional[torch.Tensor] = None, rab_pos: Optional[torch.Tensor] = None):
+                 rab_time: Optional[torch.Tensor] = None, rab_pos: Optional[torch.Tensor] = None,
+                 cta_pairs: int = 0):
         self.lib = load_library()
         if q.dtype not in DTYPE_CODES or k.dtype != q.dtype or v.dtype != q.dtype:
             raise TypeError("q, k, v must share a dtype, fp16 or bf16")
@@ -180,6 +182,7 @@ class HstuCall:
         a.timestamps_q, a.timestamps_kv = _ptr(timestamps_q), _ptr(timestamps_kv)
         a.rab_time, a.rab_pos = _ptr(rab_time), _ptr(rab_pos)
         a.rab_pos_buckets = 0 if rab_pos is None else rab_pos.shape[-1]
+        a.cta_pairs = int(cta_pairs)
         a.q_row_stride, a.k_row_stride = q.stride(0), k.stride(0)
         a.v_row_stride, a.o_row_stride = v.stride(0), out.stride(0)
         for t in (q, k, v, out):

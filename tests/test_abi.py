@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_strings_and_struct_layout(lib):
-    assert lib.hstu_abi_version() == 5
+    assert lib.hstu_abi_version() == 6
     for s in range(6):
         assert lib.hstu_status_string(s)
     assert lib.hstu_status_string(99) == b"unknown status"
@@ -64,7 +64,8 @@ def _ws(lib, a):
     ("num_groups", 3, 1), ("num_groups", 0, 1), ("num_splits", 17, 2), ("num_splits", -1, 1),
     ("q_row_stride", 100, 1), ("q_row_stride", 3, 1), ("total_kv", 999, 1), ("alpha", -1.0, 1),
     ("causal", 2, 1), ("max_seqlen_q", -5, 1),
-    ("kv_targets", 2, 1), ("kv_targets", 1, 1)])   # target keys on the key side need cross-attention
+    ("kv_targets", 2, 1), ("kv_targets", 1, 1),    # target keys on the key side need cross-attention
+    ("cta_pairs", 2, 1), ("cta_pairs", -2, 1), ("cta_pairs", 1, 0), ("cta_pairs", -1, 0)])
 def test_host_validation(lib, field, value, status):
     st, _ = _ws(lib, _args(**{field: value}))
     assert st == status
