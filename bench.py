@@ -199,7 +199,7 @@ def workload_config(w, allowed_pairs: int, world: int) -> dict:
 
 
 # ---------------------------------------------------------------- CUDA arm
-def device_call(w, q, k, v, device):
+def device_call(w, q, k, v, device, cta_pairs: int = 0):
     from recommender_attention_gb300.hstu import HstuCall
     off_q = torch.from_numpy(w.seq_offsets_q()).to(device)
     tg = torch.from_numpy(w.num_targets()).to(device)
@@ -208,7 +208,8 @@ def device_call(w, q, k, v, device):
                     causal=w.causal, local_len=list(w.local_len), context_len=list(w.context_len),
                     minfull_len=list(w.minfull_len), max_uih_len=list(w.max_uih_len),
                     num_groups=w.num_groups, softmax=w.softmax,
-                    max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()))
+                    max_seqlen_q=int(w.lengths_q().max()), max_seqlen_kv=int(w.lengths_kv().max()),
+                    cta_pairs=cta_pairs)
     return call, (dq, dk, dv, off_q, tg)
 
 
@@ -542,7 +543,7 @@ def run_cuda(args):
 
     w = rank_workload(rank, args.hdim)
     q, k, v = w.tensors()
-    call, dev = device_call(w, q, k, v, device)
+    call, dev = device_call(w, q, k, v, device, args.cta_pairs)
     st = call.stats(stream)
     if args.headline_only:
         # the headline call alone, warm-up then timed launches (for profiling
@@ -592,6 +593,15 @@ def run_cuda(args):
                           "fwd_kernel_ms": fw2, "fwd_kernel_tflops": f2 / (fw2 * 1e-3) / 1e12}
             del call2, dev2, q2, k2, v2
             torch.cuda.empty_cache()
+        # the same hdim 128 workload on the CTA-pair kernel (hstu_fwd_args::cta_pairs)
+        call2, dev2 = device_call(w, q, k, v, device, 1)
+        s2, fw2 = time_device_steps(call2, args.steps, args.warmup, world, stream)
+        s2 = reduce_max(s2, world, device)
+        tot2 = reduce_sum(flops_step, world, device)
+        extra["cta_pairs"] = {"value": tot2 / (s2 * 1e-3) / 1e12, "ms_per_step": s2, "fwd_kernel_ms": fw2,
+                              "fwd_kernel_tflops": flops_step / (fw2 * 1e-3) / 1e12}
+        del call2, dev2
+        torch.cuda.empty_cache()
 
     if args.hdim == 128 and not args.no_rab:
         peaks_r, _ = load_peaks()
@@ -825,7 +835,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--hdim", type=int, default=128, choices=[64, 128, 256])
-    ap.add_argument("--no-d256", action="store_true", help="skip the hdim 256, 96 and 96/64 repeats")
+    ap.add_argument("--no-d256", action="store_true",
+                    help="skip the hdim 256, 96 and 96/64 repeats and the CTA-pair repeat")
+    ap.add_argument("--cta-pairs", type=int, default=0, choices=[-1, 0, 1],
+                    help="forward kernel of the headline call (hstu_fwd_args::cta_pairs; for profiling)")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward lines")
     ap.add_argument("--no-rab", action="store_true", help="skip the relative attention bias lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
