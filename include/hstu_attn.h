@@ -128,8 +128,8 @@ typedef struct hstu_fwd_args {
    * position in key coordinates: i for a context row, i + (uih_kv - uih_q)
    * for UIH and target rows (the mask's bottom-right alignment).  Gaps are
    * exact unless the 128 keys of one key tile span 2^29 s (17 years) or
-   * more.  With a bias, hdim_qk ==
-   * hdim_v == 64 or 128; everything NULL / 0 = no bias. */
+   * more.  The bias works at every head-dimension pair the forward
+   * supports; everything NULL / 0 = no bias. */
   const int64_t* timestamps_q;    /* [dev] [total_q] seconds; required with rab_time */
   const int64_t* timestamps_kv;   /* [dev] [total_kv]; cross-attention with rab_time (NULL for
                                      self-attention, which uses timestamps_q) */
@@ -266,7 +266,7 @@ hstu_status hstu_attn_bwd_workspace_size(const hstu_bwd_args* args, size_t* byte
  *   softmax: p = exp(s - lse) masked  dv = c p^T g,  ds = p . (c g v^T - rowsum(g . o))
  *   both:    dq = alpha ds k,  dk = alpha ds^T q
  * Head dimensions: hdim_qk == hdim_v in {64, 96, 128}, or 96 with hdim_v 64
- * (others HSTU_ERR_UNSUPPORTED); with a bias, 64 or 128 as in the forward.
+ * (others HSTU_ERR_UNSUPPORTED), with or without a bias.
  * With a relative attention bias in fwd, s includes it and every gradient
  * flows through it; d_rab_time / d_rab_pos (when set) receive the tables'
  * gradients.

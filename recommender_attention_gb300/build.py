@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(LIB_DIR, "libhstu_attn.so")
 
 SOURCES = ["hstu_api.cu", "hstu_sched.cu", "hstu_fwd_d64.cu", "hstu_fwd_d96.cu", "hstu_fwd_d128.cu", "hstu_fwd_pair_d128.cu", "hstu_fwd_d256.cu",
            "hstu_static_ws.cu", "hstu_bwd_d64.cu", "hstu_bwd_d96.cu", "hstu_bwd_d128.cu",
-           "hstu_fwd_rab_d64.cu", "hstu_fwd_rab_d128.cu", "hstu_bwd_rab_d64.cu", "hstu_bwd_rab_d128.cu"]
+           "hstu_fwd_rab_d64.cu", "hstu_fwd_rab_d96.cu", "hstu_fwd_rab_d128.cu", "hstu_fwd_rab_d256.cu",
+           "hstu_bwd_rab_d64.cu", "hstu_bwd_rab_d96.cu", "hstu_bwd_rab_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I" + INCLUDE, "-I" + CSRC]

@@ -78,7 +78,6 @@ hstu_status validate(const hstu_fwd_args* a) {
   if (a->cta_pairs < -1 || a->cta_pairs > 1) return HSTU_ERR_INVALID_ARG;
   if (a->kv_targets && a->seq_offsets_kv == nullptr) return HSTU_ERR_INVALID_ARG;
   if (a->rab_time != nullptr || a->rab_pos != nullptr) {
-    if (a->hdim_v != a->hdim_qk || (a->hdim_qk != 64 && a->hdim_qk != 128)) return HSTU_ERR_UNSUPPORTED;
     if (a->rab_time != nullptr &&
         (a->timestamps_q == nullptr || (a->seq_offsets_kv != nullptr && a->timestamps_kv == nullptr)))
       return HSTU_ERR_INVALID_ARG;
@@ -428,8 +427,10 @@ hstu_status hstu_attn_fwd(const hstu_fwd_args* a, void* stream_ptr) {
     return HSTU_ERR_CUDA;
   cudaError_t e;
   if (pair_clusters > 0) e = launch_fwd_pair_d128(maps, fp, bf16, sm, pair_clusters, stream);
-  else if (rab) e = D == 64 ? launch_fwd_rab_d64(maps, fp, bf16, sm, grid, stream)
-                       : launch_fwd_rab_d128(maps, fp, bf16, sm, grid, stream);
+  else if (rab) e = D == 64  ? launch_fwd_rab_d64(maps, fp, bf16, sm, grid, stream)
+                  : D == 96  ? launch_fwd_rab_d96(maps, fp, a->hdim_v, bf16, sm, grid, stream)
+                  : D == 128 ? launch_fwd_rab_d128(maps, fp, bf16, sm, grid, stream)
+                             : launch_fwd_rab_d256(maps, fp, bf16, sm, grid, stream);
   else if (D == 64) e = launch_fwd_d64(maps, fp, bf16, sm, grid, stream);
   else if (D == 96) e = launch_fwd_d96(maps, fp, a->hdim_v, bf16, sm, grid, stream);
   else if (D == 128) e = launch_fwd_d128(maps, fp, bf16, sm, grid, stream);
@@ -623,7 +624,8 @@ hstu_status hstu_attn_bwd(const hstu_bwd_args* a, void* stream_ptr) {
   const int grid_kv = mk < sms ? (mk > 0 ? mk : 1) : sms;
   cudaError_t e;
   if (rab) e = D == 64 ? launch_bwd_rab_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream)
-                       : launch_bwd_rab_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
+               : D == 96 ? launch_bwd_rab_d96(maps, bw, f.hdim_v, bf16, f.softmax != 0, grid_q, grid_kv, stream)
+                         : launch_bwd_rab_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
   else if (D == 64) e = launch_bwd_d64(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);
   else if (D == 96) e = launch_bwd_d96(maps, bw, f.hdim_v, bf16, f.softmax != 0, grid_q, grid_kv, stream);
   else e = launch_bwd_d128(maps, bw, bf16, f.softmax != 0, grid_q, grid_kv, stream);

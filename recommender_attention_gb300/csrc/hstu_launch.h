@@ -50,10 +50,14 @@ cudaError_t launch_fwd_d96(const FwdMaps& m, const FwdParams& p, int hdim_v, boo
 int fwd_pair_max_clusters_d128(bool bf16, bool softmax);
 cudaError_t launch_fwd_pair_d128(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int clusters,
                                  cudaStream_t stream);
-// with a relative attention bias (FwdParams::ts_q / rab_time / rab_pos), hdim_qk == hdim_v
+// with a relative attention bias (FwdParams::ts_q / rab_time / rab_pos)
 cudaError_t launch_fwd_rab_d64(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
                                cudaStream_t stream);
+cudaError_t launch_fwd_rab_d96(const FwdMaps& m, const FwdParams& p, int hdim_v, bool bf16, bool softmax, int grid,
+                               cudaStream_t stream);
 cudaError_t launch_fwd_rab_d128(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
+                                cudaStream_t stream);
+cudaError_t launch_fwd_rab_d256(const FwdMaps& m, const FwdParams& p, bool bf16, bool softmax, int grid,
                                 cudaStream_t stream);
 // Tensor maps of the backward: 128-row boxes, and 8-row boxes for query tiles
 // whose rows come in two runs.
@@ -70,6 +74,8 @@ cudaError_t launch_bwd_d96(const BwdMaps& m, const BwdParams& p, int hdim_v, boo
                            int grid_kv, cudaStream_t stream);
 // with a relative attention bias (BwdParams::ts_q / rab_time / rab_pos)
 cudaError_t launch_bwd_rab_d64(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q,
+                               int grid_kv, cudaStream_t stream);
+cudaError_t launch_bwd_rab_d96(const BwdMaps& m, const BwdParams& p, int hdim_v, bool bf16, bool softmax, int grid_q,
                                int grid_kv, cudaStream_t stream);
 cudaError_t launch_bwd_rab_d128(const BwdMaps& m, const BwdParams& p, bool bf16, bool softmax, int grid_q,
                                 int grid_kv, cudaStream_t stream);

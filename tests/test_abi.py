@@ -118,10 +118,10 @@ def test_rab_host_validation(lib):
     assert _ws(lib, _args(rab_time=ctypes.cast(t, ctypes.c_void_p), timestamps_q=4096))[0] == 0
     assert _ws(lib, _args(rab_time=ctypes.cast(t, ctypes.c_void_p), timestamps_q=4096,
                           seq_offsets_kv=4096))[0] == 1
-    # bias kernels: hdim 64 and 128 with hdim_v == hdim_qk
-    for dqk, dv in ((96, 96), (96, 64), (256, 256)):
+    # the bias works at every head-dimension pair the forward supports, and no other
+    for dqk, dv, st in ((64, 64, 0), (96, 96, 0), (96, 64, 0), (128, 128, 0), (256, 256, 0), (128, 64, 2)):
         assert _ws(lib, _args(hdim_qk=dqk, hdim_v=dv, rab_pos=ctypes.cast(t, ctypes.c_void_p),
-                              rab_pos_buckets=4))[0] == 2
+                              rab_pos_buckets=4))[0] == st
     # the backward takes the same bias fields and checks
     b = _bwd()
     b.fwd.rab_pos = ctypes.cast(t, ctypes.c_void_p)
@@ -129,6 +129,11 @@ def test_rab_host_validation(lib):
     assert _bwd_ws(lib, b)[0] == 0
     b.fwd.rab_pos_buckets = 300
     assert _bwd_ws(lib, b)[0] == 1
+    # ... at the backward's head dimensions (no 256)
+    b.fwd.rab_pos_buckets = 4
+    for dqk, dv, st in ((96, 96, 0), (96, 64, 0), (256, 256, 2)):
+        b.fwd.hdim_qk, b.fwd.hdim_v = dqk, dv
+        assert _bwd_ws(lib, b)[0] == st
 
 
 def _bwd(**kw):

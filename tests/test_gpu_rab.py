@@ -48,6 +48,16 @@ def test_fuzz_rab(seed):
     check_rab(w, num_splits=[1, 2, 0][seed % 3])
 
 
+@pytest.mark.parametrize("dqk,dv", [(96, 96), (96, 64), (256, 256)])
+@pytest.mark.parametrize("softmax", [False, True])
+def test_rab_other_head_dims(dqk, dv, softmax):
+    """The bias at hdim 96, 96/64 and 256: the jagged validation case, and a
+    random case with a cross-attention key side and split-KV."""
+    check_rab(W.jagged_readme().with_(hdim_qk=dqk, hdim_v=dv, softmax=softmax, rab_pos_buckets=64))
+    w = W.random_small(300 + dqk + dv, hdim=dqk, hdim_v=dv, softmax=softmax, dtype="fp16", cross=True)
+    check_rab(w.with_(rab_pos_buckets=9), num_splits=2)
+
+
 @pytest.mark.parametrize("use_time,use_pos", [(True, False), (False, True)])
 @pytest.mark.parametrize("softmax", [False, True])
 def test_rab_one_term(use_time, use_pos, softmax):
