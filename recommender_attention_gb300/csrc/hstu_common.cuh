@@ -222,7 +222,8 @@ HSTU_HD void tile_range_swap_if(int& alo, int& ahi, int& blo, int& bhi) {
   }
 }
 
-HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, const QLayout& L, int m) {
+// b: q_tile_bounds(s, L, m), when the caller has it already.
+HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, const QLayout& L, int m, const TileBounds& b) {
   int i0, i1, c0, c1;   // [i0, i1): the run that may hold target rows
   q_tile_runs(s, L, m, i0, i1, c0, c1);
   TileSet t;
@@ -231,7 +232,6 @@ HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, const QLayout& L, int m) {
     t.lo0 = 0;
     t.hi0 = (s.c + kBlockN - 1) / kBlockN;
   }
-  const TileBounds b = q_tile_bounds(s, L, m);
   if (b.HI > b.LO) {
     t.lo1 = b.LO / kBlockN;
     t.hi1 = (b.HI + kBlockN - 1) / kBlockN;
@@ -267,6 +267,9 @@ HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, const QLayout& L, int m) {
   }
   t.count = (t.hi0 - t.lo0) + (t.hi1 - t.lo1) + (t.hi2 - t.lo2);
   return t;
+}
+HSTU_HD TileSet query_tile_kv_tiles(const SeqGeom& s, const QLayout& L, int m) {
+  return query_tile_kv_tiles(s, L, m, q_tile_bounds(s, L, m));
 }
 
 // The k-th tile (0-based) of a tile set.

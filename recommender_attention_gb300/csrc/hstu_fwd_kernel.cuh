@@ -159,8 +159,8 @@ __device__ __forceinline__ UnitView decode_unit(const FwdParams& p, int unit) {
   u.s = make_geom(p.off_q, p.off_kv, p.targets, b, p.ctx[u.g], p.loc[u.g], p.mf[u.g], p.causal,
                   p.self_attn, p.kv_targets);
   u.L = q_layout(u.s);
-  u.ts = query_tile_kv_tiles(u.s, u.L, u.m);
   u.tb = q_tile_bounds(u.s, u.L, u.m);
+  u.ts = query_tile_kv_tiles(u.s, u.L, u.m, u.tb);
   split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);
   u.scale = p.group_scale[u.g];
   return u;
@@ -321,8 +321,8 @@ __device__ __forceinline__ UnitView decode_fused_unit(const FwdParams& p, const 
   const int rem = local - u.h * per_h;
   u.m = u.L.nq - 1 - rem / p.splits;
   u.sp = rem % p.splits;
-  u.ts = query_tile_kv_tiles(u.s, u.L, u.m);
   u.tb = q_tile_bounds(u.s, u.L, u.m);
+  u.ts = query_tile_kv_tiles(u.s, u.L, u.m, u.tb);
   split_range(u.ts.count, u.sp, p.splits, u.k0, u.k1);
   u.scale = ctl.f_pscale[pos];
   return u;

@@ -151,17 +151,19 @@ __device__ __forceinline__ void decode_pair_unit(const FwdParams& p, const PairS
   const int pi = rem / p.splits;
   u.sp = rem - pi * p.splits;
   const int m0 = u.L.nq - 1 - 2 * pi, m1 = m0 - 1;
-  TileSet ts = query_tile_kv_tiles(u.s, u.L, m0);
-  if (m1 >= 0) ts = tileset_union(ts, query_tile_kv_tiles(u.s, u.L, m1));
+  const TileBounds tb0 = q_tile_bounds(u.s, u.L, m0);
+  const TileBounds tb1 = m1 >= 0 ? q_tile_bounds(u.s, u.L, m1) : tb0;
+  TileSet ts = query_tile_kv_tiles(u.s, u.L, m0, tb0);
+  if (m1 >= 0) ts = tileset_union(ts, query_tile_kv_tiles(u.s, u.L, m1, tb1));
   u.ts = ts;
   split_range(ts.count, u.sp, p.splits, u.k0, u.k1);
   u.scale = ctl.f_pscale[pos];
   even.u = u;
   even.u.m = m0;
-  even.u.tb = q_tile_bounds(u.s, u.L, m0);
+  even.u.tb = tb0;
   odd.u = u;
   odd.u.m = m1;
-  odd.u.tb = m1 >= 0 ? q_tile_bounds(u.s, u.L, m1) : even.u.tb;
+  odd.u.tb = tb1;
   even.live = odd.live = 1;
   even.peer_rows = m1 >= 0 ? 1 : 0;
   odd.peer_rows = 1;
