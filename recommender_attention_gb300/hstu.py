@@ -135,6 +135,22 @@ def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
     return s.cuda_stream
 
 
+def _capture(launch) -> "torch.cuda.CUDAGraph":
+    """A CUDA graph of one call: `launch(stream)` enqueues the call's kernels
+    (the header reset or scheduler, the forward or the two gradient kernels,
+    the combine) on a capture stream; replaying the graph repeats them on the
+    same buffers without the host work of a call (argument checks, tensor-map
+    encoding, launches).  The library's kernels are launched with plain stream
+    semantics and programmatic dependencies, which capture keeps."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        launch(side)
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
 class HstuCall:
     """One marshalled call: keeps the ctypes arrays alive alongside the args."""
 
@@ -225,6 +241,11 @@ class HstuCall:
         if st != HSTU_OK:
             raise HstuError(st, "hstu_attn_fwd")
 
+    def graph(self) -> "torch.cuda.CUDAGraph":
+        """This call captured as a CUDA graph (``graph.replay()`` reruns it on
+        the same buffers: inputs updated in place are read again)."""
+        return _capture(self.launch)
+
     def launch_static_ws(self, stream: Optional[torch.cuda.Stream] = None) -> None:
         """Enqueues the forward through ``hstu_attn_fwd_static_ws`` (library scratch)."""
         used = ctypes.c_void_p(0)
@@ -307,6 +328,10 @@ class HstuBwdCall:
         st = self.lib.hstu_attn_bwd(ctypes.byref(self.args), ctypes.c_void_p(_stream_handle(stream)))
         if st != HSTU_OK:
             raise HstuError(st, "hstu_attn_bwd")
+
+    def graph(self) -> "torch.cuda.CUDAGraph":
+        """This call captured as a CUDA graph (see HstuCall.graph)."""
+        return _capture(self.launch)
 
     def check(self, stream: Optional[torch.cuda.Stream] = None) -> int:
         err = ctypes.c_int32(0)
