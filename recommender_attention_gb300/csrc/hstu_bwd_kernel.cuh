@@ -51,30 +51,51 @@ struct BwdCfg {
   static constexpr int CHUNK = kBlockN * 128;   // one 128-row x 128-byte swizzle box
   static constexpr int TQ = KCH * CHUNK;        // a Q or K tile
   static constexpr int TV = VCH * CHUNK;        // a V or dO tile
-  static constexpr int STAGES = 2;
+  static constexpr int STAGES = 2;             // dK/dV kernel: the Q + dO ring
   static constexpr int RAB_OFFSET = (TQ + TV) * (1 + STAGES);   // relative attention bias tables, per warp
   // then, per elementwise warp, the gradients of the bias tables over a unit (dQ kernel)
   static constexpr int RAB_GRAD_OFFSET = RAB_OFFSET + (RAB ? 8 * static_cast<int>(sizeof(RabWarp)) : 0);
   static constexpr int SMEM_BYTES = RAB_GRAD_OFFSET + (RAB ? 8 * static_cast<int>(sizeof(RabGradWarp)) : 0) + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t ACC = 256;          // first accumulator column
+  static constexpr uint32_t ACC = 256;          // first accumulator column (dK/dV kernel)
   static_assert(D % 32 == 0 && DV % 32 == 0 && ACC + D + DV <= TMEM_COLS, "backward head dimensions");
+  // dQ kernel: the dQ product of half tile i is issued after the score
+  // products of half tile i + DQ_LAG, so the elementwise pass of a half tile
+  // has DQ_LAG half tiles of tensor work to hide behind.  That takes
+  // DQ_LAG + 1 score buffers in TMEM and DQ_LAG + 1 stages in the K ring (K
+  // feeds the dQ product too); V, read by the score products only, has a ring
+  // of its own.  With the bias, whose tables take the third K stage's room,
+  // DQ_LAG is 1.
+  static constexpr int DQ_LAG = RAB ? 1 : 2;
+  static constexpr int DQ_BUFS = DQ_LAG + 1;
+  static constexpr int DQ_KST = DQ_LAG + 1;
+  static constexpr int DQ_VST = 2;
+  static constexpr uint32_t DQ_ACC = 128u * DQ_BUFS;   // dQ accumulator's first column
+  static constexpr int DQ_TILES_BYTES = TQ + TV + DQ_KST * TQ + DQ_VST * TV;
+  static constexpr int DQ_SMEM_BYTES = RAB ? SMEM_BYTES : DQ_TILES_BYTES + 1024;
+  static_assert(DQ_ACC + D <= TMEM_COLS && DQ_BUFS <= 3, "dQ kernel TMEM");
+  static_assert(!RAB || DQ_TILES_BYTES == RAB_OFFSET, "the bias tables follow the dQ kernel's rings");
 };
 
 constexpr int kBwdEwWarps = 8;
 
 struct BwdCtl {
   uint64_t one_full, one_empty;           // dQ kernel: Q + dO of the unit; dK/dV kernel: K + V
-  uint64_t ring_full[2], ring_empty[2];   // dQ kernel: K + V per key tile; dK/dV kernel: Q + dO
-  uint64_t s_full[2], p_full[2];          // per TMEM buffer: score products ready / 16-bit operands written
+  uint64_t ring_full[2], ring_empty[2];   // dK/dV kernel: Q + dO per query tile
+  uint64_t k_full[3], k_empty[3];         // dQ kernel: K per key tile
+  uint64_t v_full[2], v_empty[2];         // dQ kernel: V per key tile
+  uint64_t s_full[3], p_full[3];          // per TMEM buffer: score products ready / 16-bit operands written
   uint64_t acc_full, acc_empty;           // accumulators complete / read out
   uint64_t sched_full[2], sched_empty[2];   // claimed units: published by the producer / taken by all
   int sched[2];                             // unit index, or -1 after the last
   uint32_t tmem_base;
   volatile int abort_flag;
-  // dK/dV elementwise warps: per warp, its 32 query columns' softmax
-  // statistics (lse in log2 units, delta / attn_scale) and allowed key
-  // intervals (lo, hi, diagonal key), read back as broadcasts
+};
+
+// dK/dV elementwise warps: per warp, its 32 query columns' softmax statistics
+// (lse in log2 units, delta / attn_scale) and allowed key intervals (lo, hi,
+// diagonal key), read back as broadcasts
+struct BwdColInfo {
   int4 col_rng[kBwdEwWarps][32];
   alignas(16) float2 col_stat[kBwdEwWarps][32];   // read two columns at a time as float4
 };
@@ -295,6 +316,12 @@ __device__ __forceinline__ void bwd_init(BwdCtl& ctl, int tid, int warp) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&ctl.ring_full[i], 1);
       ptx::mbar_init(&ctl.ring_empty[i], 1);
+      ptx::mbar_init(&ctl.v_full[i], 1);
+      ptx::mbar_init(&ctl.v_empty[i], 1);
+    }
+    for (int i = 0; i < 3; ++i) {
+      ptx::mbar_init(&ctl.k_full[i], 1);
+      ptx::mbar_init(&ctl.k_empty[i], 1);
       ptx::mbar_init(&ctl.s_full[i], 1);
       ptx::mbar_init(&ctl.p_full[i], kEwThreads);
     }
@@ -334,10 +361,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                    // Q then dO of the unit's query tile
   uint8_t* sDO = smem + Cfg::TQ;
-  uint8_t* sKV = sDO + Cfg::TV;          // ring: K then V of a key tile per stage
+  uint8_t* sK = sDO + Cfg::TV;           // K ring (DQ_KST stages), then the V ring (DQ_VST)
+  uint8_t* sV = sK + Cfg::DQ_KST * Cfg::TQ;
+  constexpr int NB = Cfg::DQ_BUFS, KST = Cfg::DQ_KST, VST = Cfg::DQ_VST, LAG = Cfg::DQ_LAG;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   bwd_init(ctl, tid, warp);
-  const uint32_t tmem = ctl.tmem_base;   // buffers [0, 256), dQ [256, 256 + D)
+  const uint32_t tmem = ctl.tmem_base;   // score buffers [0, 128 NB), dQ [128 NB, 128 NB + D)
   ptx::grid_dependency_wait();
   const int n_units = p.ws_header[kWsUnits];
 
@@ -357,15 +386,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           load_query_tile(&tm_do, &tm_do8, sDO, &ctl.one_full, u.s, u.L, u.t, u.h * DV, Cfg::VCH);
           ++one_it;
           for (int k = 0; k < ts.count; ++k) {
-            const int st = kv_it & 1;
-            if (!bwd_wait(ctl, p, &ctl.ring_empty[st], ((kv_it >> 1) & 1) ^ 1)) { ok = false; break; }
+            const int ks = kv_it % KST, vs = kv_it % VST;
             const int krow = u.s.kv0 + tileset_at(ts, k) * kBlockN;
-            uint8_t* dst = sKV + st * (Cfg::TQ + Cfg::TV);
-            ptx::mbar_arrive_expect_tx(&ctl.ring_full[st], Cfg::TQ + Cfg::TV);
+            if (!bwd_wait(ctl, p, &ctl.k_empty[ks], ((kv_it / KST) & 1) ^ 1)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(&ctl.k_full[ks], Cfg::TQ);
             for (int kc = 0; kc < Cfg::KCH; ++kc)
-              ptx::tma_load_2d(dst + kc * Cfg::CHUNK, &tm_k, &ctl.ring_full[st], u.h * D + kc * 64, krow);
+              ptx::tma_load_2d(sK + ks * Cfg::TQ + kc * Cfg::CHUNK, &tm_k, &ctl.k_full[ks], u.h * D + kc * 64, krow);
+            if (!bwd_wait(ctl, p, &ctl.v_empty[vs], ((kv_it / VST) & 1) ^ 1)) { ok = false; break; }
+            ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], Cfg::TV);
             for (int kc = 0; kc < Cfg::VCH; ++kc)
-              ptx::tma_load_2d(dst + Cfg::TQ + kc * Cfg::CHUNK, &tm_v, &ctl.ring_full[st], u.h * DV + kc * 64,
+              ptx::tma_load_2d(sV + vs * Cfg::TV + kc * Cfg::CHUNK, &tm_v, &ctl.v_full[vs], u.h * DV + kc * 64,
                                krow);
             ++kv_it;
           }
@@ -388,12 +418,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Half tile i of the unit (key tile i / 2, rows 64 (i % 2) of it) goes to
-    // buffer t & 1.  Its score products are issued before the dQ product of
-    // half tile i - 1, so the elementwise warps find the next scores ready.
+    // buffer t % NB.  Its score products are issued before the dQ product of
+    // half tile i - LAG, so the elementwise warps find the next scores ready
+    // and the tensor pipe has LAG half tiles of work queued behind them.
     const bool leader = ptx::elect_one_sync();
     constexpr uint32_t idesc_s = ptx::idesc_f16_f32acc(BF16, false, kBlockM, kHalf);
     constexpr uint32_t idesc_dq = ptx::idesc_f16_f32acc(BF16, true, kBlockM, D);
-    const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sDO), kv_base = ptx::smem_u32(sKV);
+    const uint32_t q_base = ptx::smem_u32(sQ), do_base = ptx::smem_u32(sDO);
+    const uint32_t k_ring = ptx::smem_u32(sK), v_ring = ptx::smem_u32(sV);
     int s_it = 0, one_it = 0, kv_it = 0, t_it = 0, u_it = 0, ui = -1;
     bool ok = true;
     while (ok && !ctl.abort_flag) {
@@ -406,38 +438,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int n_sub = 2 * nt;
       // dQ += dS K for half tile i (TMEM buffer of half tile t)
       auto dq_step = [&](int i, int t) -> bool {
-        const int b = t & 1, kt = kv_it + (i >> 1), st = kt & 1, hh = i & 1;
-        if (!bwd_warp_wait(ctl, p, &ctl.p_full[b], (t >> 1) & 1)) return false;
+        const int b = t % NB, kt = kv_it + (i >> 1), ks = kt % KST, hh = i & 1;
+        if (!bwd_warp_wait(ctl, p, &ctl.p_full[b], (t / NB) & 1)) return false;
         ptx::tc_fence_after();
         if (i == 0) {
           if (!bwd_warp_wait(ctl, p, &ctl.acc_empty, (u_it & 1) ^ 1)) return false;
           ptx::tc_fence_after();
         }
         if (leader) {
-          const uint32_t k_base = kv_base + st * (Cfg::TQ + Cfg::TV) + hh * kHalfBytes;
-          mma_half_ts(tmem + Cfg::ACC, tmem + 128 * b, k_base, idesc_dq, i > 0);
-          if (hh == 1) ptx::umma_commit(&ctl.ring_empty[st]);
+          const uint32_t k_base = k_ring + ks * Cfg::TQ + hh * kHalfBytes;
+          mma_half_ts(tmem + Cfg::DQ_ACC, tmem + 128 * b, k_base, idesc_dq, i > 0);
+          if (hh == 1) ptx::umma_commit(&ctl.k_empty[ks]);   // the key tile's last read
         }
         __syncwarp();
         return true;
       };
       for (int i = 0; i < n_sub && ok; ++i) {
-        const int t = t_it + i, b = t & 1, kt = kv_it + (i >> 1), st = kt & 1, hh = i & 1;
+        const int t = t_it + i, b = t % NB, kt = kv_it + (i >> 1), ks = kt % KST, vs = kt % VST, hh = i & 1;
         if (hh == 0) {
-          if (!bwd_warp_wait(ctl, p, &ctl.ring_full[st], (kt >> 1) & 1)) { ok = false; break; }
+          if (!bwd_warp_wait(ctl, p, &ctl.k_full[ks], (kt / KST) & 1)) { ok = false; break; }
+          if (!bwd_warp_wait(ctl, p, &ctl.v_full[vs], (kt / VST) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
         }
         if (leader) {
-          const uint32_t k_base = kv_base + st * (Cfg::TQ + Cfg::TV) + hh * kHalfBytes;
-          mma_scores<D / 16>(tmem + 128 * b, q_base, k_base, idesc_s);                 // S = Q K_h^T
-          mma_scores<DV / 16>(tmem + 128 * b + 64, do_base, k_base + Cfg::TQ, idesc_s);  // dP = dO V_h^T
+          const uint32_t k_base = k_ring + ks * Cfg::TQ + hh * kHalfBytes;
+          const uint32_t v_base = v_ring + vs * Cfg::TV + hh * kHalfBytes;
+          mma_scores<D / 16>(tmem + 128 * b, q_base, k_base, idesc_s);         // S = Q K_h^T
+          mma_scores<DV / 16>(tmem + 128 * b + 64, do_base, v_base, idesc_s);  // dP = dO V_h^T
+          if (hh == 1) ptx::umma_commit(&ctl.v_empty[vs]);          // V is read by dP only
           if (i == n_sub - 1) ptx::umma_commit(&ctl.one_empty);   // Q and dO are no longer read
           ptx::umma_commit(&ctl.s_full[b]);
         }
         __syncwarp();
-        if (i > 0 && !dq_step(i - 1, t - 1)) { ok = false; break; }
+        if (i >= LAG && !dq_step(i - LAG, t - LAG)) { ok = false; break; }
       }
-      if (!ok || !dq_step(n_sub - 1, t_it + n_sub - 1)) break;
+      if (!ok) break;
+      for (int i = n_sub > LAG ? n_sub - LAG : 0; i < n_sub && ok; ++i)
+        if (!dq_step(i, t_it + i)) ok = false;
+      if (!ok) break;
       if (leader) ptx::umma_commit(&ctl.acc_full);
       __syncwarp();
       t_it += n_sub;
@@ -536,10 +574,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         rm.diag = r_diag >= 0 ? r_diag - j0 : -1000000;
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
-          const int t = t_it++, b = t & 1;
+          const int t = t_it++, b = t % NB;
           const uint32_t sb = tmem + lane_base + 128 * b + 32 * wg;
           const uint32_t mb = full ? 0xFFFFFFFFu : rm.bits32(kHalf * hh + 32 * wg);
-          if (!bwd_warp_wait(ctl, p, &ctl.s_full[b], (t >> 1) & 1)) { ok = false; break; }
+          if (!bwd_warp_wait(ctl, p, &ctl.s_full[b], (t / NB) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
           uint32_t sv[32], dv[32], pk[16];
           ptx::tmem_ld32(sb, sv);
@@ -621,7 +659,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < D / 2; c += 16) {   // 16 columns at a time (hdim 96: 48 per warpgroup)
         uint32_t o[16];
-        ptx::tmem_ld16(tmem + lane_base + Cfg::ACC + wg * (D / 2) + c, o);
+        ptx::tmem_ld16(tmem + lane_base + Cfg::DQ_ACC + wg * (D / 2) + c, o);
         ptx::tmem_ld_wait(o);
         if (valid) {
           uint32_t q2[8];
@@ -654,6 +692,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using Cfg = BwdCfg<D, DV, RAB>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdCtl ctl;
+  __shared__ BwdColInfo cinfo;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sK = smem;                    // K then V of the unit's key tile
@@ -788,7 +827,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float alpha = p.alpha;
     const float half_alpha = 0.5f * p.alpha;
     constexpr float kLog2e = 1.4426950408889634f;
-    const float4* stat4 = reinterpret_cast<const float4*>(&ctl.col_stat[ew][0]);
+    const float4* stat4 = reinterpret_cast<const float4*>(&cinfo.col_stat[ew][0]);
     int s_it = 0, t_it = 0, a_it = 0, ui = -1;
     bool ok = true;
     while (ok && !ctl.abort_flag) {
@@ -847,7 +886,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 row_uih_keys(u.s, qi, lo, hi);
                 dg = row_diag_key(u.s, qi);
               }
-              ctl.col_rng[ew][lane] = make_int4(lo, hi, dg, 0);
+              cinfo.col_rng[ew][lane] = make_int4(lo, hi, dg, 0);
             }
             int c_ts = 0;   // bias: this lane's column's timestamp
             if constexpr (RAB) {
@@ -860,7 +899,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 l2 = p.lse[gq] * kLog2e;
                 dl = p.delta[gq] / u.scale;
               }
-              ctl.col_stat[ew][lane] = make_float2(l2, dl);
+              cinfo.col_stat[ew][lane] = make_float2(l2, dl);
             }
             __syncwarp();
             uint32_t allow = cvalid;
@@ -868,7 +907,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               uint32_t seen = 0u;
 #pragma unroll
               for (int kk = 0; kk < 32; ++kk) {
-                const int4 r = ctl.col_rng[ew][kk];
+                const int4 r = cinfo.col_rng[ew][kk];
                 seen |= static_cast<uint32_t>((j >= r.x && j < r.y) || j == r.z) << kk;
               }
               allow &= seen;
@@ -955,17 +994,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // Host side: both backward kernels of one head dimension, the dQ kernel first.
 template <int D, int DV, bool BF16, bool SOFTMAX, bool RAB>
 cudaError_t launch_bwd_pair(const BwdMaps& m, const BwdParams& p, int grid_q, int grid_kv, cudaStream_t stream) {
-  constexpr int smem = BwdCfg<D, DV, RAB>::SMEM_BYTES;
+  constexpr int smem = BwdCfg<D, DV, RAB>::SMEM_BYTES;        // dK/dV kernel
+  constexpr int smem_q = BwdCfg<D, DV, RAB>::DQ_SMEM_BYTES;   // dQ kernel
   // the dQ kernel that also sums the bias tables' gradients, when they are asked for
   const bool grad = RAB && (p.d_rab_time != nullptr || p.d_rab_pos != nullptr);
   auto kq = grad ? hstu_bwd_dq_kernel<D, DV, BF16, SOFTMAX, RAB, RAB> : hstu_bwd_dq_kernel<D, DV, BF16, SOFTMAX, RAB>;
   auto kkv = hstu_bwd_dkdv_kernel<D, DV, BF16, SOFTMAX, RAB>;
-  static_assert(smem + sizeof(BwdCtl) <= 232448, "shared memory over the 227 KB a CTA may use");
+  static_assert(smem + sizeof(BwdCtl) + sizeof(BwdColInfo) <= 232448, "shared memory over the 227 KB a CTA may use");
+  static_assert(smem_q + sizeof(BwdCtl) <= 232448, "shared memory over the 227 KB a CTA may use");
   static std::atomic<unsigned long long> q_attr_set{0}, qg_attr_set{0}, kv_attr_set{0};
-  cudaError_t e = ensure_smem_attr(kq, smem, grad ? qg_attr_set : q_attr_set);
+  cudaError_t e = ensure_smem_attr(kq, smem_q, grad ? qg_attr_set : q_attr_set);
   if (e == cudaSuccess) e = ensure_smem_attr(kkv, smem, kv_attr_set);
   if (e != cudaSuccess) return e;
-  kq<<<grid_q, kBwdThreads, smem, stream>>>(m.q, m.k, m.v, m.d_o, m.q8, m.d_o8, p);
+  kq<<<grid_q, kBwdThreads, smem_q, stream>>>(m.q, m.k, m.v, m.d_o, m.q8, m.d_o8, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   kkv<<<grid_kv, kBwdThreads, smem, stream>>>(m.q, m.k, m.v, m.d_o, m.q8, m.d_o8, p);
