@@ -14,13 +14,15 @@
 // units from a global counter, longest first, and publishes them to the other
 // roles through a two-slot ring), one MMA warp (the whole warp runs the loop,
 // one elected lane issues) and two elementwise warpgroups.  Work goes in half
-// tiles of 64 columns with two TMEM buffers, so the tensor core computes the
-// next half tile's score products while the elementwise warps process the
-// current one:
+// tiles of 64 columns with two or three TMEM buffers, so the tensor core
+// computes the next half tiles' score products while the elementwise warps
+// process the current one:
 //   dQ kernel, one unit per (sequence, head, query tile): for every key tile of
 //     the tile's set and each half of it, S = Q K_h^T and dP = dO V_h^T (N = 64)
-//     into buffer (t & 1), dS (16-bit) packed over S, dQ += dS K_h with K read
-//     MN-major from its tile; the elementwise warps then scale dQ by alpha.
+//     into buffer t % (DQ_LAG + 1), dS (16-bit) packed over S, dQ += dS K_h
+//     with K read MN-major from its tile, issued DQ_LAG half tiles behind the
+//     score products (K and V in rings of their own); the elementwise warps
+//     then scale dQ by alpha.
 //   dK/dV kernel, one unit per (sequence, head, key tile): for every query tile
 //     whose key-tile set holds this key tile (a bit word per 32 query tiles,
 //     written by the scheduler) and each half of it, S^T = K Q_h^T and
@@ -28,7 +30,8 @@
 //     dK += dS^T Q_h with dO and Q read MN-major; then dV * attn_scale and
 //     dK * alpha.
 // TMEM: buffer b at columns [128 b, 128 b + 128) (scores, then the score
-// gradients at +64), accumulators from column 256.  Query tiles follow the
+// gradients at +64), accumulators after the buffers (dQ kernel: from column
+// 128 (DQ_LAG + 1); dK/dV kernel: from column 256).  Query tiles follow the
 // forward's layout (q_layout): context rows may sit on the top lanes of a
 // sequence's last query tile, and that tile's Q and dO then arrive as 8-row
 // TMA boxes.  Every wait is bounded (2 s); a timeout sets the device error word
