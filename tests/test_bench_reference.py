@@ -33,3 +33,17 @@ def test_reference_arm_line(monkeypatch):
     cfg = d["config"]
     assert cfg == bench.workload_config(w, cfg["allowed_pairs"], 1)
     assert 1.0e9 < cfg["allowed_pairs"] < 1.1e9
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch):
+    """Under torchrun only rank 0 runs the oracle and prints; rank 1 returns at
+    once, without output (and without loading the oracle)."""
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    called = []
+    monkeypatch.setattr(bench, "cpu_baseline", lambda *a, **k: called.append(1))
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-seconds", "4"])
+    assert out.getvalue() == "" and called == []
